@@ -1,0 +1,82 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case below plants one slip into a copy of the oracle's C source (a dropped
+term, a wrong sign or index, a transposed operand, a wrong rounding rule),
+compiles it on the CPU into a temporary directory, swaps it in, and runs the
+pin suite of tests/test_oracle_pins.py against it.  At least one pin must fail
+for every mutant; the real oracle passes them all (that file's own run).
+"""
+import inspect
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "gdn_oracle.c")
+
+# (name, original text, replacement) -- every original must occur exactly once.
+MUTANTS = [
+    ("dropped alpha in the correction", "beta * (v[a] - alpha * work[a])", "beta * (v[a] - work[a])"),
+    ("sign of the correction", "beta * (v[a] - alpha * work[a])", "beta * (v[a] + alpha * work[a])"),
+    ("transposed state in S k", "acc += S[(int64_t)a * d + b] * k[b];", "acc += S[(int64_t)b * d + a] * k[b];"),
+    ("outer product k v^T", "alpha * S[(int64_t)a * d + b] + r * k[b];",
+     "alpha * S[(int64_t)a * d + b] + beta * (v[b] - alpha * work[b]) * k[a];"),
+    ("repeat-interleaved key heads", "int g = h % nk;", "int g = h / (nv / nk);"),
+    ("missing 1/sqrt(D)", "o[a] = acc * scale;", "o[a] = acc;"),
+    ("read-out with k instead of q", "acc += S[(int64_t)a * d + b] * q[b];", "acc += S[(int64_t)a * d + b] * k[b];"),
+    ("decay not applied", "S[(int64_t)a * d + b] = alpha * S[(int64_t)a * d + b] + r * k[b];",
+     "S[(int64_t)a * d + b] = S[(int64_t)a * d + b] + r * k[b];"),
+    ("norm without the mean", "sqrt(ss / (double)d + eps)", "sqrt(ss + eps)"),
+    ("eps outside the root", "sqrt(ss / (double)d + eps)", "(sqrt(ss / (double)d) + eps)"),
+    ("sigmoid gate instead of silu", "double silu = zz / (1.0 + exp(-zz));", "double silu = 1.0 / (1.0 + exp(-zz));"),
+    ("no norm weight", "out[h * d + a] = (double)gn[a] * oh[a] / den * silu;", "out[h * d + a] = oh[a] / den * silu;"),
+    ("prefill reuses token 0 gates", "alpha + bt * nv, beta + bt * nv", "alpha + (int64_t)b * T * nv, beta + (int64_t)b * T * nv"),
+    ("round half up", "(rem == half && (n & 1u))", "(rem == half)"),
+    ("truncating rounding", "if (rem > half || (rem == half && (n & 1u))) n += 1;", "(void)half;"),
+    ("overflow saturates", "if (E > 15) return (uint16_t)(sign | 0x7c00u);", "if (E > 15) return (uint16_t)(sign | 0x7bffu);"),
+    ("widened subnormal exponent off by one", "int32_t E = -14;\n        while", "int32_t E = -15;\n        while"),
+    ("widening drops the sign", "return sign | (ex - 15u + 127u) << 23 | (fr << 13);", "return (ex - 15u + 127u) << 23 | (fr << 13);"),
+]
+
+
+def _pin_calls():
+    """Every pin function with each of its parametrisations."""
+    calls = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        marks = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
+        if not marks:
+            calls.append((name, fn, {}))
+            continue
+        m = marks[0]
+        argnames = [a.strip() for a in m.args[0].split(",")] if isinstance(m.args[0], str) else list(m.args[0])
+        for vals in m.args[1]:
+            vals = vals if isinstance(vals, (tuple, list)) else (vals,)
+            calls.append((name, fn, dict(zip(argnames, vals))))
+    return calls
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, tmp_path):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique/absent: {old!r}"
+    mut = tmp_path / "mut.c"
+    mut.write_text(src.replace(old, new))
+    so = tmp_path / "mut.so"
+    subprocess.check_call(["gcc", *oracle.CFLAGS, "-o", str(so), str(mut), "-lm"])
+    saved = oracle._load()
+    oracle._lib = oracle.bind(str(so))
+    failed = []
+    try:
+        for pname, fn, kw in _pin_calls():
+            try:
+                fn(**kw)
+            except AssertionError:
+                failed.append(pname)
+    finally:
+        oracle._lib = saved
+    assert failed, f"no pin caught the mutant '{name}'"
