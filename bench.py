@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated delta rule hot path on GB300.
+
+Default workload (the one the headline metric is quoted on): batched decode
+of all 48 GDN layers of one token -- batch 32, NK = 16 key heads, NV = 48 value
+heads (g = h mod 16), D = 128, fp32 state [32][48 layers][48][128][128]
+(4.83 GB, larger than L2), one fused decode + gated-RMS-norm launch per layer
+with its own seeded inputs, bf16 output.  One step = the 48 layer launches.
+
+value  = token-heads/s with inputs resident in HBM (device-timed, CUDA events).
+e2e    = the same through the public API with the step's token inputs copied
+         host->device from pinned memory and the bf16 outputs copied back
+         inside the timed region (the state stays resident, as it does in a
+         model).
+roofline = the decode kernel's algorithmic HBM bytes per launch / its average
+         launch time, against the measured HBM copy bandwidth.
+cpu_baseline = the fp64 oracle, as it stands, on this host's cores over a
+         bounded sample of the same workload.
+
+Other rows of the hot path are measured under "rows" (fp16 pool decode,
+h-state converters, single-layer latency, prefill).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs the per-GPU workload on its own GPU (weak
+scaling, no collective in the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN state-update token-heads/s and achieved HBM GB/s (% of GB300 peak)"
+UNIT = "token-heads/s"
+
+# The workload.
+B, NK, NV, D, LAYERS = 32, 16, 48, 128, 48
+EPS = 1e-6
+SEED = 0
+
+# Per-launch DRAM traffic of the decode kernel from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), valid only while the kernel source is the one it was taken on.
+NCU_TRAFFIC = {
+    "decode_norm_f32": {"bytes_per_launch": None, "src_sha256": None},
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "source": "measured", "sm_max_mhz": j.get("sm_max_mhz")}
+    return {"hbm_gbs": 6800.0, "source": "fallback", "sm_max_mhz": 2070.0}
+
+
+def src_sha(name):
+    p = os.path.join(ROOT, "gated_deltanet_linear_16_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gdn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons, pw = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ workload buffers
+
+def algorithmic_bytes_decode(batch, nk, nv, d, state_elem=4, norm=True):
+    """Bytes one decode launch must move at minimum: the state read and written once,
+    every token input read once, the output written once."""
+    state = batch * nv * d * d * state_elem * 2
+    qk = batch * nk * d * 4 * 2
+    v = batch * nv * d * 4
+    gb = batch * nv * 4 * 2
+    if norm:
+        z = batch * nv * d * 4
+        gn = d * 4
+        out = batch * nv * d * 2
+    else:
+        z = gn = 0
+        out = batch * nv * d * 4
+    return state + qk + v + gb + z + gn + out
+
+
+def make_layer_inputs(torch, batch, layers, dev):
+    """Seeded token inputs for every layer, resident on the device: dict of [L][...] tensors."""
+    import gdn_synth as gs
+    xs = [gs.decode_inputs(SEED, batch, NK, NV, D, layer=l) for l in range(layers)]
+    out = {}
+    for name in ("q", "k", "v", "z", "alpha", "beta"):
+        out[name] = torch.from_numpy(np.stack([x[name] for x in xs])).to(dev)
+    gn = np.stack([gs.norm_weight(SEED, D, layer=l) for l in range(layers)])
+    out["gn"] = torch.from_numpy(gn).to(dev)
+    return out
+
+
+def layer_launch(gdn, state, x, outb, l, stream_ptr, batch=B, f16=False, pitch=None):
+    """One fused decode + norm launch for layer l (state layout [batch][layer][NV][D][D])."""
+    esz = 2 if f16 else 4
+    pitch = LAYERS * NV * D * D if pitch is None else pitch
+    gdn.gdn_decode_norm(state.data_ptr() + l * NV * D * D * esz,
+                        x["q"][l], x["k"][l], x["v"][l], x["alpha"][l], x["beta"][l],
+                        x["z"][l], x["gn"][l], outb[l],
+                        batch=batch, nk=NK, nv=NV, d=D, eps=EPS, state_pitch=pitch,
+                        state_dtype=1 if f16 else 0, stream=stream_ptr)
+
+
+# ------------------------------------------------------------------ multi-rank host logic
+
+def max_over_ranks(ms_step, world, device):
+    """Slowest rank's time per step (every rank's work counts only once all finish)."""
+    if world <= 1:
+        return ms_step
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_step], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_step):
+    """Whole-job units per second: every rank processes its own units (weak scaling)."""
+    return world * units_per_rank / (ms_step / 1e3)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import gated_deltanet_linear_16_gb300 as gdn
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gdn.load()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    # state: [B][L][NV][D][D] fp32, N(0, 0.02), drawn on the device (values do not affect timing)
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED + rank)
+    state = torch.empty((B, LAYERS, NV, D, D), dtype=torch.float32, device=dev)
+    for b in range(B):
+        state[b].normal_(0.0, 0.02, generator=g)
+    x = make_layer_inputs(torch, B, LAYERS, dev)
+    outb = torch.empty((LAYERS, B, NV * D), dtype=torch.int16, device=dev)
+
+    def step():
+        for l in range(LAYERS):
+            layer_launch(gdn, state, x, outb, l, sp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    ms_step = max_over_ranks(ms / args.steps, world, dev)
+    clocks = clk.summary()
+
+    token_heads = B * NV * LAYERS
+    value = job_throughput(token_heads, world, ms_step)
+    bytes_launch = algorithmic_bytes_decode(B, NK, NV, D)
+    launch_s = ms_step / 1e3 / LAYERS
+    pk = peaks()
+    achieved = bytes_launch / launch_s / 1e9
+    tr = NCU_TRAFFIC["decode_norm_f32"]
+    traffic = tr["bytes_per_launch"] if tr["src_sha256"] == src_sha("gdn_decode.cu") else None
+
+    # ---- e2e: host inputs in pinned memory -> device, 48 launches, bf16 outputs -> host
+    e2e = run_e2e(args, torch, gdn, state, x, outb, dev, stream)
+
+    rows = {} if args.no_rows else run_rows(torch, gdn, dev, stream, pk)
+    cpu = None if (args.no_cpu or rank != 0) else cpu_baseline(sample_layers=None)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "batched decode + fused gated RMSNorm, all 48 GDN layers of one token",
+                   "batch_per_gpu": B, "global_batch": B * world, "nk": NK, "nv": NV, "d": D,
+                   "layers": LAYERS, "state": "fp32 [32][48][48][128][128] = 4.83 GB per GPU",
+                   "out": "bf16", "eps": EPS, "launches_per_step": LAYERS,
+                   "l2": "inputs larger than L2 (4.83 GB state per step vs 129 MB L2)",
+                   "parallelism": f"dp{world}"},
+        "roofline": {"bound": "hbm", "kernel": "decode_d128<float, norm>", "achieved": achieved,
+                     "peak": pk["hbm_gbs"], "peak_source": pk["source"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": bytes_launch, "launch_us": launch_s * 1e6},
+        "e2e": e2e,
+        "gpu_launches": LAYERS * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "rows": rows,
+    }
+    return line
+
+
+def run_e2e(args, torch, gdn, state, x, outb, dev, stream):
+    """Same workload through the public API with per-step host<->device copies."""
+    host = {k: v.cpu().pin_memory() for k, v in x.items() if k != "gn"}
+    dev_in = {k: torch.empty_like(v) for k, v in host.items()}
+    dev_in["gn"] = x["gn"]
+    host_out = torch.empty(outb.shape, dtype=outb.dtype).pin_memory()
+    sp = stream.cuda_stream
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        for l in range(LAYERS):
+            layer_launch(gdn, state, dev_in, outb, l, sp)
+        host_out.copy_(outb, non_blocking=True)
+
+    steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": B * NV * LAYERS / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ secondary rows
+
+def time_fn(torch, stream, fn, reps, warm=2):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps / 1e3     # seconds per call
+
+
+def run_rows(torch, gdn, dev, stream, pk):
+    import gdn_synth as gs
+    sp = stream.cuda_stream
+    rows = {}
+    torch.cuda.empty_cache()
+
+    # fp16 h-state pool: B=256 slots, pitch 48*128*128 + 4096 halves, 16 sequential decode steps.
+    PB, pitch = 256, NV * D * D + 4096
+    pool = torch.zeros(PB * pitch, dtype=torch.float16, device=dev)
+    pool.view(PB, pitch)[:, :NV * D * D].normal_(0.0, 0.02)
+    x = make_layer_inputs(torch, PB, 1, dev)
+    ob = torch.empty((1, PB, NV * D), dtype=torch.int16, device=dev)
+
+    def f16_step():
+        layer_launch(gdn, pool, x, ob, 0, sp, batch=PB, f16=True, pitch=pitch)
+
+    s = time_fn(torch, stream, f16_step, 16)
+    by = algorithmic_bytes_decode(PB, NK, NV, D, state_elem=2)
+    rows["fp16_pool_decode_norm"] = {
+        "config": "B=256 NK=16 NV=48 D=128, fp16 pool pitch 790528 halves, fused norm -> bf16",
+        "us_per_step": s * 1e6, "token_heads_per_s": PB * NV / s, "achieved_gbs": by / s / 1e9,
+        "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}
+
+    # converters on the whole pool (padding included): fp16 -> fp32 -> fp16
+    n = PB * pitch
+    f32 = torch.empty(n, dtype=torch.float32, device=dev)
+    back = torch.empty(n, dtype=torch.float16, device=dev)
+    s_up = time_fn(torch, stream, lambda: gdn.gdn_h_f16_to_f32(pool, f32, n, stream=sp), 10)
+    s_dn = time_fn(torch, stream, lambda: gdn.gdn_h_f32_to_f16(f32, back, n, stream=sp), 10)
+    rows["h_state_converters"] = {
+        "elements": n, "f16_to_f32_us": s_up * 1e6, "f32_to_f16_us": s_dn * 1e6,
+        "f16_to_f32_gbs": 6 * n / s_up / 1e9, "f32_to_f16_gbs": 6 * n / s_dn / 1e9,
+        "frac_of_hbm_peak": [6 * n / s_up / 1e9 / pk["hbm_gbs"], 6 * n / s_dn / 1e9 / pk["hbm_gbs"]],
+        "round_trip_identity": bool(torch.equal(back.view(torch.int16), pool.view(torch.int16)))}
+    del pool, f32, back, x, ob
+    torch.cuda.empty_cache()
+
+    # single layer, batch 1 (state 3 MB: L2-resident across steps): latency per step
+    st = torch.empty((1, NV, D, D), dtype=torch.float32, device=dev).normal_(0.0, 0.02)
+    x1 = make_layer_inputs(torch, 1, 1, dev)
+    o1 = torch.empty((1, 1, NV * D), dtype=torch.int16, device=dev)
+    s = time_fn(torch, stream, lambda: layer_launch(gdn, st, x1, o1, 0, sp, batch=1, pitch=NV * D * D), 256)
+    rows["single_layer_latency"] = {"config": "B=1 NK=16 NV=48 D=128 fp32, fused norm (L2-resident)",
+                                    "us_per_step": s * 1e6, "token_heads_per_s": NV / s}
+    del st, x1, o1
+
+    # prefill: B=8, T=4096 tokens in one call, fp32 state from zero
+    PB, T = 8, 4096
+    R = PB * T
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    q = torch.randn((R, NK * D), device=dev, generator=g)
+    k = torch.randn((R, NK * D), device=dev, generator=g)
+    q = (q.view(R, NK, D) / q.view(R, NK, D).norm(dim=-1, keepdim=True)).view(R, NK * D).contiguous()
+    k = (k.view(R, NK, D) / k.view(R, NK, D).norm(dim=-1, keepdim=True)).view(R, NK * D).contiguous()
+    v = torch.randn((R, NV * D), device=dev, generator=g)
+    a = torch.sigmoid(torch.randn((R, NV), device=dev, generator=g) + 2.0)
+    bt = torch.sigmoid(torch.randn((R, NV), device=dev, generator=g))
+    o = torch.empty((R, NV * D), device=dev)
+    S = torch.zeros((PB, NV, D, D), device=dev)
+
+    def pf():
+        gdn.gdn_prefill_seq(S, q, k, v, a, bt, o, batch=PB, seq_len=T, nk=NK, nv=NV, d=D, stream=sp)
+
+    s = time_fn(torch, stream, pf, 3, warm=1)
+    th = PB * NV * T
+    io = (2 * R * NK * D + 2 * R * NV * D + 2 * R * NV) * 4 + 2 * PB * NV * D * D * 4
+    flops_instr = th * D * D * 4        # u FMA, alpha*S, update FMA, o FMA per state element
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk = (pk.get("sm_max_mhz") or 2070.0) * 1e6
+    fp32_issue_peak = sms * 128 * clk   # FP32 lane-instructions per second
+    rows["prefill"] = {"config": "B=8 T=4096 NK=16 NV=48 D=128 fp32, state on chip",
+                       "ms": s * 1e3, "token_heads_per_s": th / s,
+                       "fp32_lane_instr_per_s": flops_instr / s, "fp32_issue_peak": fp32_issue_peak,
+                       "frac_of_fp32_issue_peak": flops_instr / s / fp32_issue_peak,
+                       "achieved_gbs": io / s / 1e9, "bound": "alu"}
+    del q, k, v, a, bt, o, S
+    torch.cuda.empty_cache()
+    return rows
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+
+def cpu_baseline(sample_layers=None, budget_s=8.0):
+    """Time the fp64 oracle on this host's cores over whole layers of the workload
+    (all 32 sequences x 48 heads of a layer per unit), until ~budget_s of wall time."""
+    import oracle
+    import gdn_synth as gs
+    threads = os.cpu_count() or 1
+    S0 = gs.state_heads(SEED, range(B), range(NV), D).astype(np.float64)
+    done_heads, spent, layers = 0, 0.0, 0
+    limit = sample_layers or LAYERS
+    while layers < limit and (sample_layers or spent < budget_s):
+        x = gs.decode_inputs(SEED, B, NK, NV, D, layer=layers)
+        gn = gs.norm_weight(SEED, D, layer=layers)
+        S = S0.copy()
+        chunks = [(b0, min(B, b0 + max(1, B // threads))) for b0 in range(0, B, max(1, B // threads))]
+
+        def unit(c):
+            b0, b1 = c
+            o = oracle.decode(S[b0:b1], x["q"][b0:b1], x["k"][b0:b1], x["v"][b0:b1],
+                              x["alpha"][b0:b1], x["beta"][b0:b1], NK)
+            return oracle.gated_rmsnorm(o.reshape(-1, D), x["z"][b0:b1].reshape(-1, D), gn, EPS)
+
+        t0 = time.perf_counter()
+        # S[b0:b1] is a contiguous view, so each thread updates its own slice in place
+        oracle.parallel_map(unit, chunks, threads=threads)
+        spent += time.perf_counter() - t0
+        done_heads += B * NV
+        layers += 1
+    return {"value": done_heads / spent, "unit": UNIT, "cores": min(threads, B), "kind": "oracle",
+            "seconds": spent,
+            "sample": f"{layers} of 48 layers x 32 sequences x 48 heads ({done_heads} token-heads), "
+                      f"fp64 C oracle, {min(threads, B)} host threads"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one whole layer of the workload."""
+    if rank != 0:
+        return None
+    per = []
+    for _ in range(args.warmup):
+        cpu_baseline(sample_layers=1)
+    t0 = time.perf_counter()
+    total = 0.0
+    for _ in range(args.steps):
+        r = cpu_baseline(sample_layers=1)
+        per.append(r)
+        total += r["seconds"]
+    wall = time.perf_counter() - t0
+    heads = args.steps * B * NV
+    value = heads / total
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "batched decode + fused gated RMSNorm, all 48 GDN layers of one token",
+                   "batch_per_gpu": B, "nk": NK, "nv": NV, "d": D, "layers": LAYERS,
+                   "step_sample": "one layer (32 sequences x 48 heads) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": per[0]["cores"] if per else None,
+                         "kind": "oracle", "sample": "one whole layer per step, fp64 C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+"""gated_deltanet_linear_16_gb300 -- GB300 (sm_103a) gated delta rule library.
+
+A thin Python binding over the C-ABI library ``libgdn.so`` (declared in
+``include/gdn.h``).  Every function here has the name of its C entry point and
+only marshals arguments: torch tensors (or raw integer device addresses) become
+pointers, sizes and strides are passed through, the current torch CUDA stream
+is the default stream.  Every step of the computation runs in libgdn's CUDA
+kernels; there is no CPU path.  A nonzero status raises :class:`GdnError`.
+
+The step (logicaffeine_compile/codegen_cuda/gdn.rs, kernel ``gdn_step``), per
+sequence, value head h (key head g = h mod NK) and state row a:
+``S[a] <- alpha S[a] + beta (v[a] - alpha S[a].k) k`` and
+``o[a] = S_new[a].q / sqrt(D)``; the fused norm (same page, ``gdn_gate_norm``)
+gives ``out = gn o / sqrt(mean(o^2) + eps) * silu(z)`` in bf16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "GdnError", "load", "build", "library_path",
+    "GDN_STATE_F32", "GDN_STATE_F16", "STATUS",
+    "gdn_decode", "gdn_decode_norm", "gdn_prefill_seq",
+    "gdn_h_f32_to_f16", "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error",
+]
+
+GDN_STATE_F32 = 0
+GDN_STATE_F16 = 1
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIGN",
+          4: "GDN_ERR_ALIAS", 5: "GDN_ERR_CUDA"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GdnError(RuntimeError):
+    """A libgdn call returned a nonzero status."""
+
+    def __init__(self, fn, status, detail=""):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} {detail}".strip())
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdn.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile libgdn.so in-tree with nvcc (sm_103a)."""
+    from . import builder
+    return builder.build(force=force)
+
+
+def _declare(lib):
+    P, i32, i64, u64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
+    lib.gdn_decode.argtypes = [P, i32, i64, P, P, P, P, P, P, i32, i32, i32, i32, i64, i64, i64, i64, P]
+    lib.gdn_decode_norm.argtypes = [P, i32, i64, P, P, P, P, P, P, P, f32, P, i32, i32, i32, i32,
+                                    i64, i64, i64, i64, i64, P]
+    lib.gdn_prefill_seq.argtypes = [P, i32, i64, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                    i64, i64, i64, i64, P]
+    lib.gdn_h_f32_to_f16.argtypes = [P, P, u64, P]
+    lib.gdn_h_f16_to_f32.argtypes = [P, P, u64, P]
+    for fn in ("gdn_decode", "gdn_decode_norm", "gdn_prefill_seq", "gdn_h_f32_to_f16", "gdn_h_f16_to_f32"):
+        getattr(lib, fn).restype = i32
+    lib.gdn_status_str.argtypes = [i32]
+    lib.gdn_status_str.restype = ctypes.c_char_p
+    lib.gdn_last_cuda_error.argtypes = []
+    lib.gdn_last_cuda_error.restype = i32
+    return lib
+
+
+def load(path: str | None = None):
+    """Load libgdn.so (building it first if it is missing); raises if that fails."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = path or library_path()
+            if not os.path.exists(path):
+                build()
+            _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _ptr(x):
+    """Device address of a tensor (its first element) or an int address; None -> NULL."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, st):
+    if st != 0:
+        detail = ""
+        if st == 5:
+            detail = f"(cudaError {load().gdn_last_cuda_error()})"
+        raise GdnError(fn, st, detail)
+
+
+def _state_dtype(state, state_dtype):
+    if state_dtype is not None:
+        return state_dtype
+    import torch
+    if isinstance(state, int):
+        raise ValueError("state_dtype is required when state is a raw address")
+    if state.dtype == torch.float32:
+        return GDN_STATE_F32
+    if state.dtype == torch.float16:
+        return GDN_STATE_F16
+    raise ValueError(f"unsupported state dtype {state.dtype}")
+
+
+def gdn_decode(state, q, k, v, alpha, beta, o, *, batch, nk, nv, d,
+               state_pitch=None, state_dtype=None,
+               qk_stride=None, v_stride=None, gb_stride=None, o_stride=None, stream=None):
+    """One token through the recurrence; raw fp32 o.  See include/gdn.h."""
+    lib = load()
+    sd = _state_dtype(state, state_dtype)
+    st = lib.gdn_decode(
+        _ptr(state), sd, state_pitch if state_pitch is not None else nv * d * d,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o),
+        batch, nk, nv, d,
+        qk_stride if qk_stride is not None else nk * d,
+        v_stride if v_stride is not None else nv * d,
+        gb_stride if gb_stride is not None else nv,
+        o_stride if o_stride is not None else nv * d,
+        _stream(stream))
+    _check("gdn_decode", st)
+
+
+def gdn_decode_norm(state, q, k, v, alpha, beta, z, gn, out, *, batch, nk, nv, d, eps=1e-6,
+                    state_pitch=None, state_dtype=None,
+                    qk_stride=None, v_stride=None, gb_stride=None, z_stride=None, out_stride=None,
+                    stream=None):
+    """One token through the recurrence with the fused gated RMS norm; bf16 out."""
+    lib = load()
+    sd = _state_dtype(state, state_dtype)
+    st = lib.gdn_decode_norm(
+        _ptr(state), sd, state_pitch if state_pitch is not None else nv * d * d,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(z), _ptr(gn), float(eps), _ptr(out),
+        batch, nk, nv, d,
+        qk_stride if qk_stride is not None else nk * d,
+        v_stride if v_stride is not None else nv * d,
+        gb_stride if gb_stride is not None else nv,
+        z_stride if z_stride is not None else nv * d,
+        out_stride if out_stride is not None else nv * d,
+        _stream(stream))
+    _check("gdn_decode_norm", st)
+
+
+def gdn_prefill_seq(state, q, k, v, alpha, beta, o, *, batch, seq_len, nk, nv, d,
+                    state_pitch=None, state_dtype=None,
+                    qk_stride=None, v_stride=None, gb_stride=None, o_stride=None, stream=None):
+    """seq_len tokens per sequence in one launch (token rows b*seq_len + t); raw fp32 o."""
+    lib = load()
+    sd = _state_dtype(state, state_dtype)
+    st = lib.gdn_prefill_seq(
+        _ptr(state), sd, state_pitch if state_pitch is not None else nv * d * d,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o),
+        batch, seq_len, nk, nv, d,
+        qk_stride if qk_stride is not None else nk * d,
+        v_stride if v_stride is not None else nv * d,
+        gb_stride if gb_stride is not None else nv,
+        o_stride if o_stride is not None else nv * d,
+        _stream(stream))
+    _check("gdn_prefill_seq", st)
+
+
+def gdn_h_f32_to_f16(src, dst, n=None, stream=None):
+    """n h-state elements fp32 -> fp16 (round to nearest even)."""
+    lib = load()
+    n = src.numel() if n is None else n
+    _check("gdn_h_f32_to_f16", lib.gdn_h_f32_to_f16(_ptr(src), _ptr(dst), n, _stream(stream)))
+
+
+def gdn_h_f16_to_f32(src, dst, n=None, stream=None):
+    """n h-state elements fp16 -> fp32 (exact)."""
+    lib = load()
+    n = src.numel() if n is None else n
+    _check("gdn_h_f16_to_f32", lib.gdn_h_f16_to_f32(_ptr(src), _ptr(dst), n, _stream(stream)))
+
+
+def gdn_status_str(status: int) -> str:
+    return load().gdn_status_str(status).decode()
+
+
+def gdn_last_cuda_error() -> int:
+    return load().gdn_last_cuda_error()

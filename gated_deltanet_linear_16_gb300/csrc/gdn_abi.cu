@@ -1,0 +1,266 @@
+// gdn_abi.cu -- the extern "C" entry points of libgdn (declared in
+// include/gdn.h): argument checks on the host, then one kernel launch.
+//
+// Every check runs before any CUDA call, so a rejected call has no effect and
+// the checks can be exercised on a machine without a GPU.
+#include <cmath>
+#include <cstdint>
+
+#include "gdn.h"
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+int sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return GDN_OK;
+    t_last_cuda_error = (int)e;
+    return GDN_ERR_CUDA;
+}
+
+// A byte range [lo, hi) touched by one operand.
+struct Span {
+    uintptr_t lo, hi;
+};
+
+// Bytes spanned by `rows` rows of `len` elements, `stride` elements apart.
+bool rows_span(const void *base, int64_t rows, int64_t len, int64_t stride, int64_t elem, Span *out)
+{
+    if (rows <= 0 || len <= 0) { out->lo = out->hi = (uintptr_t)base; return true; }
+    // (rows - 1) * stride + len elements, guarding 64-bit overflow
+    if (stride > 0 && rows - 1 > (INT64_MAX - len) / stride) return false;
+    const int64_t elems = (rows - 1) * stride + len;
+    if (elems > INT64_MAX / elem) return false;
+    out->lo = (uintptr_t)base;
+    out->hi = out->lo + (uintptr_t)(elems * elem);
+    return out->hi >= out->lo;
+}
+
+bool overlap(const Span &a, const Span &b) { return a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Checks shared by decode and prefill.  `rows` is the number of token rows
+// (batch for decode, batch * seq_len for prefill).
+struct Operand {
+    const void *p;
+    int64_t rows, len, stride, elem;
+};
+
+int check_common(int batch, int nk, int nv, int d, int64_t pitch, int state_dtype)
+{
+    if (batch < 0 || nk <= 0 || nv <= 0 || d <= 0) return GDN_ERR_ARG;
+    if (state_dtype != GDN_STATE_F32 && state_dtype != GDN_STATE_F16) return GDN_ERR_UNSUPPORTED;
+    if (d > 256) return GDN_ERR_UNSUPPORTED;
+    if ((int64_t)batch * nv > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+    const int64_t head_elems = (int64_t)nv * d * d;
+    if (pitch < head_elems) return GDN_ERR_ARG;
+    return GDN_OK;
+}
+
+// Every operand: non-null, stride >= row length, element-aligned; outputs
+// (the first `n_out` entries) overlap nothing else.
+int check_operands(const Operand *ops, int n_ops, int n_out)
+{
+    Span spans[16];
+    for (int i = 0; i < n_ops; ++i) {
+        const Operand &o = ops[i];
+        if (o.p == nullptr) return GDN_ERR_ARG;
+        if (o.rows > 1 && o.stride < o.len) return GDN_ERR_ARG;
+        if (!aligned(o.p, (uintptr_t)o.elem)) return GDN_ERR_ALIGN;
+        if (!rows_span(o.p, o.rows, o.len, o.stride, o.elem, &spans[i])) return GDN_ERR_ARG;
+    }
+    for (int i = 0; i < n_out; ++i)
+        for (int j = 0; j < n_ops; ++j)
+            if (j != i && overlap(spans[i], spans[j])) return GDN_ERR_ALIAS;
+    return GDN_OK;
+}
+
+bool vec16(const void *p) { return aligned(p, 16); }
+
+float inv_sqrt(int d) { return (float)(1.0 / std::sqrt((double)d)); }
+
+int decode_entry(void *state, int state_dtype, int64_t state_pitch,
+                 const float *q, const float *k, const float *v,
+                 const float *alpha, const float *beta,
+                 const float *z, const float *gn, float eps,
+                 float *o, uint16_t *out,
+                 int batch, int nk, int nv, int d,
+                 int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                 int64_t z_stride, int64_t o_stride, int64_t out_stride,
+                 bool norm, void *stream)
+{
+    int st = check_common(batch, nk, nv, d, state_pitch, state_dtype);
+    if (st != GDN_OK) return st;
+    if (norm && !(eps >= 0.0f && std::isfinite(eps))) return GDN_ERR_ARG;
+    const int64_t selem = state_dtype == GDN_STATE_F16 ? 2 : 4;
+    const int64_t B = batch, hv = (int64_t)nv * d, hk = (int64_t)nk * d;
+    Operand ops[10];
+    int n = 0;
+    ops[n++] = {state, B, (int64_t)nv * d * d, state_pitch, selem};
+    if (norm) ops[n++] = {out, B, hv, out_stride, 2};
+    else ops[n++] = {o, B, hv, o_stride, 4};
+    const int n_out = n;
+    ops[n++] = {q, B, hk, qk_stride, 4};
+    ops[n++] = {k, B, hk, qk_stride, 4};
+    ops[n++] = {v, B, hv, v_stride, 4};
+    ops[n++] = {alpha, B, nv, gb_stride, 4};
+    ops[n++] = {beta, B, nv, gb_stride, 4};
+    if (norm) {
+        ops[n++] = {z, B, hv, z_stride, 4};
+        ops[n++] = {gn, 1, d, d, 4};
+    }
+    if (batch == 0) {
+        // empty call: still reject null pointers, nothing to launch
+        for (int i = 0; i < n; ++i) if (ops[i].p == nullptr) return GDN_ERR_ARG;
+        return GDN_OK;
+    }
+    st = check_operands(ops, n, n_out);
+    if (st != GDN_OK) return st;
+
+    DecodeParams p{};
+    p.state = state; p.pitch = state_pitch;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
+    p.z = z; p.gn = gn; p.o = o; p.out = out;
+    p.qk_stride = qk_stride; p.v_stride = v_stride; p.gb_stride = gb_stride;
+    p.z_stride = z_stride; p.o_stride = o_stride; p.out_stride = out_stride;
+    p.batch = batch; p.nk = nk; p.nv = nv; p.d = d;
+    p.eps = eps; p.inv_sqrt_d = inv_sqrt(d);
+
+    // D == 128 vector path: 16-byte state rows and 16-byte k/q columns.
+    // (v, z, gn, alpha, beta, o and out are read/written as scalars.)
+    const bool fast = d == 128 && vec16(state) && (state_pitch * selem) % 16 == 0 &&
+                      vec16(q) && vec16(k) && (qk_stride * 4) % 16 == 0;
+    return cuda_status(launch_decode(p, state_dtype == GDN_STATE_F16, norm, fast, (cudaStream_t)stream));
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+GDN_API int gdn_decode(void *state, int state_dtype, int64_t state_pitch,
+                       const float *q, const float *k, const float *v,
+                       const float *alpha, const float *beta, float *o,
+                       int batch, int nk, int nv, int d,
+                       int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                       int64_t o_stride, void *stream)
+{
+    return decode_entry(state, state_dtype, state_pitch, q, k, v, alpha, beta, nullptr, nullptr, 0.0f,
+                        o, nullptr, batch, nk, nv, d, qk_stride, v_stride, gb_stride, 0, o_stride, 0,
+                        false, stream);
+}
+
+GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
+                            const float *q, const float *k, const float *v,
+                            const float *alpha, const float *beta,
+                            const float *z, const float *gn, float eps,
+                            uint16_t *out,
+                            int batch, int nk, int nv, int d,
+                            int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                            int64_t z_stride, int64_t out_stride, void *stream)
+{
+    return decode_entry(state, state_dtype, state_pitch, q, k, v, alpha, beta, z, gn, eps,
+                        nullptr, out, batch, nk, nv, d, qk_stride, v_stride, gb_stride, z_stride, 0,
+                        out_stride, true, stream);
+}
+
+GDN_API int gdn_prefill_seq(void *state, int state_dtype, int64_t state_pitch,
+                            const float *q, const float *k, const float *v,
+                            const float *alpha, const float *beta, float *o,
+                            int batch, int seq_len, int nk, int nv, int d,
+                            int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                            int64_t o_stride, void *stream)
+{
+    int st = check_common(batch, nk, nv, d, state_pitch, state_dtype);
+    if (st != GDN_OK) return st;
+    if (state_dtype != GDN_STATE_F32) return GDN_ERR_UNSUPPORTED;
+    if (seq_len < 0) return GDN_ERR_ARG;
+    const int64_t B = batch, R = (int64_t)batch * seq_len;
+    const int64_t hv = (int64_t)nv * d, hk = (int64_t)nk * d;
+    Operand ops[7] = {
+        {state, B, (int64_t)nv * d * d, state_pitch, 4},
+        {o, R, hv, o_stride, 4},
+        {q, R, hk, qk_stride, 4},
+        {k, R, hk, qk_stride, 4},
+        {v, R, hv, v_stride, 4},
+        {alpha, R, nv, gb_stride, 4},
+        {beta, R, nv, gb_stride, 4},
+    };
+    if (R == 0) {
+        for (auto &op : ops) if (op.p == nullptr) return GDN_ERR_ARG;
+        return GDN_OK;
+    }
+    st = check_operands(ops, 7, 2);
+    if (st != GDN_OK) return st;
+
+    PrefillParams p{};
+    p.state = (float *)state; p.pitch = state_pitch;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.o = o;
+    p.qk_stride = qk_stride; p.v_stride = v_stride; p.gb_stride = gb_stride; p.o_stride = o_stride;
+    p.batch = batch; p.seq_len = seq_len; p.nk = nk; p.nv = nv; p.d = d;
+    p.inv_sqrt_d = inv_sqrt(d);
+    p.zero = 0;
+    // D == 128 path: 16-byte state rows, 16-byte k/q rows and 16-byte v row blocks
+    const bool fast = d == 128 && vec16(state) && (state_pitch * 4) % 16 == 0 &&
+                      vec16(q) && vec16(k) && (qk_stride * 4) % 16 == 0 &&
+                      vec16(v) && (v_stride * 4) % 16 == 0;
+    return cuda_status(launch_prefill(p, fast, (cudaStream_t)stream));
+}
+
+GDN_API int gdn_h_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, void *stream)
+{
+    if (src == nullptr || dst == nullptr) return GDN_ERR_ARG;
+    if (n == 0) return GDN_OK;
+    if (n > (uint64_t)INT64_MAX / 4) return GDN_ERR_ARG;
+    if (!aligned(src, 4) || !aligned(dst, 2)) return GDN_ERR_ALIGN;
+    const Span a{(uintptr_t)src, (uintptr_t)src + n * 4}, b{(uintptr_t)dst, (uintptr_t)dst + n * 2};
+    if (overlap(a, b)) return GDN_ERR_ALIAS;
+    return cuda_status(launch_f32_to_f16(src, dst, n, vec16(src) && vec16(dst), (cudaStream_t)stream));
+}
+
+GDN_API int gdn_h_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, void *stream)
+{
+    if (src == nullptr || dst == nullptr) return GDN_ERR_ARG;
+    if (n == 0) return GDN_OK;
+    if (n > (uint64_t)INT64_MAX / 4) return GDN_ERR_ARG;
+    if (!aligned(src, 2) || !aligned(dst, 4)) return GDN_ERR_ALIGN;
+    const Span a{(uintptr_t)src, (uintptr_t)src + n * 2}, b{(uintptr_t)dst, (uintptr_t)dst + n * 4};
+    if (overlap(a, b)) return GDN_ERR_ALIAS;
+    return cuda_status(launch_f16_to_f32(src, dst, n, vec16(src) && vec16(dst), (cudaStream_t)stream));
+}
+
+GDN_API const char *gdn_status_str(int status)
+{
+    switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_ARG: return "GDN_ERR_ARG: invalid argument (null pointer, bad size, short stride or pitch, bad eps)";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: unsupported shape or state dtype";
+    case GDN_ERR_ALIGN: return "GDN_ERR_ALIGN: pointer not aligned to its element size";
+    case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS: an output overlaps another operand";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA launch failed";
+    default: return "GDN_ERR_UNKNOWN";
+    }
+}
+
+GDN_API int gdn_last_cuda_error(void) { return t_last_cuda_error; }
+
+}  // extern "C"

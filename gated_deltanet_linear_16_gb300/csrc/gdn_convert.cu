@@ -1,0 +1,157 @@
+// gdn_convert.cu -- h-state dtype converters, binary32 <-> binary16.
+//
+// Follows metrale_model_layers/layers/ops/ssm_gdn_a.rs, launchers
+// `ssm_h_state_f32_to_f16` (round to nearest even) and
+// `ssm_h_state_f16_to_f32` (exact widening): n elements, grid-stride, source
+// and destination must not alias.
+//
+// Pure HBM streams (6 bytes per element either way).  The vector kernels move
+// 8 elements per thread per step (two 16-byte fp32 vectors <-> one 16-byte
+// fp16 vector) and keep 4 steps in flight per thread; the grid is a whole
+// number of waves (4 CTAs of 256 threads per SM), and the few elements past
+// the last full vector are done by the first threads.  Unaligned pointers take
+// a scalar grid-stride kernel with the same results.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 4;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ unsigned pack_h2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<unsigned *>(&h);
+}
+__device__ __forceinline__ float2 unpack_h2(unsigned u) {
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    return __half22float2(h);
+}
+
+__global__ void __launch_bounds__(kThreads)
+f32_to_f16_vec(const float *__restrict__ src, uint16_t *__restrict__ dst, uint64_t n)
+{
+    const uint64_t nvec = n / 8;
+    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    uint64_t i = tid;
+    for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
+        uint4 a[kUnroll], b[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            a[u] = __ldcs(s4 + 2 * (i + u * stride));
+            b[u] = __ldcs(s4 + 2 * (i + u * stride) + 1);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            uint4 r;
+            r.x = pack_h2(__uint_as_float(a[u].x), __uint_as_float(a[u].y));
+            r.y = pack_h2(__uint_as_float(a[u].z), __uint_as_float(a[u].w));
+            r.z = pack_h2(__uint_as_float(b[u].x), __uint_as_float(b[u].y));
+            r.w = pack_h2(__uint_as_float(b[u].z), __uint_as_float(b[u].w));
+            __stcs(d4 + i + u * stride, r);
+        }
+    }
+    for (; i < nvec; i += stride) {
+        const uint4 a = __ldcs(s4 + 2 * i), b = __ldcs(s4 + 2 * i + 1);
+        uint4 r;
+        r.x = pack_h2(__uint_as_float(a.x), __uint_as_float(a.y));
+        r.y = pack_h2(__uint_as_float(a.z), __uint_as_float(a.w));
+        r.z = pack_h2(__uint_as_float(b.x), __uint_as_float(b.y));
+        r.w = pack_h2(__uint_as_float(b.z), __uint_as_float(b.w));
+        __stcs(d4 + i, r);
+    }
+    const uint64_t tail = nvec * 8 + tid;
+    if (tail < n) {
+        __half h = __float2half_rn(src[tail]);
+        dst[tail] = *reinterpret_cast<uint16_t *>(&h);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+f16_to_f32_vec(const uint16_t *__restrict__ src, float *__restrict__ dst, uint64_t n)
+{
+    const uint64_t nvec = n / 8;
+    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    uint64_t i = tid;
+    for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
+        uint4 a[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) a[u] = __ldcs(s4 + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const float2 x0 = unpack_h2(a[u].x), x1 = unpack_h2(a[u].y);
+            const float2 x2 = unpack_h2(a[u].z), x3 = unpack_h2(a[u].w);
+            __stcs(d4 + 2 * (i + u * stride), make_uint4(__float_as_uint(x0.x), __float_as_uint(x0.y),
+                                                         __float_as_uint(x1.x), __float_as_uint(x1.y)));
+            __stcs(d4 + 2 * (i + u * stride) + 1, make_uint4(__float_as_uint(x2.x), __float_as_uint(x2.y),
+                                                             __float_as_uint(x3.x), __float_as_uint(x3.y)));
+        }
+    }
+    for (; i < nvec; i += stride) {
+        const uint4 a = __ldcs(s4 + i);
+        const float2 x0 = unpack_h2(a.x), x1 = unpack_h2(a.y), x2 = unpack_h2(a.z), x3 = unpack_h2(a.w);
+        __stcs(d4 + 2 * i, make_uint4(__float_as_uint(x0.x), __float_as_uint(x0.y),
+                                      __float_as_uint(x1.x), __float_as_uint(x1.y)));
+        __stcs(d4 + 2 * i + 1, make_uint4(__float_as_uint(x2.x), __float_as_uint(x2.y),
+                                          __float_as_uint(x3.x), __float_as_uint(x3.y)));
+    }
+    const uint64_t tail = nvec * 8 + tid;
+    if (tail < n) {
+        __half h = *reinterpret_cast<const __half *>(src + tail);
+        dst[tail] = __half2float(h);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+f32_to_f16_scalar(const float *__restrict__ src, uint16_t *__restrict__ dst, uint64_t n)
+{
+    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+    for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += stride) {
+        __half h = __float2half_rn(src[i]);
+        dst[i] = *reinterpret_cast<uint16_t *>(&h);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+f16_to_f32_scalar(const uint16_t *__restrict__ src, float *__restrict__ dst, uint64_t n)
+{
+    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+    for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += stride) {
+        __half h = *reinterpret_cast<const __half *>(src + i);
+        dst[i] = __half2float(h);
+    }
+}
+
+unsigned grid_for(uint64_t work_items)
+{
+    // whole waves of kCtasPerSm CTAs per SM, never more CTAs than work
+    const uint64_t full = (uint64_t)sm_count() * kCtasPerSm;
+    const uint64_t need = (work_items + kThreads - 1) / kThreads;
+    const uint64_t g = need < full ? need : full;
+    return (unsigned)(g > 0 ? g : 1);
+}
+
+}  // namespace
+
+cudaError_t launch_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, bool vec, cudaStream_t s)
+{
+    if (vec) f32_to_f16_vec<<<grid_for(n / 8 > 0 ? n / 8 : n), kThreads, 0, s>>>(src, dst, n);
+    else f32_to_f16_scalar<<<grid_for(n), kThreads, 0, s>>>(src, dst, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, bool vec, cudaStream_t s)
+{
+    if (vec) f16_to_f32_vec<<<grid_for(n / 8 > 0 ? n / 8 : n), kThreads, 0, s>>>(src, dst, n);
+    else f16_to_f32_scalar<<<grid_for(n), kThreads, 0, s>>>(src, dst, n);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

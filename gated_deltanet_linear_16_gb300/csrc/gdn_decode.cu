@@ -1,0 +1,293 @@
+// gdn_decode.cu -- single-token gated delta rule kernels (raw fp32 output, or
+// the gated RMS norm fused in the same CTA with a bf16 output), for fp32 and
+// fp16 h-states.
+//
+// The step (logicaffeine_compile/codegen_cuda/gdn.rs, kernel `gdn_step`), for
+// value head h, key/query head g = h mod NK and state row a:
+//   u = S[a].k, w = S[a].q, kq = k.q, coef = beta (v[a] - alpha u),
+//   o[a] = (alpha w + coef kq) / sqrt(D),  S[a][c] <- alpha S[a][c] + coef k[c].
+// The norm (same page, kernel `gdn_gate_norm`): out = gn o / sqrt(mean o^2 + eps)
+// * silu(z).  The fused variants follow metrale_model_layers/layers/ops/
+// ssm_gdn_a.rs (`gdn_decode_f32_strided_norm`, `gdn_decode_f16_strided_norm`):
+// the norm runs in the CTA that owns the head and only bf16 leaves the chip.
+//
+// GB300 design.  The state is ~99% of the bytes and is touched exactly once
+// (one read, one write per element), so the kernel is an HBM stream:
+//  * one CTA owns one (sequence, head): 8 warps x 16 rows, so the norm's
+//    reduction over the head's D outputs needs a single __syncthreads;
+//  * every state access is a 16-byte vector: an fp32 row (512 B) is one
+//    warp-wide load, an fp16 row (256 B) half of one, so a warp touches whole
+//    128-byte lines and stores never leave partial sectors;
+//  * each lane issues all of its 16-byte state loads (16 for fp32, 8 for fp16)
+//    before it needs the first one, so a CTA keeps its whole head (64 KB fp32,
+//    32 KB fp16) in flight; with two or more CTAs per SM that is >= 128 KB of
+//    outstanding loads per SM, enough to cover HBM latency at full bandwidth;
+//  * k and q are read as this lane's own 16-byte columns, v/z/gn as one
+//    coalesced 64-byte read per warp that lanes then broadcast by shuffle;
+//  * the three dot products are butterfly shuffles inside the group of lanes
+//    that holds a row (32 lanes fp32, 16 lanes fp16); k.q is reduced once per
+//    warp, not per row.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kWarps = 8;
+constexpr int kRowsPerWarp = kD / kWarps;   // 16
+
+// A 16-byte vector of state elements, widened to / narrowed from fp32.
+template <typename TS> struct Vec16;
+
+template <> struct Vec16<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void unpack(const uint4 r, float (&x)[N]) {
+        x[0] = __uint_as_float(r.x); x[1] = __uint_as_float(r.y);
+        x[2] = __uint_as_float(r.z); x[3] = __uint_as_float(r.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&x)[N]) {
+        return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
+                          __float_as_uint(x[2]), __float_as_uint(x[3]));
+    }
+};
+
+template <> struct Vec16<__half> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static float2 h2f(unsigned u) {
+        __half2 h = *reinterpret_cast<__half2 *>(&u);
+        return __half22float2(h);
+    }
+    __device__ __forceinline__ static unsigned f2h(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);           // round to nearest even
+        return *reinterpret_cast<unsigned *>(&h);
+    }
+    __device__ __forceinline__ static void unpack(const uint4 r, float (&x)[N]) {
+        float2 t;
+        t = h2f(r.x); x[0] = t.x; x[1] = t.y;
+        t = h2f(r.y); x[2] = t.x; x[3] = t.y;
+        t = h2f(r.z); x[4] = t.x; x[5] = t.y;
+        t = h2f(r.w); x[6] = t.x; x[7] = t.y;
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&x)[N]) {
+        return make_uint4(f2h(x[0], x[1]), f2h(x[2], x[3]), f2h(x[4], x[5]), f2h(x[6], x[7]));
+    }
+};
+
+template <typename TS> __device__ __forceinline__ float to_f32(TS x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <typename TS> __device__ __forceinline__ TS from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+
+// ------------------------------------------------------------------ D == 128
+
+template <typename TS> struct FastOcc { static constexpr int kMinBlocks = 2; };
+template <> struct FastOcc<__half> { static constexpr int kMinBlocks = 3; };
+
+template <typename TS, bool NORM>
+__global__ void __launch_bounds__(kWarps * 32, FastOcc<TS>::kMinBlocks)
+decode_d128(const DecodeParams p)
+{
+    using V = Vec16<TS>;
+    constexpr int EPV = V::N;                  // state elements per 16-byte vector
+    constexpr int LPR = kD / EPV;              // lanes per state row: 32 fp32, 16 fp16
+    constexpr int RPL = 32 / LPR;              // rows per warp-wide load: 1 fp32, 2 fp16
+    constexpr int NLD = kRowsPerWarp / RPL;    // 16-byte state loads per lane
+
+    const int unit = blockIdx.x;               // (sequence, value head)
+    const int seq = unit / p.nv;
+    const int h = unit - seq * p.nv;
+    const int g = h % p.nk;                    // tiled key-head pairing
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / LPR;                // which row of a warp-wide load
+    const int col = (lane % LPR) * EPV;        // first column this lane owns
+    const int row0 = warp * kRowsPerWarp;
+
+    TS *S = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD;
+    TS *rowp = S + (int64_t)(row0 + sub) * kD + col;
+
+    // 1. the whole slice of the state this lane owns, in flight at once
+    uint4 raw[NLD];
+#pragma unroll
+    for (int i = 0; i < NLD; ++i) raw[i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
+
+    // 2. token inputs
+    const float *kp = p.k + seq * p.qk_stride + (int64_t)g * kD + col;
+    const float *qp = p.q + seq * p.qk_stride + (int64_t)g * kD + col;
+    float kx[EPV], qx[EPV];
+#pragma unroll
+    for (int j = 0; j < EPV; j += 4) {
+        const float4 a = ld_ro_f4(kp + j), b = ld_ro_f4(qp + j);
+        kx[j] = a.x; kx[j + 1] = a.y; kx[j + 2] = a.z; kx[j + 3] = a.w;
+        qx[j] = b.x; qx[j + 1] = b.y; qx[j + 2] = b.z; qx[j + 3] = b.w;
+    }
+    const bool row_lane = lane < kRowsPerWarp;  // lane r carries row row0 + r
+    const float v_l = row_lane ? __ldg(p.v + seq * p.v_stride + (int64_t)h * kD + row0 + lane) : 0.f;
+    float z_l = 0.f, gn_l = 0.f;
+    if (NORM && row_lane) {
+        z_l = __ldg(p.z + seq * p.z_stride + (int64_t)h * kD + row0 + lane);
+        gn_l = __ldg(p.gn + row0 + lane);
+    }
+    const float alpha = __ldg(p.alpha + seq * p.gb_stride + h);
+    const float beta = __ldg(p.beta + seq * p.gb_stride + h);
+
+    float kq = 0.f;
+#pragma unroll
+    for (int j = 0; j < EPV; ++j) kq = fmaf(kx[j], qx[j], kq);
+    kq = group_sum<LPR>(kq);
+
+    // 3. per row: two dot products, the delta coefficient, output, write-back
+    float o_keep = 0.f;                        // lane r < 16 keeps o of row row0 + r
+#pragma unroll
+    for (int i = 0; i < NLD; ++i) {
+        float s[EPV];
+        V::unpack(raw[i], s);
+        float u = 0.f, w = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
+        u = group_sum<LPR>(u);
+        w = group_sum<LPR>(w);
+        const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
+        const float coef = beta * (va - alpha * u);
+        const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
+        st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
+        if constexpr (RPL == 1) {
+            if (lane == i) o_keep = oa;
+        } else {
+#pragma unroll
+            for (int r = 0; r < RPL; ++r) {
+                const float orr = __shfl_sync(kFull, oa, r * LPR);
+                if (lane == i * RPL + r) o_keep = orr;
+            }
+        }
+    }
+
+    if constexpr (!NORM) {
+        if (row_lane) p.o[seq * p.o_stride + (int64_t)h * kD + row0 + lane] = o_keep;
+    } else {
+        // 4. gated RMS norm over the head's 128 outputs, in this CTA
+        __shared__ float red[kWarps];
+        const float ss = group_sum<32>(o_keep * o_keep);   // lanes >= 16 hold 0
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int i = 0; i < kWarps; ++i) tot += red[i];
+        const float rstd = rsqrtf(tot * (1.0f / kD) + p.eps);
+        if (row_lane) {
+            const float y = gn_l * o_keep * rstd * silu(z_l);
+            p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ any D <= 256
+
+// One CTA per (sequence, head), one warp per row (rows strided over 4 warps),
+// lanes strided over columns with the row cached in registers, so the state is
+// still read once and written once.  Handles D < 32, D not a multiple of 32,
+// and any element alignment.
+constexpr int kGenWarps = 4;
+constexpr int kMaxD = 256;
+
+template <typename TS, bool NORM>
+__global__ void __launch_bounds__(kGenWarps * 32)
+decode_generic(const DecodeParams p)
+{
+    constexpr int MAXV = kMaxD / 32;
+    __shared__ float o_s[kMaxD];
+    __shared__ float red[kGenWarps];
+
+    const int D = p.d;
+    const int unit = blockIdx.x;
+    const int seq = unit / p.nv;
+    const int h = unit - seq * p.nv;
+    const int g = h % p.nk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    TS *S = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * D * D;
+    const float *kp = p.k + seq * p.qk_stride + (int64_t)g * D;
+    const float *qp = p.q + seq * p.qk_stride + (int64_t)g * D;
+    const float *vp = p.v + seq * p.v_stride + (int64_t)h * D;
+    const float alpha = p.alpha[seq * p.gb_stride + h];
+    const float beta = p.beta[seq * p.gb_stride + h];
+
+    float kreg[MAXV], qreg[MAXV];
+    float kq = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+        const int c = lane + 32 * j;
+        kreg[j] = c < D ? kp[c] : 0.f;
+        qreg[j] = c < D ? qp[c] : 0.f;
+        kq = fmaf(kreg[j], qreg[j], kq);
+    }
+    kq = group_sum<32>(kq);
+
+    for (int a = warp; a < D; a += kGenWarps) {
+        TS *row = S + (int64_t)a * D;
+        float s[MAXV];
+        float u = 0.f, w = 0.f;
+#pragma unroll
+        for (int j = 0; j < MAXV; ++j) {
+            const int c = lane + 32 * j;
+            s[j] = c < D ? to_f32<TS>(row[c]) : 0.f;
+            u = fmaf(s[j], kreg[j], u);
+            w = fmaf(s[j], qreg[j], w);
+        }
+        u = group_sum<32>(u);
+        w = group_sum<32>(w);
+        const float coef = beta * (vp[a] - alpha * u);
+        const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
+#pragma unroll
+        for (int j = 0; j < MAXV; ++j) {
+            const int c = lane + 32 * j;
+            if (c < D) row[c] = from_f32<TS>(fmaf(coef, kreg[j], alpha * s[j]));
+        }
+        if (lane == 0) o_s[a] = oa;
+    }
+    __syncthreads();
+
+    if constexpr (!NORM) {
+        for (int a = threadIdx.x; a < D; a += kGenWarps * 32)
+            p.o[seq * p.o_stride + (int64_t)h * D + a] = o_s[a];
+    } else {
+        float ss = 0.f;
+        for (int a = threadIdx.x; a < D; a += kGenWarps * 32) ss += o_s[a] * o_s[a];
+        ss = group_sum<32>(ss);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int i = 0; i < kGenWarps; ++i) tot += red[i];
+        const float rstd = rsqrtf(tot / (float)D + p.eps);
+        const float *zp = p.z + seq * p.z_stride + (int64_t)h * D;
+        uint16_t *op = p.out + seq * p.out_stride + (int64_t)h * D;
+        for (int a = threadIdx.x; a < D; a += kGenWarps * 32)
+            op[a] = bf16_bits_rn(p.gn[a] * o_s[a] * rstd * silu(zp[a]));
+    }
+}
+
+template <typename TS, bool NORM>
+cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
+{
+    const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
+    if (fast) decode_d128<TS, NORM><<<grid, kWarps * 32, 0, s>>>(p);
+    else decode_generic<TS, NORM><<<grid, kGenWarps * 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams &p, bool f16_state, bool norm, bool fast, cudaStream_t s)
+{
+    if (f16_state) {
+        return norm ? launch_typed<__half, true>(p, fast, s) : launch_typed<__half, false>(p, fast, s);
+    }
+    return norm ? launch_typed<float, true>(p, fast, s) : launch_typed<float, false>(p, fast, s);
+}
+
+}  // namespace gdn

@@ -1,0 +1,82 @@
+// gdn_internal.cuh -- parameter blocks, launcher declarations and small device
+// helpers shared by the libgdn translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Everything one decode launch needs.  Pointers are device pointers; strides
+// and the pitch are in elements of their own arrays.
+struct DecodeParams {
+    void *state;            // float* or __half*
+    int64_t pitch;          // state elements between sequence slots
+    const float *q, *k, *v, *alpha, *beta;
+    const float *z, *gn;    // norm variant only
+    float *o;               // raw variant only
+    uint16_t *out;          // norm variant only (bf16 bits)
+    int64_t qk_stride, v_stride, gb_stride, z_stride, o_stride, out_stride;
+    int batch, nk, nv, d;
+    float eps;
+    float inv_sqrt_d;       // 1/sqrt(D) rounded once on the host
+};
+
+struct PrefillParams {
+    float *state;
+    int64_t pitch;
+    const float *q, *k, *v, *alpha, *beta;
+    float *o;
+    int64_t qk_stride, v_stride, gb_stride, o_stride;   // per token row
+    int batch, seq_len, nk, nv, d;
+    float inv_sqrt_d;
+    unsigned zero;          // always 0; see prefill_d128 (orders shared loads)
+};
+
+// Launchers (one per translation unit family).  They pick the kernel variant
+// (fast D == 128 path when the alignment allows it, general otherwise) and
+// return the launch status.
+cudaError_t launch_decode(const DecodeParams &p, bool f16_state, bool norm, bool fast, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams &p, bool fast, cudaStream_t s);
+cudaError_t launch_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, bool vec, cudaStream_t s);
+cudaError_t launch_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, bool vec, cudaStream_t s);
+
+// Number of SMs of the current device (cached per device id).
+int sm_count();
+
+// ---------------------------------------------------------------- device helpers
+
+// Streaming 16-byte global load / store: the state is touched once per call,
+// so keep it from displacing reusable lines (cache-streaming hint).
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ void st_stream16(void *p, uint4 v) {
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+// Read-only 16-byte load through the non-coherent path (inputs shared by heads).
+__device__ __forceinline__ float4 ld_ro_f4(const float *p) {
+    return __ldg(reinterpret_cast<const float4 *>(p));
+}
+
+// Butterfly sum over groups of W consecutive lanes (W a power of two <= 32);
+// every lane of the group ends with the group total.
+template <int W>
+__device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+    for (int off = W / 2; off > 0; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
+    return x;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+
+__device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
+    __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&b);
+}
+
+}  // namespace gdn

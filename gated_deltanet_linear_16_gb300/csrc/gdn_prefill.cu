@@ -1,0 +1,252 @@
+// gdn_prefill.cu -- token-sequential prefill: seq_len tokens per sequence
+// through the gated delta rule in one launch, the state held on chip.
+//
+// Follows metrale_model_layers/layers/ops/ssm_gdn_a.rs, launcher
+// `gdn_prefill_regresident` (the recurrence walks the tokens in order, the
+// state stays in registers, raw o for every token, no norm); the step itself
+// is logicaffeine_compile/codegen_cuda/gdn.rs, kernel `gdn_step`.
+//
+// Rows of S never interact: row a needs only k, q, alpha, beta of the token
+// and its own v[a].  So the GB300 kernel gives each THREAD one whole state row
+// (128 fp32 registers) for all tokens:
+//  * u = S[a].k and o[a] = S_new[a].q are thread-local dot products (no
+//    shuffles at all); k and q come from shared memory as broadcast 16-byte
+//    reads, the same address for every lane;
+//  * o is read out of the updated state, o = S_new q / sqrt(D), which equals
+//    (alpha w + coef kq)/sqrt(D) and needs no per-token k.q;
+//  * a CTA is one warp (32 rows of one head).  With ~160 registers a thread
+//    an SM holds 12 such warps, and one-warp CTAs let the block scheduler
+//    spread the B*NV*D/32 warps evenly over the 152 SMs (a 4-warp CTA per head
+//    would leave some SMs with 3 heads and others with 2);
+//  * per-token inputs stream through a two-stage cp.async ring in shared
+//    memory (8 tokens per stage), so the next chunk's loads overlap this
+//    chunk's arithmetic.  cp.async waits are hardware group waits (no spin
+//    loop on a flag).
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTC = 8;            // tokens per stage
+constexpr int kRows = 32;         // rows per CTA (one warp)
+
+struct __align__(16) Stage {
+    float k[kTC][kD];
+    float q[kTC][kD];
+    float v[kTC][kRows];
+    float alpha[kTC];
+    float beta[kTC];
+};
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ float4 lds128(unsigned addr) {
+    float4 r;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr));
+    return r;
+}
+
+// `addr` made data-dependent on `dep` through a mask that is zero at run time
+// but unknown to the compiler.  Without it the scheduler lifts the second
+// pass's 64 shared loads above the first pass's reduction (they do not depend
+// on coef) and the 128-register state row spills.
+__device__ __forceinline__ unsigned after(unsigned addr, float dep, unsigned zero) {
+    return addr + (__float_as_uint(dep) & zero);
+}
+
+// Stage tokens [t0, t0 + n) of this warp's (sequence, head, row block).  The
+// loops stay rolled: they run while the 128 state registers are live, so they
+// must not need many registers of their own.
+__device__ __forceinline__ void stage_chunk(Stage &st, const PrefillParams &p, int seq, int h, int g,
+                                            int r0, int t0, int n, int lane)
+{
+    const int64_t tok0 = (int64_t)seq * p.seq_len + t0;
+    const float *kp = p.k + tok0 * p.qk_stride + (int64_t)g * kD + 4 * lane;
+    const float *qp = p.q + tok0 * p.qk_stride + (int64_t)g * kD + 4 * lane;
+#pragma unroll 1
+    for (int tt = 0; tt < n; ++tt) {
+        cp_async16(&st.k[tt][4 * lane], kp);
+        cp_async16(&st.q[tt][4 * lane], qp);
+        kp += p.qk_stride;
+        qp += p.qk_stride;
+    }
+    // v: n tokens x 32 rows = n x 8 vectors of 16 bytes
+#pragma unroll 1
+    for (int c = lane; c < n * (kRows / 4); c += 32) {
+        const int tt = c / (kRows / 4), part = c % (kRows / 4);
+        cp_async16(&st.v[tt][4 * part], p.v + (tok0 + tt) * p.v_stride + (int64_t)h * kD + r0 + 4 * part);
+    }
+    if (lane < n) {
+        cp_async4(&st.alpha[lane], p.alpha + (tok0 + lane) * p.gb_stride + h);
+        cp_async4(&st.beta[lane], p.beta + (tok0 + lane) * p.gb_stride + h);
+    }
+}
+
+__global__ void __launch_bounds__(kRows, 12)
+prefill_d128(const PrefillParams p)
+{
+    __shared__ Stage ring[2];
+
+    const int lane = threadIdx.x;
+    const int blocks_per_head = kD / kRows;           // 4
+    const int head = blockIdx.x / blocks_per_head;    // (sequence, value head)
+    const int r0 = (blockIdx.x - head * blocks_per_head) * kRows;
+    const int seq = head / p.nv;
+    const int h = head - seq * p.nv;
+    const int g = h % p.nk;
+    const int a = r0 + lane;                           // this thread's state row
+
+    const int T = p.seq_len;
+    const int nchunks = (T + kTC - 1) / kTC;
+    stage_chunk(ring[0], p, seq, h, g, r0, 0, min(kTC, T), lane);   // before S is live
+    cp_async_commit();
+
+    float *row = p.state + seq * p.pitch + (int64_t)h * kD * kD + (int64_t)a * kD;
+    float S[kD];
+#pragma unroll
+    for (int j = 0; j < kD; j += 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(row + j);
+        S[j] = t.x; S[j + 1] = t.y; S[j + 2] = t.z; S[j + 3] = t.w;
+    }
+
+    float *orow = p.o + (int64_t)seq * T * p.o_stride + (int64_t)h * kD + a;
+    for (int c = 0; c < nchunks; ++c) {
+        if (c + 1 < nchunks) {
+            const int t1 = (c + 1) * kTC;
+            stage_chunk(ring[(c + 1) & 1], p, seq, h, g, r0, t1, min(kTC, T - t1), lane);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncwarp();
+        const Stage &st = ring[c & 1];
+        const int n = min(kTC, T - c * kTC);
+        const unsigned k_s = (unsigned)__cvta_generic_to_shared(st.k[0]);
+        const unsigned q_s = (unsigned)__cvta_generic_to_shared(st.q[0]);
+        for (int tt = 0; tt < n; ++tt) {
+            const unsigned kt = k_s + tt * (kD * 4), qt = q_s + tt * (kD * 4);
+            // pass 1: u = S[a] . k
+            float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < kD / 4; ++j) {
+                const float4 kk = lds128(kt + 16 * j);
+                u0 = fmaf(S[4 * j], kk.x, u0);
+                u1 = fmaf(S[4 * j + 1], kk.y, u1);
+                u2 = fmaf(S[4 * j + 2], kk.z, u2);
+                u3 = fmaf(S[4 * j + 3], kk.w, u3);
+            }
+            const float u = (u0 + u1) + (u2 + u3);
+            const float alpha = st.alpha[tt], beta = st.beta[tt];
+            const float coef = beta * (st.v[tt][lane] - alpha * u);
+            // pass 2: S[a] <- alpha S[a] + coef k ;  o = S_new[a] . q
+            const unsigned k2 = after(kt, coef, p.zero), q2 = after(qt, coef, p.zero);
+            const float a2 = __uint_as_float(after(__float_as_uint(alpha), coef, p.zero));  // == alpha
+            float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < kD / 4; ++j) {
+                const float4 kk = lds128(k2 + 16 * j), qq = lds128(q2 + 16 * j);
+                S[4 * j] = fmaf(coef, kk.x, a2 * S[4 * j]);
+                S[4 * j + 1] = fmaf(coef, kk.y, a2 * S[4 * j + 1]);
+                S[4 * j + 2] = fmaf(coef, kk.z, a2 * S[4 * j + 2]);
+                S[4 * j + 3] = fmaf(coef, kk.w, a2 * S[4 * j + 3]);
+                o0 = fmaf(S[4 * j], qq.x, o0);
+                o1 = fmaf(S[4 * j + 1], qq.y, o1);
+                o2 = fmaf(S[4 * j + 2], qq.z, o2);
+                o3 = fmaf(S[4 * j + 3], qq.w, o3);
+            }
+            __stcs(orow + (int64_t)(c * kTC + tt) * p.o_stride, ((o0 + o1) + (o2 + o3)) * p.inv_sqrt_d);
+        }
+        __syncwarp();   // every lane is done with this stage before it is refilled
+    }
+
+#pragma unroll
+    for (int j = 0; j < kD; j += 4)
+        *reinterpret_cast<float4 *>(row + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+}
+
+// Any D <= 256 and any alignment: one CTA per (sequence, head), one warp per
+// row (rows strided over 4 warps), lanes strided over columns with the row in
+// registers for all tokens; token inputs read straight from global memory.
+constexpr int kGenWarps = 4;
+constexpr int kMaxD = 256;
+
+__global__ void __launch_bounds__(kGenWarps * 32)
+prefill_generic(const PrefillParams p)
+{
+    constexpr int MAXV = kMaxD / 32;
+    const int D = p.d;
+    const int seq = blockIdx.x / p.nv;
+    const int h = blockIdx.x - seq * p.nv;
+    const int g = h % p.nk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = p.seq_len;
+
+    for (int a = warp; a < D; a += kGenWarps) {
+        float *row = p.state + seq * p.pitch + (int64_t)h * D * D + (int64_t)a * D;
+        float s[MAXV];
+#pragma unroll
+        for (int j = 0; j < MAXV; ++j) {
+            const int c = lane + 32 * j;
+            s[j] = c < D ? row[c] : 0.f;
+        }
+        for (int t = 0; t < T; ++t) {
+            const int64_t tok = (int64_t)seq * T + t;
+            const float *kp = p.k + tok * p.qk_stride + (int64_t)g * D;
+            const float *qp = p.q + tok * p.qk_stride + (int64_t)g * D;
+            float kr[MAXV];
+            float u = 0.f;
+#pragma unroll
+            for (int j = 0; j < MAXV; ++j) {
+                const int c = lane + 32 * j;
+                kr[j] = c < D ? kp[c] : 0.f;
+                u = fmaf(s[j], kr[j], u);
+            }
+            u = group_sum<32>(u);
+            const float alpha = p.alpha[tok * p.gb_stride + h];
+            const float beta = p.beta[tok * p.gb_stride + h];
+            const float coef = beta * (p.v[tok * p.v_stride + (int64_t)h * D + a] - alpha * u);
+            float w = 0.f;
+#pragma unroll
+            for (int j = 0; j < MAXV; ++j) {
+                const int c = lane + 32 * j;
+                s[j] = fmaf(coef, kr[j], alpha * s[j]);
+                if (c < D) w = fmaf(s[j], qp[c], w);
+            }
+            w = group_sum<32>(w);
+            if (lane == 0) p.o[tok * p.o_stride + (int64_t)h * D + a] = w * p.inv_sqrt_d;
+        }
+#pragma unroll
+        for (int j = 0; j < MAXV; ++j) {
+            const int c = lane + 32 * j;
+            if (c < D) row[c] = s[j];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams &p, bool fast, cudaStream_t s)
+{
+    const int64_t heads = (int64_t)p.batch * p.nv;
+    if (fast) {
+        prefill_d128<<<(unsigned)(heads * (kD / kRows)), kRows, 0, s>>>(p);
+    } else {
+        prefill_generic<<<(unsigned)heads, kGenWarps * 32, 0, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,172 @@
+/*
+ * gdn.h -- C-ABI of libgdn, the GB300 (sm_103a) gated delta rule library.
+ *
+ * The method (logicaffeine_compile/codegen_cuda/gdn.rs, kernel `gdn_step`):
+ * for every sequence b and value head h, with key/query head g = h mod NK
+ * (heads are tiled, not repeat-interleaved), the D x D state S of (b, h)
+ * takes one token as
+ *
+ *     u[a]    = S[a] . k_g                    (row a of S against the key)
+ *     coef[a] = beta_h * (v_h[a] - alpha_h * u[a])
+ *     S[a][c] = alpha_h * S[a][c] + coef[a] * k_g[c]
+ *     o[a]    = (S_new[a] . q_g) / sqrt(D)
+ *
+ * i.e. S <- alpha S + beta (v - alpha S k) k^T and o = S q / sqrt(D).  The
+ * gated RMS norm that follows (same page, kernel `gdn_gate_norm`) is
+ *
+ *     out[a]  = gn[a] * o[a] / sqrt(mean_a(o^2) + eps) * z[a] * sigmoid(z[a])
+ *
+ * (normalise first, then gate).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Memory: every pointer is a DEVICE pointer to memory the caller owns.  The
+ *   library allocates nothing, keeps no per-call state, and updates the state
+ *   in place.  Calls are asynchronous on `stream` (a cudaStream_t passed as
+ *   void*; NULL is the legacy default stream); the caller synchronises.
+ * - State layout: sequence b's slot starts `b * state_pitch` ELEMENTS after
+ *   `state`; inside a slot, head h is a contiguous D x D row-major block at
+ *   `h * D * D`, row a = value index, column c = key index.  state_pitch >=
+ *   NV * D * D; a pitch larger than that leaves padding the library never
+ *   reads or writes.  (metrale_model_layers/layers/ops/ssm_gdn_a.rs,
+ *   `gdn_decode_f16_strided_norm`, passes the slot pitch the same way: in
+ *   elements, set by how the pool was sized.)
+ * - Token rows: q and k rows hold NK * D floats, v, z, o and out rows NV * D,
+ *   alpha and beta rows NV.  Row i (sequence b for decode; token (b, t) at
+ *   i = b * seq_len + t for prefill) starts `i * <x>_stride` ELEMENTS after its
+ *   base pointer; a stride must be at least the row length.
+ * - Return value: GDN_OK, or a GDN_ERR_* code.  Arguments are checked on the
+ *   host before anything is launched; a rejected call touches no memory.
+ *   GDN_ERR_CUDA means the launch itself failed; gdn_last_cuda_error() gives
+ *   the cudaError_t.  A batch, seq_len or n of 0 is a valid empty call.
+ * - Fast paths (D == 128, 16-byte aligned base pointers, strides and pitch
+ *   that keep every row 16-byte aligned) are taken automatically; any other
+ *   1 <= D <= 256 runs a general kernel with the same results up to fp32
+ *   summation order.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stdint.h>
+
+#if defined(_WIN32)
+#define GDN_API __declspec(dllexport)
+#else
+#define GDN_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define GDN_OK 0
+#define GDN_ERR_ARG 1          /* null pointer, negative or zero dims, short stride/pitch, bad eps */
+#define GDN_ERR_UNSUPPORTED 2  /* D > 256, unknown state dtype */
+#define GDN_ERR_ALIGN 3        /* a pointer not aligned to its element size */
+#define GDN_ERR_ALIAS 4        /* an output overlaps another operand */
+#define GDN_ERR_CUDA 5         /* the CUDA launch failed (see gdn_last_cuda_error) */
+
+/* Storage type of the h-state. */
+typedef enum { GDN_STATE_F32 = 0, GDN_STATE_F16 = 1 } gdn_state_dtype;
+
+/*
+ * gdn_decode -- one token through the recurrence for `batch` sequences,
+ * raw fp32 output.
+ *   Defined by: gdn.rs, kernel `gdn_step` (the step, g = h mod NK, the
+ *   1/sqrt(D) output scale); ssm_gdn_a.rs, launchers `gdn_decode` and
+ *   `gdn_decode_f32_strided` (batched, per-sequence row strides).
+ *   state        [batch] slots, dtype `state_dtype` (fp32, or fp16 that is
+ *                read to fp32, updated in fp32 and stored back
+ *                round-to-nearest-even), updated in place.
+ *   q, k         [batch] rows of NK*D fp32 (already L2-normalised upstream).
+ *   v            [batch] rows of NV*D fp32.
+ *   alpha, beta  [batch] rows of NV fp32: linear decay in (0,1] and write
+ *                strength.
+ *   o            [batch] rows of NV*D fp32, written.
+ *   Errors: GDN_ERR_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIGN, GDN_ERR_ALIAS
+ *   (state or o overlapping any operand), GDN_ERR_CUDA.
+ */
+GDN_API int gdn_decode(void *state, int state_dtype, int64_t state_pitch,
+                       const float *q, const float *k, const float *v,
+                       const float *alpha, const float *beta, float *o,
+                       int batch, int nk, int nv, int d,
+                       int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                       int64_t o_stride, void *stream);
+
+/*
+ * gdn_decode_norm -- gdn_decode with the gated RMS norm fused in the same
+ * kernel; writes bf16 and no fp32 output.
+ *   Defined by: gdn.rs, kernels `gdn_step` and `gdn_gate_norm` (norm over
+ *   the D outputs of a head, mean of squares plus eps under the root, weight
+ *   gn shared by all heads, then the silu(z) gate); ssm_gdn_a.rs,
+ *   `gdn_decode_f32_norm` / `gdn_decode_f32_strided_norm` (fused, bf16 out)
+ *   and `gdn_decode_f16_strided_norm` (fp16 h-state pool with a slot pitch).
+ *   z            [batch] rows of NV*D fp32 gate input.
+ *   gn           [D] fp32 norm weight.
+ *   eps          >= 0, finite.
+ *   out          [batch] rows of NV*D bf16 (raw uint16 bits), written,
+ *                rounded to nearest even.
+ *   Other arguments and errors as gdn_decode.
+ */
+GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
+                            const float *q, const float *k, const float *v,
+                            const float *alpha, const float *beta,
+                            const float *z, const float *gn, float eps,
+                            uint16_t *out,
+                            int batch, int nk, int nv, int d,
+                            int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                            int64_t z_stride, int64_t out_stride, void *stream);
+
+/*
+ * gdn_prefill_seq -- seq_len tokens per sequence through the recurrence in
+ * one launch, token by token in order, the state held on chip between
+ * tokens; writes the raw fp32 o of every token (no norm).
+ *   Defined by: ssm_gdn_a.rs, launcher `gdn_prefill_regresident`
+ *   (token-sequential prefill with the state in registers); the step is
+ *   gdn.rs `gdn_step`.
+ *   state        as gdn_decode; only GDN_STATE_F32 (GDN_ERR_UNSUPPORTED
+ *                otherwise).
+ *   q, k         [batch * seq_len] rows of NK*D, row b*seq_len + t.
+ *   v            [batch * seq_len] rows of NV*D.
+ *   alpha, beta  [batch * seq_len] rows of NV.
+ *   o            [batch * seq_len] rows of NV*D, written.
+ *   Splitting seq_len into consecutive calls gives the same result as one
+ *   call, up to fp32 rounding order.
+ *   Errors as gdn_decode.
+ */
+GDN_API int gdn_prefill_seq(void *state, int state_dtype, int64_t state_pitch,
+                            const float *q, const float *k, const float *v,
+                            const float *alpha, const float *beta, float *o,
+                            int batch, int seq_len, int nk, int nv, int d,
+                            int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                            int64_t o_stride, void *stream);
+
+/*
+ * gdn_h_f32_to_f16 -- n h-state elements binary32 -> binary16, round to
+ * nearest, ties to even (overflow to +-inf, subnormals kept, NaN stays NaN).
+ *   Defined by: ssm_gdn_a.rs, launcher `ssm_h_state_f32_to_f16`.
+ *   src [n] fp32, dst [n] fp16 bits.  src and dst must not overlap
+ *   (GDN_ERR_ALIAS): an in-place narrowing conversion would race.
+ */
+GDN_API int gdn_h_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, void *stream);
+
+/*
+ * gdn_h_f16_to_f32 -- n h-state elements binary16 -> binary32, exact.
+ *   Defined by: ssm_gdn_a.rs, launcher `ssm_h_state_f16_to_f32`.
+ *   src [n] fp16 bits, dst [n] fp32; no overlap (GDN_ERR_ALIAS).
+ */
+GDN_API int gdn_h_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+GDN_API const char *gdn_status_str(int status);
+
+/* The cudaError_t of the last GDN_ERR_CUDA returned on the calling host
+ * thread (0 if none). */
+GDN_API int gdn_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,150 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports exactly the
+entry points include/gdn.h declares, and rejects bad arguments on the host
+before any CUDA call (so a rejected call touches no memory)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gated_deltanet_linear_16_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+OK, ARG, UNSUP, ALIGN, ALIAS, CUDA = 0, 1, 2, 3, 4, 5
+A = 1 << 20          # fake, 16-byte aligned "device" addresses: never dereferenced by a rejected call
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"GDN_API\s+[\w\s\*]*?\b(gdn_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    gdn.build()
+    return gdn.load()
+
+
+@pytest.fixture(scope="module")
+def lib(built):
+    """The library, for calls with fake addresses: only where no CUDA device exists, so a
+    call that wrongly passed validation could never reach a real GPU."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("fake-pointer validation tests run only on hosts without a GPU")
+    return built
+
+
+def test_exports_match_header(built):
+    want = declared_symbols()
+    assert want == sorted(["gdn_decode", "gdn_decode_norm", "gdn_prefill_seq", "gdn_h_f32_to_f16",
+                           "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error"])
+    out = subprocess.run(["nm", "-D", "--defined-only", gdn.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = sorted({line.split()[-1] for line in out.splitlines() if line.split()[-1].startswith("gdn_")})
+    assert exported == want
+    for name in want:
+        assert hasattr(built, name)
+
+
+def test_status_strings(built):
+    for code in range(6):
+        assert gdn.gdn_status_str(code).startswith(gdn.STATUS[code])
+    assert gdn.gdn_status_str(99) == "GDN_ERR_UNKNOWN"
+
+
+def decode(lib, **kw):
+    a = dict(state=A, dt=0, pitch=48 * 128 * 128, q=A + (1 << 30), k=A + (2 << 30), v=A + (3 << 30),
+             alpha=A + (4 << 30), beta=A + (5 << 30), o=A + (6 << 30), batch=2, nk=16, nv=48, d=128,
+             qk=16 * 128, vs=48 * 128, gb=48, os=48 * 128)
+    a.update(kw)
+    return lib.gdn_decode(a["state"], a["dt"], a["pitch"], a["q"], a["k"], a["v"], a["alpha"], a["beta"],
+                          a["o"], a["batch"], a["nk"], a["nv"], a["d"], a["qk"], a["vs"], a["gb"], a["os"], None)
+
+
+def decode_norm(lib, **kw):
+    a = dict(state=A, dt=1, pitch=4 * 4 * 4, q=A + (1 << 30), k=A + (2 << 30), v=A + (3 << 30),
+             alpha=A + (4 << 30), beta=A + (5 << 30), z=A + (7 << 30), gn=A + (8 << 30), eps=1e-6,
+             out=A + (6 << 30), batch=2, nk=1, nv=4, d=4, qk=4, vs=16, gb=4, zs=16, outs=16)
+    a.update(kw)
+    return lib.gdn_decode_norm(a["state"], a["dt"], a["pitch"], a["q"], a["k"], a["v"], a["alpha"], a["beta"],
+                               a["z"], a["gn"], a["eps"], a["out"], a["batch"], a["nk"], a["nv"], a["d"],
+                               a["qk"], a["vs"], a["gb"], a["zs"], a["outs"], None)
+
+
+def prefill(lib, **kw):
+    a = dict(state=A, dt=0, pitch=3 * 128 * 128, q=A + (1 << 30), k=A + (2 << 30), v=A + (3 << 30),
+             alpha=A + (4 << 30), beta=A + (5 << 30), o=A + (6 << 30), batch=2, T=5, nk=1, nv=3, d=128,
+             qk=128, vs=3 * 128, gb=3, os=3 * 128)
+    a.update(kw)
+    return lib.gdn_prefill_seq(a["state"], a["dt"], a["pitch"], a["q"], a["k"], a["v"], a["alpha"], a["beta"],
+                               a["o"], a["batch"], a["T"], a["nk"], a["nv"], a["d"], a["qk"], a["vs"], a["gb"],
+                               a["os"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(state=None), ARG), (dict(q=None), ARG), (dict(o=None), ARG), (dict(beta=None), ARG),
+    (dict(batch=-1), ARG), (dict(nk=0), ARG), (dict(nv=0), ARG), (dict(d=0), ARG),
+    (dict(d=257, pitch=48 * 257 * 257, qk=16 * 257, vs=48 * 257, os=48 * 257), UNSUP),
+    (dict(dt=2), UNSUP),
+    (dict(pitch=48 * 128 * 128 - 1), ARG),               # slot pitch shorter than NV*D*D
+    (dict(qk=16 * 128 - 1), ARG), (dict(vs=48 * 128 - 4), ARG), (dict(gb=47), ARG), (dict(os=100), ARG),
+    (dict(q=A + (1 << 30) + 2), ALIGN),                  # fp32 pointer not 4-byte aligned
+    (dict(state=A + 1, dt=1), ALIGN),                    # fp16 state not 2-byte aligned
+    (dict(o=A + 4096), ALIAS),                           # output inside the state
+    (dict(o=A + (1 << 30) + 64), ALIAS),                 # output overlapping q
+    (dict(q=A + 8), ALIAS),                              # input inside the state (state is written)
+])
+def test_decode_rejects(lib, kw, want):
+    assert decode(lib, **kw) == want
+
+
+def test_decode_empty_batch_is_ok(lib):
+    assert decode(lib, batch=0) == OK
+    assert decode(lib, batch=0, q=None) == ARG
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(eps=-1.0), ARG), (dict(eps=float("inf")), ARG), (dict(eps=float("nan")), ARG),
+    (dict(z=None), ARG), (dict(gn=None), ARG), (dict(out=None), ARG),
+    (dict(out=A + (6 << 30) + 1), ALIGN),                # bf16 output not 2-byte aligned
+    (dict(zs=15), ARG), (dict(outs=15), ARG),
+    (dict(out=A + (8 << 30) + 8), ALIAS),                # output on top of gn
+])
+def test_decode_norm_rejects(lib, kw, want):
+    assert decode_norm(lib, **kw) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(dt=1), UNSUP), (dict(T=-1), ARG), (dict(o=None), ARG),
+    (dict(os=10), ARG), (dict(o=A + 100), ALIAS),
+])
+def test_prefill_rejects(lib, kw, want):
+    assert prefill(lib, **kw) == want
+
+
+def test_prefill_empty_is_ok(lib):
+    assert prefill(lib, T=0) == OK
+    assert prefill(lib, batch=0) == OK
+
+
+def test_converters_reject(lib):
+    f = lib.gdn_h_f32_to_f16
+    g = lib.gdn_h_f16_to_f32
+    assert f(None, A, 10, None) == ARG and g(A, None, 10, None) == ARG
+    assert f(A, A + (1 << 30), 0, None) == OK and g(A, A + (1 << 30), 0, None) == OK
+    assert f(A + 1, A + (1 << 30), 10, None) == ALIGN
+    assert g(A + 1, A + (1 << 30), 10, None) == ALIGN
+    assert f(A, A + 8, 10, None) == ALIAS            # in-place narrowing would race
+    assert g(A + 16, A, 10, None) == ALIAS
+
+
+def test_converter_adjacent_ranges_are_not_alias(lib):
+    # [A, A+40) and [A+40, A+60): touching, not overlapping -> passes the alias check.  With no GPU
+    # the launch itself fails, which must come back as GDN_ERR_CUDA, not a crash.
+    st = lib.gdn_h_f32_to_f16(A, A + 40, 10, None)
+    assert st == CUDA
+    assert lib.gdn_last_cuda_error() != 0

@@ -1,0 +1,95 @@
+"""GPU parity: gdn_decode / gdn_decode_norm (fp32 and fp16 h-state) against the fp64 oracle.
+
+Sizes are small enough for the oracle to finish in seconds yet span several
+CTAs, ragged head counts (NV not a multiple of NK), strided rows with padding,
+padded slot pitches, tiny and odd D (general kernel) and D = 128 (vector
+kernel), and misaligned bases that force the general kernel at D = 128."""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_16_gb300 as gdn
+from tests.gpu_helpers import check_decode, run_decode_case, Rows, state_pool
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _lib(cuda_lib):
+    return cuda_lib
+
+
+@pytest.mark.parametrize("norm", [True, False])
+def test_tiny_config_64_steps(norm):
+    """Batch 1, NK = 1, NV = 2, D = 4, 64 sequential steps from a zero state."""
+    r = run_decode_case(1, 1, 2, 4, 64, norm=norm, init="zero")
+    check_decode(r, f16=False, norm=norm)
+
+
+@pytest.mark.parametrize("f16", [False, True])
+@pytest.mark.parametrize("norm", [True, False])
+def test_d128_vector_path(f16, norm):
+    r = run_decode_case(3, 2, 5, 128, 6, f16=f16, norm=norm, seed=1)
+    check_decode(r, f16=f16, norm=norm)
+
+
+@pytest.mark.parametrize("f16", [False, True])
+def test_d128_strided_rows_and_padded_pitch(f16):
+    """Row padding on every operand (multiples of 4 floats keep the vector path) and 4096 slot padding."""
+    r = run_decode_case(4, 2, 6, 128, 4, f16=f16, norm=True, seed=2, pad=(8, 4, 3, 12, 6), pitch_pad=4096)
+    check_decode(r, f16=f16, norm=True)
+
+
+@pytest.mark.parametrize("f16", [False, True])
+@pytest.mark.parametrize("norm", [True, False])
+def test_d128_misaligned_takes_general_kernel(f16, norm):
+    r = run_decode_case(2, 2, 3, 128, 3, f16=f16, norm=norm, seed=3, misalign=1, pad=(1, 0, 0, 0, 0))
+    check_decode(r, f16=f16, norm=norm)
+
+
+@pytest.mark.parametrize("D", [1, 2, 5, 31, 33, 64, 96, 127, 200, 256])
+@pytest.mark.parametrize("f16", [False, True])
+def test_general_kernel_any_d(D, f16):
+    r = run_decode_case(2, 2, 3, D, 3, f16=f16, norm=True, seed=D)
+    check_decode(r, f16=f16, norm=True)
+
+
+def test_many_heads_several_waves():
+    """B * NV = 640 CTAs: several waves over the SMs, with NV = 40 not a multiple of NK = 16."""
+    r = run_decode_case(16, 16, 40, 128, 2, f16=False, norm=True, seed=4)
+    check_decode(r, f16=False, norm=True)
+
+
+@pytest.mark.parametrize("f16", [False, True])
+def test_alpha_one_beta_zero_leaves_state_bitwise(f16):
+    """alpha = 1, beta = 0: coef = 0 and S <- fma(0, k, 1 * S) = S exactly, on both kernels."""
+    for D in (128, 48):
+        r = run_decode_case(2, 2, 3, D, 3, f16=f16, norm=True, seed=5, alpha=1.0, beta=0.0)
+        assert r["intact"]
+        assert np.array_equal(r["S_gpu"], r["S_ref"])
+
+
+def test_beta_zero_is_pure_decay_on_gpu():
+    """beta = 0: S_T = (prod alpha) S_0 up to fp32 rounding of the products."""
+    r = run_decode_case(2, 2, 4, 128, 5, norm=False, seed=6, beta=0.0)
+    check_decode(r, f16=False, norm=False)
+
+
+def test_empty_batch_is_a_no_op():
+    st = state_pool(1, 2, 128, False)
+    before = st.raw.clone()
+    q = Rows(1, 256)
+    gdn.gdn_decode(st.ptr, q.ptr, q.ptr, q.ptr, q.ptr, q.ptr, Rows(1, 256).ptr, batch=0, nk=2, nv=2, d=128)
+    torch.cuda.synchronize()
+    assert torch.equal(before, st.raw)
+
+
+def test_rejected_call_raises_and_touches_nothing():
+    st = state_pool(1, 2, 128, False)
+    before = st.raw.clone()
+    q = Rows(1, 256)
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_decode(st.ptr, q.ptr, q.ptr, q.ptr, q.ptr, q.ptr, st.ptr + 64, batch=1, nk=2, nv=2, d=128)
+    assert e.value.status == 4           # output inside the state
+    torch.cuda.synchronize()
+    assert torch.equal(before, st.raw)

@@ -1,0 +1,63 @@
+"""GPU parity: gdn_prefill_seq against the fp64 oracle's token-sequential prefill."""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_16_gb300 as gdn
+from tests.gpu_helpers import TOL_F32, Rows, run_prefill_case, state_pool
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _lib(cuda_lib):
+    return cuda_lib
+
+
+def check(r):
+    assert r["intact"], "guard band or padding overwritten"
+    assert r["state_max_rel"] <= TOL_F32, r["state_max_rel"]
+    assert r["o_max_rel"] <= TOL_F32, r["o_max_rel"]
+
+
+@pytest.mark.parametrize("T", [1, 7, 8, 9, 37])
+def test_d128_register_resident(T):
+    """Ragged token counts around the 8-token staging chunk; NV = 3 over NK = 2."""
+    check(run_prefill_case(2, 2, 3, 128, T, seed=T))
+
+
+def test_d128_from_random_state_with_strides():
+    check(run_prefill_case(2, 2, 5, 128, 20, seed=11, init="normal", pad=(4, 8, 1, 3), pitch_pad=4096))
+
+
+def test_d128_long_sequence():
+    check(run_prefill_case(1, 2, 4, 128, 300, seed=12, init="normal"))
+
+
+def test_d128_split_calls_equal_one_call():
+    """Two consecutive calls (T1 + T2, per sequence) match the oracle's single pass."""
+    check(run_prefill_case(2, 2, 3, 128, 29, seed=13, init="normal", splits=(13, 16)))
+
+
+def test_d128_misaligned_takes_general_kernel():
+    check(run_prefill_case(2, 2, 3, 128, 9, seed=14, misalign=1, pad=(1, 0, 0, 0)))
+
+
+@pytest.mark.parametrize("D", [1, 4, 33, 64, 100, 256])
+def test_general_kernel_any_d(D):
+    check(run_prefill_case(2, 2, 3, D, 11, seed=D, init="normal"))
+
+
+def test_many_warps():
+    """B * NV * D / 32 = 1280 one-warp CTAs: more than one per SM slot on some SMs."""
+    check(run_prefill_case(4, 16, 80, 128, 5, seed=15, init="normal"))
+
+
+def test_empty_sequence_is_a_no_op():
+    st = state_pool(1, 2, 128, False)
+    before = st.raw.clone()
+    q = Rows(1, 256)
+    gdn.gdn_prefill_seq(st.ptr, q.ptr, q.ptr, q.ptr, q.ptr, q.ptr, Rows(1, 256).ptr,
+                        batch=1, seq_len=0, nk=2, nv=2, d=128)
+    torch.cuda.synchronize()
+    assert torch.equal(before, st.raw)
