@@ -1,0 +1,187 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration bench.py times.
+
+The oracle cannot afford every head at these sizes, so each test checks a
+seeded sample of heads (drawn with the counter-based generator, so the sampled
+heads' inputs are exactly the generator's) element by element, plus
+properties that hold at any size (finite results, untouched padding, bit-exact
+converters over the whole pool).  Heads outside the sample are filled with
+torch's normal generator at the same distribution: heads never interact, so
+they cannot affect the sampled ones."""
+import numpy as np
+import pytest
+import torch
+
+import gdn_synth as gs
+import gated_deltanet_linear_16_gb300 as gdn
+import oracle
+from tests.gpu_helpers import TOL_F32, TOL_REL_L2, bf16_to_f64, max_rel_err, rel_l2, run_decode_case
+
+pytestmark = pytest.mark.gpu
+
+NK, NV, D = 16, 48, 128
+EPS = 1e-6
+SEED = 0
+
+
+@pytest.fixture(autouse=True)
+def _lib(cuda_lib):
+    yield cuda_lib
+    torch.cuda.empty_cache()
+
+
+def test_single_layer_256_steps():
+    """Batch 1, one Qwen3.8-27B-shaped GDN layer, 256 sequential steps, fused norm -> bf16: every head."""
+    r = run_decode_case(1, NK, NV, D, 256, norm=True, seed=SEED)
+    assert r["intact"]
+    assert r["state_max_rel"] <= TOL_F32, r["state_max_rel"]
+    assert r["out_worst"] <= TOL_REL_L2, r["out_worst"]
+
+
+def test_batched_48_layers_one_token():
+    """Batch 32, 48 layers, fp32 state [32][48][48][128][128] (4.83 GB), one fused launch per layer."""
+    B, L = 32, 48
+    dev = torch.device("cuda")
+    state = torch.empty((B, L, NV, D, D), dtype=torch.float32, device=dev)
+    for b in range(B):
+        state[b].normal_(0.0, 0.02)
+    rng = np.random.default_rng(7)
+    sample = [(int(rng.integers(B)), l, int(rng.integers(NV))) for l in range(L) for _ in range(2)]
+    S0 = {}
+    for (b, l, h) in sample:
+        s0 = gs.state_heads(SEED, [b], [h], D, layer=l)[0, 0]
+        S0[(b, l, h)] = s0
+        state[b, l, h] = torch.from_numpy(s0).to(dev)
+    xs = [gs.decode_inputs(SEED, B, NK, NV, D, layer=l) for l in range(L)]
+    gns = [gs.norm_weight(SEED, D, layer=l) for l in range(L)]
+    dx = {n: torch.from_numpy(np.stack([x[n] for x in xs])).to(dev) for n in xs[0]}
+    dgn = torch.from_numpy(np.stack(gns)).to(dev)
+    out = torch.empty((L, B, NV * D), dtype=torch.int16, device=dev)
+    for l in range(L):
+        gdn.gdn_decode_norm(state.data_ptr() + l * NV * D * D * 4, dx["q"][l], dx["k"][l], dx["v"][l],
+                            dx["alpha"][l], dx["beta"][l], dx["z"][l], dgn[l], out[l],
+                            batch=B, nk=NK, nv=NV, d=D, eps=EPS, state_pitch=L * NV * D * D)
+    torch.cuda.synchronize()
+    assert torch.isfinite(state).all().item()
+    worst_s, worst_o = 0.0, 0.0
+    for (b, l, h) in sample:
+        x, g = xs[l], h % NK
+        S = S0[(b, l, h)].astype(np.float64)[None, None]
+        o = oracle.decode(S, x["q"][b:b + 1, g * D:(g + 1) * D], x["k"][b:b + 1, g * D:(g + 1) * D],
+                          x["v"][b:b + 1, h * D:(h + 1) * D], x["alpha"][b:b + 1, h:h + 1],
+                          x["beta"][b:b + 1, h:h + 1], 1)
+        ref_out = oracle.gated_rmsnorm(o, x["z"][b:b + 1, h * D:(h + 1) * D], gns[l], EPS)
+        got_s = state[b, l, h].cpu().numpy().astype(np.float64)
+        got_o = bf16_to_f64(out[l, b, h * D:(h + 1) * D].cpu().numpy())
+        worst_s = max(worst_s, max_rel_err(got_s, S[0, 0]))
+        worst_o = max(worst_o, rel_l2(got_o, ref_out[0]))
+    assert worst_s <= TOL_F32, worst_s
+    assert worst_o <= TOL_REL_L2, worst_o
+
+
+def test_fp16_pool_16_steps_and_converters():
+    """Batch 256 fp16 pool, pitch 48*128*128 + 4096 halves: the f16 -> f32 -> f16 round trip over the
+    whole pool, bit-exact against the oracle's IEEE rounding; then 16 steps with the fused norm."""
+    PB, T = 256, 16
+    hs = NV * D * D
+    pitch = hs + 4096
+    dev = torch.device("cuda")
+    pool = torch.zeros((PB, pitch), dtype=torch.float16, device=dev)
+    pool[:, :hs].normal_(0.0, 0.02)
+    sample_slots = [0, 77, 255]
+    S = {}
+    for b in sample_slots:
+        s0 = gs.state_heads(SEED, [b], range(NV), D, dtype=np.float16)[0]
+        pool[b, :hs] = torch.from_numpy(s0.reshape(-1)).to(dev)
+        S[b] = s0.astype(np.float64)[None]
+
+    # converters over the whole pool (padding included), on the initial pool, whose contents come
+    # from the generator and torch's RNG only
+    n = PB * pitch
+    f32 = torch.empty(n, dtype=torch.float32, device=dev)
+    gdn.gdn_h_f16_to_f32(pool, f32, n)
+    back = torch.empty(n, dtype=torch.float16, device=dev)
+    gdn.gdn_h_f32_to_f16(f32, back, n)
+    torch.cuda.synchronize()
+    assert torch.equal(back.view(torch.int16), pool.view(-1).view(torch.int16))
+    host16 = pool.view(-1).view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(f32.view(torch.int32).cpu().numpy().view(np.uint32), oracle.f16_to_f32_bits(host16))
+    del f32
+    # narrowing with real rounding work: host-built fp32 values carrying bits below binary16 precision
+    wide = host16.view(np.float16).astype(np.float32) * np.float32(1.0 + 2.0 ** -12) + np.float32(1e-9)
+    dwide = torch.from_numpy(wide).to(dev)
+    gdn.gdn_h_f32_to_f16(dwide, back, n)
+    torch.cuda.synchronize()
+    want = oracle.f32_to_f16_bits(wide)
+    assert np.array_equal(back.view(torch.int16).cpu().numpy().view(np.uint16), want)
+    del dwide, back, wide, host16
+    torch.cuda.empty_cache()
+
+    # 16 decode steps with the fused norm
+    gn = gs.norm_weight(SEED, D)
+    dgn = torch.from_numpy(gn).to(dev)
+    out = torch.empty((PB, NV * D), dtype=torch.int16, device=dev)
+    worst_o = 0.0
+    for t in range(T):
+        x = gs.decode_inputs(SEED, PB, NK, NV, D, step=t)
+        dx = {k: torch.from_numpy(v).to(dev) for k, v in x.items()}
+        gdn.gdn_decode_norm(pool, dx["q"], dx["k"], dx["v"], dx["alpha"], dx["beta"], dx["z"], dgn, out,
+                            batch=PB, nk=NK, nv=NV, d=D, eps=EPS, state_pitch=pitch)
+        torch.cuda.synchronize()
+        for b in sample_slots:
+            o = oracle.decode(S[b], x["q"][b:b + 1], x["k"][b:b + 1], x["v"][b:b + 1],
+                              x["alpha"][b:b + 1], x["beta"][b:b + 1], NK)
+            ref = oracle.gated_rmsnorm(o.reshape(NV, D), x["z"][b].reshape(NV, D), gn, EPS)
+            got = bf16_to_f64(out[b].cpu().numpy()).reshape(NV, D)
+            worst_o = max(worst_o, rel_l2(got, ref))
+    assert worst_o <= TOL_REL_L2, worst_o
+    for b in sample_slots:
+        got = pool[b, :hs].float().cpu().numpy().astype(np.float64).reshape(1, NV, D, D)
+        assert rel_l2(got, S[b]) <= TOL_REL_L2
+    assert torch.count_nonzero(pool[:, hs:]).item() == 0, "slot padding (canary) was written"
+    assert torch.isfinite(pool).all().item()
+
+
+def test_prefill_4096_tokens():
+    """Batch 8, T = 4096 tokens in one call, fp32 state from zero; sampled heads over every token."""
+    B, T = 8, 4096
+    R = B * T
+    dev = torch.device("cuda")
+    q = torch.randn((R, NK * D), device=dev)
+    k = torch.randn((R, NK * D), device=dev)
+    q = (q.view(R, NK, D) / q.view(R, NK, D).norm(dim=-1, keepdim=True)).reshape(R, NK * D).contiguous()
+    k = (k.view(R, NK, D) / k.view(R, NK, D).norm(dim=-1, keepdim=True)).reshape(R, NK * D).contiguous()
+    v = torch.randn((R, NV * D), device=dev)
+    a = torch.sigmoid(torch.randn((R, NV), device=dev) + 2.0)
+    bt = torch.sigmoid(torch.randn((R, NV), device=dev))
+    seqs = [2, 5]
+    xs = gs.prefill_inputs(SEED, B, T, NK, NV, D, seqs=seqs)
+    for i, b in enumerate(seqs):
+        rows = slice(b * T, (b + 1) * T)
+        q[rows] = torch.from_numpy(xs["q"][i]).to(dev)
+        k[rows] = torch.from_numpy(xs["k"][i]).to(dev)
+        v[rows] = torch.from_numpy(xs["v"][i]).to(dev)
+        a[rows] = torch.from_numpy(xs["alpha"][i]).to(dev)
+        bt[rows] = torch.from_numpy(xs["beta"][i]).to(dev)
+    o = torch.empty((R, NV * D), device=dev)
+    S = torch.zeros((B, NV, D, D), device=dev)
+    gdn.gdn_prefill_seq(S, q, k, v, a, bt, o, batch=B, seq_len=T, nk=NK, nv=NV, d=D)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all().item() and torch.isfinite(S).all().item()
+    heads = [(0, 0), (0, 17), (0, 47), (1, 3), (1, 16), (1, 40)]
+
+    def one(ih):
+        i, h = ih
+        g = h % NK
+        Sref = np.zeros((1, 1, D, D))
+        oref = oracle.prefill(Sref, xs["q"][i:i + 1, :, g * D:(g + 1) * D], xs["k"][i:i + 1, :, g * D:(g + 1) * D],
+                              xs["v"][i:i + 1, :, h * D:(h + 1) * D], xs["alpha"][i:i + 1, :, h:h + 1],
+                              xs["beta"][i:i + 1, :, h:h + 1], 1)
+        return Sref, oref
+
+    refs = oracle.parallel_map(one, heads)
+    for (i, h), (Sref, oref) in zip(heads, refs):
+        b = seqs[i]
+        got_o = o[b * T:(b + 1) * T, h * D:(h + 1) * D].cpu().numpy().astype(np.float64)
+        got_s = S[b, h].cpu().numpy().astype(np.float64)
+        assert max_rel_err(got_o, oref[0]) <= TOL_F32
+        assert max_rel_err(got_s, Sref[0, 0]) <= TOL_F32
