@@ -33,8 +33,6 @@ namespace gdn {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kWarps = 8;
-constexpr int kRowsPerWarp = kD / kWarps;   // 16
 
 // A 16-byte vector of state elements, widened to / narrowed from fp32.
 template <typename TS> struct Vec16;
@@ -82,18 +80,28 @@ template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return
 
 // ------------------------------------------------------------------ D == 128
 
-template <typename TS> struct FastOcc { static constexpr int kMinBlocks = 2; };
-template <> struct FastOcc<__half> { static constexpr int kMinBlocks = 3; };
+// Shape of the D == 128 kernel: WARPS warps share one head (128 / WARPS rows
+// each); each lane's state loads are issued in NB batches, batch b + 1 in
+// flight while batch b is computed (NB == 1: everything in flight at once).
+template <typename TS> struct FastShape {
+    static constexpr int kWarps = 8, kBatches = 1, kMinBlocks = 2;
+};
+template <> struct FastShape<__half> {
+    static constexpr int kWarps = 8, kBatches = 1, kMinBlocks = 3;
+};
 
-template <typename TS, bool NORM>
-__global__ void __launch_bounds__(kWarps * 32, FastOcc<TS>::kMinBlocks)
+template <typename TS, bool NORM, int WARPS, int NB, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
 decode_d128(const DecodeParams p)
 {
     using V = Vec16<TS>;
     constexpr int EPV = V::N;                  // state elements per 16-byte vector
     constexpr int LPR = kD / EPV;              // lanes per state row: 32 fp32, 16 fp16
     constexpr int RPL = 32 / LPR;              // rows per warp-wide load: 1 fp32, 2 fp16
-    constexpr int NLD = kRowsPerWarp / RPL;    // 16-byte state loads per lane
+    constexpr int RPW = kD / WARPS;            // rows per warp
+    constexpr int NLD = RPW / RPL;             // 16-byte state loads per lane
+    constexpr int LPB = NLD / NB;              // loads per batch
+    static_assert(RPW <= 32 && NLD % NB == 0, "shape");
 
     const int unit = blockIdx.x;               // (sequence, value head)
     const int seq = unit / p.nv;
@@ -103,15 +111,15 @@ decode_d128(const DecodeParams p)
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR;                // which row of a warp-wide load
     const int col = (lane % LPR) * EPV;        // first column this lane owns
-    const int row0 = warp * kRowsPerWarp;
+    const int row0 = warp * RPW;
 
     TS *S = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD;
     TS *rowp = S + (int64_t)(row0 + sub) * kD + col;
 
-    // 1. the whole slice of the state this lane owns, in flight at once
-    uint4 raw[NLD];
+    // 1. the first batch of this lane's state slice, in flight before anything else
+    uint4 raw[NB > 1 ? 2 : 1][LPB];
 #pragma unroll
-    for (int i = 0; i < NLD; ++i) raw[i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
+    for (int i = 0; i < LPB; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
 
     // 2. token inputs
     const float *kp = p.k + seq * p.qk_stride + (int64_t)g * kD + col;
@@ -123,7 +131,7 @@ decode_d128(const DecodeParams p)
         kx[j] = a.x; kx[j + 1] = a.y; kx[j + 2] = a.z; kx[j + 3] = a.w;
         qx[j] = b.x; qx[j + 1] = b.y; qx[j + 2] = b.z; qx[j + 3] = b.w;
     }
-    const bool row_lane = lane < kRowsPerWarp;  // lane r carries row row0 + r
+    const bool row_lane = lane < RPW;          // lane r carries row row0 + r
     const float v_l = row_lane ? __ldg(p.v + seq * p.v_stride + (int64_t)h * kD + row0 + lane) : 0.f;
     float z_l = 0.f, gn_l = 0.f;
     if (NORM && row_lane) {
@@ -139,29 +147,38 @@ decode_d128(const DecodeParams p)
     kq = group_sum<LPR>(kq);
 
     // 3. per row: two dot products, the delta coefficient, output, write-back
-    float o_keep = 0.f;                        // lane r < 16 keeps o of row row0 + r
+    float o_keep = 0.f;                        // lane r keeps o of row row0 + r
 #pragma unroll
-    for (int i = 0; i < NLD; ++i) {
-        float s[EPV];
-        V::unpack(raw[i], s);
-        float u = 0.f, w = 0.f;
+    for (int bt = 0; bt < NB; ++bt) {
+        if (bt + 1 < NB) {
 #pragma unroll
-        for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
-        u = group_sum<LPR>(u);
-        w = group_sum<LPR>(w);
-        const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
-        const float coef = beta * (va - alpha * u);
-        const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
+            for (int i = 0; i < LPB; ++i)
+                raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * LPB + i) * RPL * kD);
+        }
 #pragma unroll
-        for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
-        st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
-        if constexpr (RPL == 1) {
-            if (lane == i) o_keep = oa;
-        } else {
+        for (int ii = 0; ii < LPB; ++ii) {
+            const int i = bt * LPB + ii;       // load index within the lane's slice
+            float s[EPV];
+            V::unpack(raw[bt & 1][ii], s);
+            float u = 0.f, w = 0.f;
 #pragma unroll
-            for (int r = 0; r < RPL; ++r) {
-                const float orr = __shfl_sync(kFull, oa, r * LPR);
-                if (lane == i * RPL + r) o_keep = orr;
+            for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
+            u = group_sum<LPR>(u);
+            w = group_sum<LPR>(w);
+            const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
+            const float coef = beta * (va - alpha * u);
+            const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
+            st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
+            if constexpr (RPL == 1) {
+                if (lane == i) o_keep = oa;
+            } else {
+#pragma unroll
+                for (int r = 0; r < RPL; ++r) {
+                    const float orr = __shfl_sync(kFull, oa, r * LPR);
+                    if (lane == i * RPL + r) o_keep = orr;
+                }
             }
         }
     }
@@ -170,13 +187,13 @@ decode_d128(const DecodeParams p)
         if (row_lane) p.o[seq * p.o_stride + (int64_t)h * kD + row0 + lane] = o_keep;
     } else {
         // 4. gated RMS norm over the head's 128 outputs, in this CTA
-        __shared__ float red[kWarps];
-        const float ss = group_sum<32>(o_keep * o_keep);   // lanes >= 16 hold 0
+        __shared__ float red[WARPS];
+        const float ss = group_sum<32>(o_keep * o_keep);   // lanes >= RPW hold 0
         if (lane == 0) red[warp] = ss;
         __syncthreads();
         float tot = 0.f;
 #pragma unroll
-        for (int i = 0; i < kWarps; ++i) tot += red[i];
+        for (int i = 0; i < WARPS; ++i) tot += red[i];
         const float rstd = rsqrtf(tot * (1.0f / kD) + p.eps);
         if (row_lane) {
             const float y = gn_l * o_keep * rstd * silu(z_l);
@@ -275,7 +292,8 @@ template <typename TS, bool NORM>
 cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
 {
     const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
-    if (fast) decode_d128<TS, NORM><<<grid, kWarps * 32, 0, s>>>(p);
+    using F = FastShape<TS>;
+    if (fast) decode_d128<TS, NORM, F::kWarps, F::kBatches, F::kMinBlocks><<<grid, F::kWarps * 32, 0, s>>>(p);
     else decode_generic<TS, NORM><<<grid, kGenWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
