@@ -79,7 +79,8 @@ def test_empty_batch_is_a_no_op():
     st = state_pool(1, 2, 128, False)
     before = st.raw.clone()
     q = Rows(1, 256)
-    gdn.gdn_decode(st.ptr, q.ptr, q.ptr, q.ptr, q.ptr, q.ptr, Rows(1, 256).ptr, batch=0, nk=2, nv=2, d=128)
+    gdn.gdn_decode(st.ptr, q.ptr, q.ptr, q.ptr, q.ptr, q.ptr, Rows(1, 256).ptr, batch=0, nk=2, nv=2, d=128,
+                   state_dtype=gdn.GDN_STATE_F32)
     torch.cuda.synchronize()
     assert torch.equal(before, st.raw)
 
@@ -89,7 +90,8 @@ def test_rejected_call_raises_and_touches_nothing():
     before = st.raw.clone()
     q = Rows(1, 256)
     with pytest.raises(gdn.GdnError) as e:
-        gdn.gdn_decode(st.ptr, q.ptr, q.ptr, q.ptr, q.ptr, q.ptr, st.ptr + 64, batch=1, nk=2, nv=2, d=128)
+        gdn.gdn_decode(st.ptr, q.ptr, q.ptr, q.ptr, q.ptr, q.ptr, st.ptr + 64, batch=1, nk=2, nv=2, d=128,
+                       state_dtype=gdn.GDN_STATE_F32)
     assert e.value.status == 4           # output inside the state
     torch.cuda.synchronize()
     assert torch.equal(before, st.raw)

@@ -59,7 +59,8 @@ def test_batched_48_layers_one_token():
     for l in range(L):
         gdn.gdn_decode_norm(state.data_ptr() + l * NV * D * D * 4, dx["q"][l], dx["k"][l], dx["v"][l],
                             dx["alpha"][l], dx["beta"][l], dx["z"][l], dgn[l], out[l],
-                            batch=B, nk=NK, nv=NV, d=D, eps=EPS, state_pitch=L * NV * D * D)
+                            batch=B, nk=NK, nv=NV, d=D, eps=EPS, state_pitch=L * NV * D * D,
+                            state_dtype=gdn.GDN_STATE_F32)
     torch.cuda.synchronize()
     assert torch.isfinite(state).all().item()
     worst_s, worst_o = 0.0, 0.0

@@ -58,6 +58,7 @@ def test_empty_sequence_is_a_no_op():
     before = st.raw.clone()
     q = Rows(1, 256)
     gdn.gdn_prefill_seq(st.ptr, q.ptr, q.ptr, q.ptr, q.ptr, q.ptr, Rows(1, 256).ptr,
-                        batch=1, seq_len=0, nk=2, nv=2, d=128)
+                        batch=1, seq_len=0, nk=2, nv=2, d=128,
+                        state_dtype=gdn.GDN_STATE_F32)
     torch.cuda.synchronize()
     assert torch.equal(before, st.raw)
