@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-graph", action="store_true", help="launch every kernel from Python instead of "
+                    "replaying a captured CUDA graph")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers (a smaller case for profiling; not a bench line)")
     ap.add_argument("--prefill-tokens", type=int, default=4096,
@@ -190,6 +192,27 @@ def layer_launch(gdn, state, x, outb, l, stream_ptr, batch=B, f16=False, pitch=N
                         state_dtype=1 if f16 else 0, stream=stream_ptr)
 
 
+# ------------------------------------------------------------------ launch submission
+
+def graphed(torch, fn, stream, enable=True):
+    """Capture fn's launches once into a CUDA graph and return a replay function (the way a
+    decode step is replayed in a serving loop); falls back to calling fn directly if the
+    capture is not possible.  Returns (callable, used_graph)."""
+    if not enable:
+        return fn, False
+    try:
+        fn()                                   # warm (first-call set-up outside the capture)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay, True
+    except Exception:                          # capture unsupported here: plain launches
+        torch.cuda.synchronize()
+        return fn, False
+
+
 # ------------------------------------------------------------------ multi-rank host logic
 
 def max_over_ranks(ms_step, world, device):
@@ -231,9 +254,14 @@ def run_ours(args, rank, world, local_rank):
     x = make_layer_inputs(torch, B, L, dev)
     outb = torch.empty((L, B, NV * D), dtype=torch.int16, device=dev)
 
-    def step():
+    def launches():
+        # stream None: the binding launches on the current stream (the capture stream while
+        # the graph is being captured)
         for l in range(L):
-            layer_launch(gdn, state, x, outb, l, sp)
+            layer_launch(gdn, state, x, outb, l, None)
+
+    cap = torch.cuda.Stream(device=dev)
+    step, used_graph = graphed(torch, launches, cap, enable=not args.no_graph)
 
     for _ in range(args.warmup):
         step()
@@ -264,11 +292,12 @@ def run_ours(args, rank, world, local_rank):
     traffic = tr["bytes_per_launch"] if tr["src_sha256"] == src_sha("gdn_decode.cu") else None
 
     # ---- e2e: host inputs in pinned memory -> device, 48 launches, bf16 outputs -> host
-    e2e = None if args.no_e2e else run_e2e(args, torch, gdn, state, x, outb, dev, stream)
+    e2e = None if args.no_e2e else run_e2e(args, torch, gdn, state, x, outb, dev, stream, not args.no_graph)
     del state, x, outb
     torch.cuda.empty_cache()
 
-    rows = {} if args.no_rows else run_rows(torch, gdn, dev, stream, pk, args.rows_only, args.prefill_tokens)
+    rows = {} if args.no_rows else run_rows(torch, gdn, dev, stream, pk, args.rows_only, args.prefill_tokens,
+                                            graph=not args.no_graph)
     cpu = None if (args.no_cpu or rank != 0) else cpu_baseline(sample_layers=None)
 
     line = {
@@ -280,6 +309,7 @@ def run_ours(args, rank, world, local_rank):
                    "layers": L, "state": f"fp32 [32][{L}][48][128][128] = {B * L * NV * D * D * 4 / 1e9:.2f} GB per GPU",
                    "out": "bf16", "eps": EPS, "launches_per_step": L,
                    "l2": "inputs larger than L2 (4.83 GB state per step vs 129 MB L2)",
+                   "submission": "one CUDA graph replay per step" if used_graph else "eager launches",
                    "parallelism": f"dp{world}"},
         "roofline": {"bound": "hbm", "kernel": "decode_d128<float, norm>", "achieved": achieved,
                      "peak": pk["hbm_gbs"], "peak_source": pk["source"], "unit": "GB/s",
@@ -294,8 +324,11 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-def run_e2e(args, torch, gdn, state, x, outb, dev, stream):
-    """Same workload through the public API with per-step host<->device copies."""
+def run_e2e(args, torch, gdn, state, x, outb, dev, stream, graph=True):
+    """Same workload through the public API with per-step host<->device copies: the step's
+    token inputs from pinned host memory to the device, the layer calls, the bf16 outputs back
+    to pinned host memory (captured once into a CUDA graph and replayed, as a serving loop
+    would, unless graph is False)."""
     host = {k: v.cpu().pin_memory() for k, v in x.items() if k != "gn"}
     dev_in = {k: torch.empty_like(v) for k, v in host.items()}
     dev_in["gn"] = x["gn"]
@@ -304,13 +337,14 @@ def run_e2e(args, torch, gdn, state, x, outb, dev, stream):
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = host_out.numel() * host_out.element_size()
 
-    def step():
+    def launches():
         for k, v in host.items():
             dev_in[k].copy_(v, non_blocking=True)
         for l in range(outb.shape[0]):
-            layer_launch(gdn, state, dev_in, outb, l, sp)
+            layer_launch(gdn, state, dev_in, outb, l, None)
         host_out.copy_(outb, non_blocking=True)
 
+    step, used = graphed(torch, launches, torch.cuda.Stream(device=dev), enable=graph)
     steps = max(3, min(args.steps, 10))
     for _ in range(2):
         step()
@@ -323,6 +357,7 @@ def run_e2e(args, torch, gdn, state, x, outb, dev, stream):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     return {"value": B * NV * outb.shape[0] / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
+            "submission": "one CUDA graph replay per step (copies + launches)" if used else "eager",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
@@ -341,14 +376,14 @@ def time_fn(torch, stream, fn, reps, warm=2):
     return e0.elapsed_time(e1) / reps / 1e3     # seconds per call
 
 
-def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096):
+def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096, graph=True):
     want = set(only.split(",")) if only else {"fp16", "conv", "latency", "prefill"}
     rows = {}
     torch.cuda.empty_cache()
     if want & {"fp16", "conv"}:
         rows.update(row_fp16_pool(torch, gdn, dev, stream, pk, want))
     if "latency" in want:
-        rows.update(row_latency(torch, gdn, dev, stream))
+        rows.update(row_latency(torch, gdn, dev, stream, graph))
     if "prefill" in want:
         rows.update(row_prefill(torch, gdn, dev, stream, pk, prefill_tokens))
     return rows
@@ -391,14 +426,23 @@ def row_fp16_pool(torch, gdn, dev, stream, pk, want):
     return rows
 
 
-def row_latency(torch, gdn, dev, stream):
-    """One layer, batch 1 (3 MB state, L2-resident across steps): time per fused decode step."""
-    sp = stream.cuda_stream
+def row_latency(torch, gdn, dev, stream, graph=True):
+    """One layer, batch 1 (3 MB state, L2-resident across steps): time per fused decode step,
+    256 sequential steps replayed from one CUDA graph (launch submission excluded)."""
+    cap = torch.cuda.Stream(device=dev)
     st = torch.empty((1, NV, D, D), dtype=torch.float32, device=dev).normal_(0.0, 0.02)
     x1 = make_layer_inputs(torch, 1, 1, dev)
     o1 = torch.empty((1, 1, NV * D), dtype=torch.int16, device=dev)
-    s = time_fn(torch, stream, lambda: layer_launch(gdn, st, x1, o1, 0, sp, batch=1, pitch=NV * D * D), 256)
+    n = 256
+
+    def steps():
+        for _ in range(n):
+            layer_launch(gdn, st, x1, o1, 0, None, batch=1, pitch=NV * D * D)
+
+    fn, used = graphed(torch, steps, cap, enable=graph)
+    s = time_fn(torch, stream, fn, 4) / n
     return {"single_layer_latency": {"config": "B=1 NK=16 NV=48 D=128 fp32, fused norm (L2-resident)",
+                                     "submission": "CUDA graph of 256 steps" if used else "eager launches",
                                      "us_per_step": s * 1e6, "token_heads_per_s": NV / s}}
 
 

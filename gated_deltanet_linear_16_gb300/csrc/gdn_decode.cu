@@ -13,17 +13,18 @@
 //
 // GB300 design.  The state is ~99% of the bytes and is touched exactly once
 // (one read, one write per element), so the kernel is an HBM stream:
-//  * one CTA owns one (sequence, head): 8 warps x 16 rows, so the norm's
-//    reduction over the head's D outputs needs a single __syncthreads;
+//  * one CTA owns one (sequence, head) -- 4 warps x 32 rows (fp32) or 8 warps
+//    x 16 rows (fp16) -- so the norm's reduction over the head's D outputs
+//    needs a single __syncthreads;
 //  * every state access is a 16-byte vector: an fp32 row (512 B) is one
 //    warp-wide load, an fp16 row (256 B) half of one, so a warp touches whole
 //    128-byte lines and stores never leave partial sectors;
-//  * each lane issues all of its 16-byte state loads (16 for fp32, 8 for fp16)
-//    before it needs the first one, so a CTA keeps its whole head (64 KB fp32,
-//    32 KB fp16) in flight; with two or more CTAs per SM that is >= 128 KB of
-//    outstanding loads per SM, enough to cover HBM latency at full bandwidth;
+//  * each lane's state loads are issued in batches, the next batch in flight
+//    while the current one is computed and written back, with 4 CTAs per SM:
+//    about 64 KB of loads outstanding per SM, enough to cover HBM latency at
+//    full bandwidth while the stores of earlier rows drain;
 //  * k and q are read as this lane's own 16-byte columns, v/z/gn as one
-//    coalesced 64-byte read per warp that lanes then broadcast by shuffle;
+//    coalesced read per warp (a float per row) that lanes broadcast by shuffle;
 //  * the three dot products are butterfly shuffles inside the group of lanes
 //    that holds a row (32 lanes fp32, 16 lanes fp16); k.q is reduced once per
 //    warp, not per row.
@@ -83,11 +84,14 @@ template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return
 // Shape of the D == 128 kernel: WARPS warps share one head (128 / WARPS rows
 // each); each lane's state loads are issued in NB batches, batch b + 1 in
 // flight while batch b is computed (NB == 1: everything in flight at once).
+// Chosen by measurement on GB300 (48-layer fp32 workload, 256-slot fp16 pool):
+// fp32 4 warps x 32 rows, 4 batches of 8 loads, 4 CTAs per SM; fp16 8 warps x
+// 16 rows, 2 batches of 4 loads, 4 CTAs per SM.
 template <typename TS> struct FastShape {
-    static constexpr int kWarps = 8, kBatches = 1, kMinBlocks = 2;
+    static constexpr int kWarps = 4, kBatches = 4, kMinBlocks = 4;
 };
 template <> struct FastShape<__half> {
-    static constexpr int kWarps = 8, kBatches = 1, kMinBlocks = 3;
+    static constexpr int kWarps = 8, kBatches = 2, kMinBlocks = 4;
 };
 
 template <typename TS, bool NORM, int WARPS, int NB, int MINB>

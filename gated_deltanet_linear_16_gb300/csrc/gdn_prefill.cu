@@ -14,9 +14,17 @@
 //    reads, the same address for every lane;
 //  * o is read out of the updated state, o = S_new q / sqrt(D), which equals
 //    (alpha w + coef kq)/sqrt(D) and needs no per-token k.q;
-//  * a CTA is one warp (32 rows of one head).  With ~160 registers a thread
-//    an SM holds 12 such warps, and one-warp CTAs let the block scheduler
-//    spread the B*NV*D/32 warps evenly over the 152 SMs (a 4-warp CTA per head
+//  * the decay is deferred: the row is held as S = gam * R with a per-row
+//    scalar gam (the product of the alphas since the last fold), so a token
+//    costs three multiply-adds per element (u, the rank-1 write into R, o)
+//    instead of four; gam is folded back into R before it could underflow
+//    (below 2^-32, or alpha = 0);
+//  * the multiply-adds are Blackwell's paired fp32 FMA (fma.rn.f32x2), two
+//    lanes of work per issued instruction, which leaves issue slots for the
+//    shared loads;
+//  * a CTA is one warp (32 rows of one head).  With ~168 registers a thread
+//    an SM holds 11-12 such warps, and one-warp CTAs let the block scheduler
+//    spread the B*NV*D/32 warps evenly over the SMs (a 4-warp CTA per head
 //    would leave some SMs with 3 heads and others with 2);
 //  * per-token inputs stream through a two-stage cp.async ring in shared
 //    memory (8 tokens per stage), so the next chunk's loads overlap this
@@ -94,6 +102,23 @@ __device__ __forceinline__ void stage_chunk(Stage &st, const PrefillParams &p, i
     }
 }
 
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long ra = *reinterpret_cast<unsigned long long *>(&a);
+    unsigned long long rb = *reinterpret_cast<unsigned long long *>(&b);
+    unsigned long long rc = *reinterpret_cast<unsigned long long *>(&c), rd;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    return *reinterpret_cast<float2 *>(&rd);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    unsigned long long ra = *reinterpret_cast<unsigned long long *>(&a);
+    unsigned long long rb = *reinterpret_cast<unsigned long long *>(&b), rd;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+    return *reinterpret_cast<float2 *>(&rd);
+}
+
+// Smallest scale kept deferred before it is folded back into the stored row.
+constexpr float kMinScale = 0x1p-32f;
+
 __global__ void __launch_bounds__(kRows, 12)
 prefill_d128(const PrefillParams p)
 {
@@ -113,13 +138,18 @@ prefill_d128(const PrefillParams p)
     stage_chunk(ring[0], p, seq, h, g, r0, 0, min(kTC, T), lane);   // before S is live
     cp_async_commit();
 
+    // The row is kept as S = gam * R: the decay multiplies the scalar gam, and the
+    // rank-1 write adds (coef / gam_new) k to R -- one fused multiply-add per element.
+    // Before gam could underflow it is folded back into R.
     float *row = p.state + seq * p.pitch + (int64_t)h * kD * kD + (int64_t)a * kD;
-    float S[kD];
+    float2 R[kD / 2];
 #pragma unroll
-    for (int j = 0; j < kD; j += 4) {
-        const float4 t = *reinterpret_cast<const float4 *>(row + j);
-        S[j] = t.x; S[j + 1] = t.y; S[j + 2] = t.z; S[j + 3] = t.w;
+    for (int j = 0; j < kD / 4; ++j) {
+        const float4 t = *reinterpret_cast<const float4 *>(row + 4 * j);
+        R[2 * j] = make_float2(t.x, t.y);
+        R[2 * j + 1] = make_float2(t.z, t.w);
     }
+    float gam = 1.0f;
 
     float *orow = p.o + (int64_t)seq * T * p.o_stride + (int64_t)h * kD + a;
     for (int c = 0; c < nchunks; ++c) {
@@ -138,43 +168,53 @@ prefill_d128(const PrefillParams p)
         const unsigned q_s = (unsigned)__cvta_generic_to_shared(st.q[0]);
         for (int tt = 0; tt < n; ++tt) {
             const unsigned kt = k_s + tt * (kD * 4), qt = q_s + tt * (kD * 4);
-            // pass 1: u = S[a] . k
-            float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+            float2 u0 = make_float2(0.f, 0.f), u1 = u0;
 #pragma unroll
             for (int j = 0; j < kD / 4; ++j) {
                 const float4 kk = lds128(kt + 16 * j);
-                u0 = fmaf(S[4 * j], kk.x, u0);
-                u1 = fmaf(S[4 * j + 1], kk.y, u1);
-                u2 = fmaf(S[4 * j + 2], kk.z, u2);
-                u3 = fmaf(S[4 * j + 3], kk.w, u3);
+                u0 = ffma2(R[2 * j], make_float2(kk.x, kk.y), u0);
+                u1 = ffma2(R[2 * j + 1], make_float2(kk.z, kk.w), u1);
             }
-            const float u = (u0 + u1) + (u2 + u3);
+            const float u = gam * ((u0.x + u0.y) + (u1.x + u1.y));
             const float alpha = st.alpha[tt], beta = st.beta[tt];
             const float coef = beta * (st.v[tt][lane] - alpha * u);
-            // pass 2: S[a] <- alpha S[a] + coef k ;  o = S_new[a] . q
+            const float gnew = alpha * gam;
             const unsigned k2 = after(kt, coef, p.zero), q2 = after(qt, coef, p.zero);
-            const float a2 = __uint_as_float(after(__float_as_uint(alpha), coef, p.zero));  // == alpha
-            float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+            float2 o0 = make_float2(0.f, 0.f), o1 = o0;
+            if (gnew >= kMinScale) {            // warp-uniform: one head per warp
+                const float cs = coef / gnew;
+                const float2 c2 = make_float2(cs, cs);
 #pragma unroll
-            for (int j = 0; j < kD / 4; ++j) {
-                const float4 kk = lds128(k2 + 16 * j), qq = lds128(q2 + 16 * j);
-                S[4 * j] = fmaf(coef, kk.x, a2 * S[4 * j]);
-                S[4 * j + 1] = fmaf(coef, kk.y, a2 * S[4 * j + 1]);
-                S[4 * j + 2] = fmaf(coef, kk.z, a2 * S[4 * j + 2]);
-                S[4 * j + 3] = fmaf(coef, kk.w, a2 * S[4 * j + 3]);
-                o0 = fmaf(S[4 * j], qq.x, o0);
-                o1 = fmaf(S[4 * j + 1], qq.y, o1);
-                o2 = fmaf(S[4 * j + 2], qq.z, o2);
-                o3 = fmaf(S[4 * j + 3], qq.w, o3);
+                for (int j = 0; j < kD / 4; ++j) {
+                    const float4 kk = lds128(k2 + 16 * j), qq = lds128(q2 + 16 * j);
+                    R[2 * j] = ffma2(c2, make_float2(kk.x, kk.y), R[2 * j]);
+                    R[2 * j + 1] = ffma2(c2, make_float2(kk.z, kk.w), R[2 * j + 1]);
+                    o0 = ffma2(R[2 * j], make_float2(qq.x, qq.y), o0);
+                    o1 = ffma2(R[2 * j + 1], make_float2(qq.z, qq.w), o1);
+                }
+                gam = gnew;
+            } else {
+                const float2 g2 = make_float2(gnew, gnew), c2 = make_float2(coef, coef);
+#pragma unroll
+                for (int j = 0; j < kD / 4; ++j) {
+                    const float4 kk = lds128(k2 + 16 * j), qq = lds128(q2 + 16 * j);
+                    R[2 * j] = ffma2(c2, make_float2(kk.x, kk.y), fmul2(g2, R[2 * j]));
+                    R[2 * j + 1] = ffma2(c2, make_float2(kk.z, kk.w), fmul2(g2, R[2 * j + 1]));
+                    o0 = ffma2(R[2 * j], make_float2(qq.x, qq.y), o0);
+                    o1 = ffma2(R[2 * j + 1], make_float2(qq.z, qq.w), o1);
+                }
+                gam = 1.0f;
             }
-            __stcs(orow + (int64_t)(c * kTC + tt) * p.o_stride, ((o0 + o1) + (o2 + o3)) * p.inv_sqrt_d);
+            const float o = gam * ((o0.x + o0.y) + (o1.x + o1.y));
+            __stcs(orow + (int64_t)(c * kTC + tt) * p.o_stride, o * p.inv_sqrt_d);
         }
-        __syncwarp();   // every lane is done with this stage before it is refilled
+        __syncwarp();
     }
 
 #pragma unroll
-    for (int j = 0; j < kD; j += 4)
-        *reinterpret_cast<float4 *>(row + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    for (int j = 0; j < kD / 4; ++j)
+        *reinterpret_cast<float4 *>(row + 4 * j) =
+            make_float4(gam * R[2 * j].x, gam * R[2 * j].y, gam * R[2 * j + 1].x, gam * R[2 * j + 1].y);
 }
 
 // Any D <= 256 and any alignment: one CTA per (sequence, head), one warp per

@@ -188,7 +188,7 @@ def check_decode(res, f16, norm):
 
 
 def run_prefill_case(B, NK, NV, D, T, *, seed=0, init="zero", pad=(0, 0, 0, 0), pitch_pad=0, misalign=0,
-                     splits=None):
+                     splits=None, alpha=None, beta=None):
     """Prefill of T tokens on the GPU (one call, or per-sequence calls over `splits`)
     and in the oracle; returns error metrics."""
     if init == "zero":
@@ -196,6 +196,10 @@ def run_prefill_case(B, NK, NV, D, T, *, seed=0, init="zero", pad=(0, 0, 0, 0), 
     else:
         S0 = gs.state_heads(seed, range(B), range(NV), D)
     x = gs.prefill_inputs(seed, B, T, NK, NV, D)
+    if alpha is not None:          # host-side override of the drawn gates (array or scalar)
+        x["alpha"][...] = alpha
+    if beta is not None:
+        x["beta"][...] = beta
     pool = state_pool(B, NV, D, False, pitch_pad, misalign)
     pool.write(S0.reshape(B, -1))
     R = B * T
@@ -233,4 +237,5 @@ def run_prefill_case(B, NK, NV, D, T, *, seed=0, init="zero", pad=(0, 0, 0, 0), 
         "state_max_rel": max_rel_err(S_gpu, ref),
         "o_max_rel": max_rel_err(o_gpu, o_ref),
         "intact": all(b.intact() for b in (pool, qb, kb, vb, ab, bb, ob)),
+        "S_gpu": S_gpu, "S_ref": ref,
     }

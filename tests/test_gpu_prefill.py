@@ -39,6 +39,23 @@ def test_d128_split_calls_equal_one_call():
     check(run_prefill_case(2, 2, 3, 128, 29, seed=13, init="normal", splits=(13, 16)))
 
 
+def test_d128_low_and_zero_decay():
+    """Decays far below the typical ~0.86, with exact zeros: the kernel's deferred decay scale drops
+    below its fold threshold every few tokens (and alpha = 0 folds at once), so both update forms
+    run many times in one sequence."""
+    rng = np.random.default_rng(21)
+    B, NV, T = 2, 3, 64
+    a = rng.uniform(1e-3, 0.3, size=(B, T, NV)).astype(np.float32)
+    a[:, ::7, :] = 0.0
+    check(run_prefill_case(B, 2, NV, 128, T, seed=21, init="normal", alpha=a))
+
+
+def test_d128_alpha_one_beta_zero_leaves_state_bitwise():
+    r = run_prefill_case(2, 2, 3, 128, 17, seed=22, init="normal", alpha=1.0, beta=0.0)
+    assert r["intact"]
+    assert np.array_equal(r["S_gpu"], r["S_ref"])
+
+
 def test_d128_misaligned_takes_general_kernel():
     check(run_prefill_case(2, 2, 3, 128, 9, seed=14, misalign=1, pad=(1, 0, 0, 0)))
 
