@@ -22,7 +22,7 @@ import threading
 __all__ = [
     "GdnError", "load", "build", "library_path",
     "GDN_STATE_F32", "GDN_STATE_F16", "STATUS",
-    "gdn_decode", "gdn_decode_norm", "gdn_prefill_seq",
+    "gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_prefill_seq",
     "gdn_h_f32_to_f16", "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error",
 ]
 
@@ -58,11 +58,14 @@ def _declare(lib):
     lib.gdn_decode.argtypes = [P, i32, i64, P, P, P, P, P, P, i32, i32, i32, i32, i64, i64, i64, i64, P]
     lib.gdn_decode_norm.argtypes = [P, i32, i64, P, P, P, P, P, P, P, f32, P, i32, i32, i32, i32,
                                     i64, i64, i64, i64, i64, P]
+    lib.gdn_decode_chunk2.argtypes = [P, i32, i64, P, i64, P, P, P, P, P, P, i32, i32, i32, i32,
+                                      i64, i64, i64, i64, P]
     lib.gdn_prefill_seq.argtypes = [P, i32, i64, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                     i64, i64, i64, i64, P]
     lib.gdn_h_f32_to_f16.argtypes = [P, P, u64, P]
     lib.gdn_h_f16_to_f32.argtypes = [P, P, u64, P]
-    for fn in ("gdn_decode", "gdn_decode_norm", "gdn_prefill_seq", "gdn_h_f32_to_f16", "gdn_h_f16_to_f32"):
+    for fn in ("gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_prefill_seq", "gdn_h_f32_to_f16",
+               "gdn_h_f16_to_f32"):
         getattr(lib, fn).restype = i32
     lib.gdn_status_str.argtypes = [i32]
     lib.gdn_status_str.restype = ctypes.c_char_p
@@ -160,6 +163,26 @@ def gdn_decode_norm(state, q, k, v, alpha, beta, z, gn, out, *, batch, nk, nv, d
         out_stride if out_stride is not None else nv * d,
         _stream(stream))
     _check("gdn_decode_norm", st)
+
+
+def gdn_decode_chunk2(state, state_mid, q, k, v, alpha, beta, o, *, batch, nk, nv, d,
+                      state_pitch=None, mid_pitch=None, state_dtype=None,
+                      qk_stride=None, v_stride=None, gb_stride=None, o_stride=None, stream=None):
+    """Two tokens per sequence in one launch (token rows 2*b + t); state_mid receives the state
+    after the first token, state the state after both; raw fp32 o for both tokens."""
+    lib = load()
+    sd = _state_dtype(state, state_dtype)
+    st = lib.gdn_decode_chunk2(
+        _ptr(state), sd, state_pitch if state_pitch is not None else nv * d * d,
+        _ptr(state_mid), mid_pitch if mid_pitch is not None else nv * d * d,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o),
+        batch, nk, nv, d,
+        qk_stride if qk_stride is not None else nk * d,
+        v_stride if v_stride is not None else nv * d,
+        gb_stride if gb_stride is not None else nv,
+        o_stride if o_stride is not None else nv * d,
+        _stream(stream))
+    _check("gdn_decode_chunk2", st)
 
 
 def gdn_prefill_seq(state, q, k, v, alpha, beta, o, *, batch, seq_len, nk, nv, d,

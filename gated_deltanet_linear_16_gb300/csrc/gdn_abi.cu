@@ -183,6 +183,50 @@ GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
                         out_stride, true, stream);
 }
 
+GDN_API int gdn_decode_chunk2(void *state, int state_dtype, int64_t state_pitch,
+                              void *state_mid, int64_t mid_pitch,
+                              const float *q, const float *k, const float *v,
+                              const float *alpha, const float *beta, float *o,
+                              int batch, int nk, int nv, int d,
+                              int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                              int64_t o_stride, void *stream)
+{
+    int st = check_common(batch, nk, nv, d, state_pitch, state_dtype);
+    if (st != GDN_OK) return st;
+    if (mid_pitch < (int64_t)nv * d * d) return GDN_ERR_ARG;
+    const int64_t selem = state_dtype == GDN_STATE_F16 ? 2 : 4;
+    const int64_t B = batch, R = 2 * (int64_t)batch;
+    const int64_t hv = (int64_t)nv * d, hk = (int64_t)nk * d;
+    Operand ops[8] = {
+        {state, B, (int64_t)nv * d * d, state_pitch, selem},
+        {state_mid, B, (int64_t)nv * d * d, mid_pitch, selem},
+        {o, R, hv, o_stride, 4},
+        {q, R, hk, qk_stride, 4},
+        {k, R, hk, qk_stride, 4},
+        {v, R, hv, v_stride, 4},
+        {alpha, R, nv, gb_stride, 4},
+        {beta, R, nv, gb_stride, 4},
+    };
+    if (batch == 0) {
+        for (auto &op : ops) if (op.p == nullptr) return GDN_ERR_ARG;
+        return GDN_OK;
+    }
+    st = check_operands(ops, 8, 3);
+    if (st != GDN_OK) return st;
+
+    DecodeParams p{};
+    p.state = state; p.pitch = state_pitch;
+    p.state_mid = state_mid; p.mid_pitch = mid_pitch;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.o = o;
+    p.qk_stride = qk_stride; p.v_stride = v_stride; p.gb_stride = gb_stride; p.o_stride = o_stride;
+    p.batch = batch; p.nk = nk; p.nv = nv; p.d = d;
+    p.inv_sqrt_d = inv_sqrt(d);
+    const bool fast = d == 128 && vec16(state) && (state_pitch * selem) % 16 == 0 &&
+                      vec16(state_mid) && (mid_pitch * selem) % 16 == 0 &&
+                      vec16(q) && vec16(k) && (qk_stride * 4) % 16 == 0;
+    return cuda_status(launch_decode_chunk2(p, state_dtype == GDN_STATE_F16, fast, (cudaStream_t)stream));
+}
+
 GDN_API int gdn_prefill_seq(void *state, int state_dtype, int64_t state_pitch,
                             const float *q, const float *k, const float *v,
                             const float *alpha, const float *beta, float *o,

@@ -1,0 +1,232 @@
+// gdn_chunk2.cu -- two tokens through the gated delta rule in one launch (the
+// verify step of speculative decoding), writing the state after the first
+// token to a second buffer so a rejected draft token can be rolled back.
+//
+// Follows metrale_model_layers/layers/ops/ssm_gdn_a.rs, launcher
+// `gdn_decode_chunk2` (two tokens per launch, the intermediate state written
+// for rollback, strides in elements); the step is
+// logicaffeine_compile/codegen_cuda/gdn.rs, kernel `gdn_step`.
+//
+// Per row the arithmetic is exactly that of the single-token kernels in
+// gdn_decode.cu, applied twice with the row slice kept in registers: the state
+// is read once and written twice (intermediate + final), instead of read twice
+// and written twice by two launches.  With an fp16 state the row is rounded to
+// fp16 after the first token and the second token continues from the rounded
+// values, so the result is bitwise the one two single-token calls give.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kD = 128;
+
+template <typename TS> struct Chunk2Shape {
+    static constexpr int kWarps = 4, kBatches = 4, kMinBlocks = 4;
+};
+template <> struct Chunk2Shape<__half> {
+    static constexpr int kWarps = 8, kBatches = 2, kMinBlocks = 3;
+};
+
+template <typename TS, int WARPS, int NB, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+chunk2_d128(const DecodeParams p)
+{
+    using V = Vec16<TS>;
+    constexpr int EPV = V::N;                  // state elements per 16-byte vector
+    constexpr int LPR = kD / EPV;              // lanes per state row: 32 fp32, 16 fp16
+    constexpr int RPL = 32 / LPR;              // rows per warp-wide load
+    constexpr int RPW = kD / WARPS;            // rows per warp
+    constexpr int NLD = RPW / RPL;             // 16-byte state loads per lane
+    constexpr int LPB = NLD / NB;              // loads per batch
+    static_assert(RPW <= 32 && NLD % NB == 0, "shape");
+
+    const int unit = blockIdx.x;               // (sequence, value head)
+    const int seq = unit / p.nv;
+    const int h = unit - seq * p.nv;
+    const int g = h % p.nk;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / LPR;
+    const int col = (lane % LPR) * EPV;
+    const int row0 = warp * RPW;
+    const int64_t slice = (int64_t)h * kD * kD + (int64_t)(row0 + sub) * kD + col;
+
+    TS *rowp = reinterpret_cast<TS *>(p.state) + seq * p.pitch + slice;
+    TS *midp = reinterpret_cast<TS *>(p.state_mid) + seq * p.mid_pitch + slice;
+
+    uint4 raw[NB > 1 ? 2 : 1][LPB];
+#pragma unroll
+    for (int i = 0; i < LPB; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
+
+    // token t of sequence b reads input row 2 b + t
+    const bool row_lane = lane < RPW;
+    float kx[2][EPV], qx[2][EPV], v_l[2], alpha[2], beta[2], kq[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int64_t row = (int64_t)seq * 2 + t;
+        const float *kp = p.k + row * p.qk_stride + (int64_t)g * kD + col;
+        const float *qp = p.q + row * p.qk_stride + (int64_t)g * kD + col;
+#pragma unroll
+        for (int j = 0; j < EPV; j += 4) {
+            const float4 a = ld_ro_f4(kp + j), b = ld_ro_f4(qp + j);
+            kx[t][j] = a.x; kx[t][j + 1] = a.y; kx[t][j + 2] = a.z; kx[t][j + 3] = a.w;
+            qx[t][j] = b.x; qx[t][j + 1] = b.y; qx[t][j + 2] = b.z; qx[t][j + 3] = b.w;
+        }
+        v_l[t] = row_lane ? __ldg(p.v + row * p.v_stride + (int64_t)h * kD + row0 + lane) : 0.f;
+        alpha[t] = __ldg(p.alpha + row * p.gb_stride + h);
+        beta[t] = __ldg(p.beta + row * p.gb_stride + h);
+        float a = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) a = fmaf(kx[t][j], qx[t][j], a);
+        kq[t] = group_sum<LPR>(a);
+    }
+
+    float o_keep[2] = {0.f, 0.f};
+#pragma unroll
+    for (int bt = 0; bt < NB; ++bt) {
+        if (bt + 1 < NB) {
+#pragma unroll
+            for (int i = 0; i < LPB; ++i)
+                raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * LPB + i) * RPL * kD);
+        }
+#pragma unroll
+        for (int ii = 0; ii < LPB; ++ii) {
+            const int i = bt * LPB + ii;
+            float s[EPV];
+            V::unpack(raw[bt & 1][ii], s);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                float u = 0.f, w = 0.f;
+#pragma unroll
+                for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[t][j], u); w = fmaf(s[j], qx[t][j], w); }
+                u = group_sum<LPR>(u);
+                w = group_sum<LPR>(w);
+                const float va = __shfl_sync(kFull, v_l[t], i * RPL + sub);
+                const float coef = beta[t] * (va - alpha[t] * u);
+                const float oa = (alpha[t] * w + coef * kq[t]) * p.inv_sqrt_d;
+#pragma unroll
+                for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[t][j], alpha[t] * s[j]);
+                const uint4 packed = V::pack(s);
+                if (t == 0) {
+                    st_stream16(midp + (int64_t)i * RPL * kD, packed);
+                    V::unpack(packed, s);      // continue from the stored (rounded) state
+                } else {
+                    st_stream16(rowp + (int64_t)i * RPL * kD, packed);
+                }
+                if constexpr (RPL == 1) {
+                    if (lane == i) o_keep[t] = oa;
+                } else {
+#pragma unroll
+                    for (int r = 0; r < RPL; ++r) {
+                        const float orr = __shfl_sync(kFull, oa, r * LPR);
+                        if (lane == i * RPL + r) o_keep[t] = orr;
+                    }
+                }
+            }
+        }
+    }
+    if (row_lane) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+            p.o[((int64_t)seq * 2 + t) * p.o_stride + (int64_t)h * kD + row0 + lane] = o_keep[t];
+    }
+}
+
+// Any D <= 256 and any alignment: the general single-token kernel's per-row
+// arithmetic, applied twice.
+constexpr int kGenWarps = 4;
+constexpr int kMaxD = 256;
+
+template <typename TS>
+__global__ void __launch_bounds__(kGenWarps * 32)
+chunk2_generic(const DecodeParams p)
+{
+    constexpr int MAXV = kMaxD / 32;
+    __shared__ float o_s[2][kMaxD];
+
+    const int D = p.d;
+    const int seq = blockIdx.x / p.nv;
+    const int h = blockIdx.x - seq * p.nv;
+    const int g = h % p.nk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    TS *S = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * D * D;
+    TS *M = reinterpret_cast<TS *>(p.state_mid) + seq * p.mid_pitch + (int64_t)h * D * D;
+    const float *vp[2];
+    float alpha[2], beta[2], kq[2], kreg[2][MAXV], qreg[2][MAXV];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int64_t row = (int64_t)seq * 2 + t;
+        const float *kp = p.k + row * p.qk_stride + (int64_t)g * D;
+        const float *qp = p.q + row * p.qk_stride + (int64_t)g * D;
+        vp[t] = p.v + row * p.v_stride + (int64_t)h * D;
+        alpha[t] = p.alpha[row * p.gb_stride + h];
+        beta[t] = p.beta[row * p.gb_stride + h];
+        float a = 0.f;
+#pragma unroll
+        for (int j = 0; j < MAXV; ++j) {
+            const int c = lane + 32 * j;
+            kreg[t][j] = c < D ? kp[c] : 0.f;
+            qreg[t][j] = c < D ? qp[c] : 0.f;
+            a = fmaf(kreg[t][j], qreg[t][j], a);
+        }
+        kq[t] = group_sum<32>(a);
+    }
+
+    for (int a = warp; a < D; a += kGenWarps) {
+        float s[MAXV];
+#pragma unroll
+        for (int j = 0; j < MAXV; ++j) {
+            const int c = lane + 32 * j;
+            s[j] = c < D ? to_f32<TS>(S[(int64_t)a * D + c]) : 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            float u = 0.f, w = 0.f;
+#pragma unroll
+            for (int j = 0; j < MAXV; ++j) {
+                u = fmaf(s[j], kreg[t][j], u);
+                w = fmaf(s[j], qreg[t][j], w);
+            }
+            u = group_sum<32>(u);
+            w = group_sum<32>(w);
+            const float coef = beta[t] * (vp[t][a] - alpha[t] * u);
+            const float oa = (alpha[t] * w + coef * kq[t]) * p.inv_sqrt_d;
+            TS *dst = (t == 0 ? M : S) + (int64_t)a * D;
+#pragma unroll
+            for (int j = 0; j < MAXV; ++j) {
+                const int c = lane + 32 * j;
+                const TS st = from_f32<TS>(fmaf(coef, kreg[t][j], alpha[t] * s[j]));
+                s[j] = c < D ? to_f32<TS>(st) : 0.f;   // continue from the stored value
+                if (c < D) dst[c] = st;
+            }
+            if (lane == 0) o_s[t][a] = oa;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+        for (int a = threadIdx.x; a < D; a += kGenWarps * 32)
+            p.o[((int64_t)seq * 2 + t) * p.o_stride + (int64_t)h * D + a] = o_s[t][a];
+}
+
+template <typename TS>
+cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
+{
+    const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
+    using F = Chunk2Shape<TS>;
+    if (fast)
+        chunk2_d128<TS, F::kWarps, F::kBatches, F::kMinBlocks><<<grid, F::kWarps * 32, 0, s>>>(p);
+    else
+        chunk2_generic<TS><<<grid, kGenWarps * 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_chunk2(const DecodeParams &p, bool f16_state, bool fast, cudaStream_t s)
+{
+    return f16_state ? launch_typed<__half>(p, fast, s) : launch_typed<float>(p, fast, s);
+}
+
+}  // namespace gdn

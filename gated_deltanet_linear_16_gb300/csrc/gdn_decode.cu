@@ -35,50 +35,6 @@ namespace {
 
 constexpr int kD = 128;
 
-// A 16-byte vector of state elements, widened to / narrowed from fp32.
-template <typename TS> struct Vec16;
-
-template <> struct Vec16<float> {
-    static constexpr int N = 4;
-    __device__ __forceinline__ static void unpack(const uint4 r, float (&x)[N]) {
-        x[0] = __uint_as_float(r.x); x[1] = __uint_as_float(r.y);
-        x[2] = __uint_as_float(r.z); x[3] = __uint_as_float(r.w);
-    }
-    __device__ __forceinline__ static uint4 pack(const float (&x)[N]) {
-        return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
-                          __float_as_uint(x[2]), __float_as_uint(x[3]));
-    }
-};
-
-template <> struct Vec16<__half> {
-    static constexpr int N = 8;
-    __device__ __forceinline__ static float2 h2f(unsigned u) {
-        __half2 h = *reinterpret_cast<__half2 *>(&u);
-        return __half22float2(h);
-    }
-    __device__ __forceinline__ static unsigned f2h(float a, float b) {
-        __half2 h = __floats2half2_rn(a, b);           // round to nearest even
-        return *reinterpret_cast<unsigned *>(&h);
-    }
-    __device__ __forceinline__ static void unpack(const uint4 r, float (&x)[N]) {
-        float2 t;
-        t = h2f(r.x); x[0] = t.x; x[1] = t.y;
-        t = h2f(r.y); x[2] = t.x; x[3] = t.y;
-        t = h2f(r.z); x[4] = t.x; x[5] = t.y;
-        t = h2f(r.w); x[6] = t.x; x[7] = t.y;
-    }
-    __device__ __forceinline__ static uint4 pack(const float (&x)[N]) {
-        return make_uint4(f2h(x[0], x[1]), f2h(x[2], x[3]), f2h(x[4], x[5]), f2h(x[6], x[7]));
-    }
-};
-
-template <typename TS> __device__ __forceinline__ float to_f32(TS x);
-template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
-template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
-template <typename TS> __device__ __forceinline__ TS from_f32(float x);
-template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
-template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
-
 // ------------------------------------------------------------------ D == 128
 
 // Shape of the D == 128 kernel: WARPS warps share one head (128 / WARPS rows

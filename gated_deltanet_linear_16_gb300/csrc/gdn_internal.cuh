@@ -24,6 +24,10 @@ struct DecodeParams {
     int batch, nk, nv, d;
     float eps;
     float inv_sqrt_d;       // 1/sqrt(D) rounded once on the host
+    // two-token variant only: the state after the first token, slot pitch in elements.
+    // Token rows are then b * 2 + t for q, k, v, alpha, beta and o.
+    void *state_mid;
+    int64_t mid_pitch;
 };
 
 struct PrefillParams {
@@ -41,6 +45,7 @@ struct PrefillParams {
 // (fast D == 128 path when the alignment allows it, general otherwise) and
 // return the launch status.
 cudaError_t launch_decode(const DecodeParams &p, bool f16_state, bool norm, bool fast, cudaStream_t s);
+cudaError_t launch_decode_chunk2(const DecodeParams &p, bool f16_state, bool fast, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, bool fast, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, bool vec, cudaStream_t s);
 cudaError_t launch_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, bool vec, cudaStream_t s);
@@ -78,5 +83,49 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
     __nv_bfloat16 b = __float2bfloat16_rn(x);
     return *reinterpret_cast<uint16_t *>(&b);
 }
+
+// A 16-byte vector of state elements, widened to / narrowed from fp32.
+template <typename TS> struct Vec16;
+
+template <> struct Vec16<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void unpack(const uint4 r, float (&x)[N]) {
+        x[0] = __uint_as_float(r.x); x[1] = __uint_as_float(r.y);
+        x[2] = __uint_as_float(r.z); x[3] = __uint_as_float(r.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&x)[N]) {
+        return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
+                          __float_as_uint(x[2]), __float_as_uint(x[3]));
+    }
+};
+
+template <> struct Vec16<__half> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static float2 h2f(unsigned u) {
+        __half2 h = *reinterpret_cast<__half2 *>(&u);
+        return __half22float2(h);
+    }
+    __device__ __forceinline__ static unsigned f2h(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);           // round to nearest even
+        return *reinterpret_cast<unsigned *>(&h);
+    }
+    __device__ __forceinline__ static void unpack(const uint4 r, float (&x)[N]) {
+        float2 t;
+        t = h2f(r.x); x[0] = t.x; x[1] = t.y;
+        t = h2f(r.y); x[2] = t.x; x[3] = t.y;
+        t = h2f(r.z); x[4] = t.x; x[5] = t.y;
+        t = h2f(r.w); x[6] = t.x; x[7] = t.y;
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&x)[N]) {
+        return make_uint4(f2h(x[0], x[1]), f2h(x[2], x[3]), f2h(x[4], x[5]), f2h(x[6], x[7]));
+    }
+};
+
+template <typename TS> __device__ __forceinline__ float to_f32(TS x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <typename TS> __device__ __forceinline__ TS from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
 
 }  // namespace gdn

@@ -119,6 +119,34 @@ GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
                             int64_t z_stride, int64_t out_stride, void *stream);
 
 /*
+ * gdn_decode_chunk2 -- two tokens per sequence through the recurrence in one
+ * launch (the verify step of speculative decoding), keeping the state after
+ * the first token so that a rejected draft token can be rolled back.
+ *   Defined by: ssm_gdn_a.rs, launcher `gdn_decode_chunk2` (two tokens per
+ *   launch, the intermediate state written for rollback, strides in
+ *   elements); the step is gdn.rs `gdn_step`.
+ *   state        as gdn_decode; on return it holds the state after BOTH
+ *                tokens.
+ *   state_mid    [batch] slots of the same dtype, slot pitch mid_pitch >=
+ *                NV*D*D elements: written with the state after the FIRST
+ *                token (fp16: rounded, as it would be stored between two
+ *                calls).
+ *   q, k         [2*batch] rows of NK*D; token t of sequence b is row 2b+t.
+ *   v            [2*batch] rows of NV*D.  alpha, beta: [2*batch] rows of NV.
+ *   o            [2*batch] rows of NV*D fp32 (raw o of each token, no norm).
+ *   The result equals two gdn_decode calls on the same kernel path, bit for
+ *   bit, while the state is read once instead of twice.
+ *   Errors as gdn_decode (state_mid overlapping any operand: GDN_ERR_ALIAS).
+ */
+GDN_API int gdn_decode_chunk2(void *state, int state_dtype, int64_t state_pitch,
+                              void *state_mid, int64_t mid_pitch,
+                              const float *q, const float *k, const float *v,
+                              const float *alpha, const float *beta, float *o,
+                              int batch, int nk, int nv, int d,
+                              int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                              int64_t o_stride, void *stream);
+
+/*
  * gdn_prefill_seq -- seq_len tokens per sequence through the recurrence in
  * one launch, token by token in order, the state held on chip between
  * tokens; writes the raw fp32 o of every token (no norm).

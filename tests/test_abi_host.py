@@ -40,7 +40,7 @@ def lib(built):
 
 def test_exports_match_header(built):
     want = declared_symbols()
-    assert want == sorted(["gdn_decode", "gdn_decode_norm", "gdn_prefill_seq", "gdn_h_f32_to_f16",
+    assert want == sorted(["gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_prefill_seq", "gdn_h_f32_to_f16",
                            "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error"])
     out = subprocess.run(["nm", "-D", "--defined-only", gdn.library_path()], capture_output=True, text=True,
                          check=True).stdout
@@ -73,6 +73,31 @@ def decode_norm(lib, **kw):
     return lib.gdn_decode_norm(a["state"], a["dt"], a["pitch"], a["q"], a["k"], a["v"], a["alpha"], a["beta"],
                                a["z"], a["gn"], a["eps"], a["out"], a["batch"], a["nk"], a["nv"], a["d"],
                                a["qk"], a["vs"], a["gb"], a["zs"], a["outs"], None)
+
+
+def chunk2(lib, **kw):
+    a = dict(state=A, dt=0, pitch=3 * 128 * 128, mid=A + (9 << 30), mpitch=3 * 128 * 128, q=A + (1 << 30),
+             k=A + (2 << 30), v=A + (3 << 30), alpha=A + (4 << 30), beta=A + (5 << 30), o=A + (6 << 30),
+             batch=2, nk=1, nv=3, d=128, qk=128, vs=3 * 128, gb=3, os=3 * 128)
+    a.update(kw)
+    return lib.gdn_decode_chunk2(a["state"], a["dt"], a["pitch"], a["mid"], a["mpitch"], a["q"], a["k"], a["v"],
+                                 a["alpha"], a["beta"], a["o"], a["batch"], a["nk"], a["nv"], a["d"], a["qk"],
+                                 a["vs"], a["gb"], a["os"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(mid=None), ARG), (dict(mpitch=3 * 128 * 128 - 1), ARG), (dict(dt=3), UNSUP),
+    (dict(mid=A + 1024), ALIAS),                         # intermediate state inside the state
+    (dict(o=A + (9 << 30) + 64), ALIAS),                 # output inside the intermediate state
+    (dict(mid=A + (9 << 30) + 2), ALIGN),                # fp32 intermediate not 4-byte aligned
+    (dict(os=100), ARG),
+])
+def test_chunk2_rejects(lib, kw, want):
+    assert chunk2(lib, **kw) == want
+
+
+def test_chunk2_empty_is_ok(lib):
+    assert chunk2(lib, batch=0) == OK
 
 
 def prefill(lib, **kw):
