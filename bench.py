@@ -27,6 +27,7 @@ scaling, no collective in the data path); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -59,7 +60,7 @@ NCU_TRAFFIC = {
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
@@ -96,12 +97,18 @@ def src_sha(name):
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
+        # nvidia-smi numbers GPUs physically; the process may see a remapped index, so use the UUID
         self.gpu = gpu_index
+        try:
+            import torch
+            self.gpu = "GPU-" + str(torch.cuda.get_device_properties(gpu_index).uuid)
+        except Exception:
+            pass
         self.proc = None
         self.path = os.path.join("/tmp", f"gdn_clocks_{os.getpid()}.csv")
 
@@ -109,7 +116,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -124,15 +131,31 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
+    def mark(self, which):
+        """Record the wall-clock start or end of the timed region."""
+        setattr(self, which, datetime.datetime.now())
+
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return None
         sm, mx, reasons, pw = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
+        lo, hi = getattr(self, "start", None), getattr(self, "end", None)
+        lines = [[p.strip() for p in line.split(",")] for line in open(self.path)]
+        lines = [p for p in lines if len(p) >= 9]
+
+        def when(p):
+            try:
+                return datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                return None
+
+        inside = [p for p in lines if lo and hi and when(p) and lo <= when(p) <= hi]
+        if not inside and lines and lo:
+            # region shorter than the sampling period: the samples nearest to it
+            after = [p for p in lines if when(p) and when(p) >= lo]
+            inside = after[:1] or lines[-1:]
+        for parts in inside:
             try:
                 sm.append(float(parts[1]))
                 mx.append(float(parts[2]))
@@ -146,6 +169,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "window_s": (hi - lo).total_seconds() if lo and hi else None,
                 "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons)}
 
 
@@ -270,12 +294,16 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk:
+        time.sleep(0.3)                       # let the sampler start before the timed region
         torch.cuda.synchronize()
+        clk.mark("start")
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
+        clk.mark("end")
+        time.sleep(0.05)
     if world > 1:
         dist.barrier()
     ms = e0.elapsed_time(e1)
@@ -377,16 +405,45 @@ def time_fn(torch, stream, fn, reps, warm=2):
 
 
 def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096, graph=True):
-    want = set(only.split(",")) if only else {"fp16", "conv", "latency", "prefill"}
+    want = set(only.split(",")) if only else {"fp16", "conv", "latency", "prefill", "chunk2"}
     rows = {}
     torch.cuda.empty_cache()
     if want & {"fp16", "conv"}:
         rows.update(row_fp16_pool(torch, gdn, dev, stream, pk, want))
     if "latency" in want:
         rows.update(row_latency(torch, gdn, dev, stream, graph))
+    if "chunk2" in want:
+        rows.update(row_chunk2(torch, gdn, dev, stream, pk))
     if "prefill" in want:
         rows.update(row_prefill(torch, gdn, dev, stream, pk, prefill_tokens))
     return rows
+
+
+def row_chunk2(torch, gdn, dev, stream, pk):
+    """Two-token verify step on one layer at batch 32 (fp32 state): the state is read once and
+    written twice (intermediate + final); both tokens' inputs read, both outputs written."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(2)
+    S = torch.empty((B, NV, D, D), device=dev).normal_(0.0, 0.02, generator=g)
+    M = torch.empty_like(S)
+    R = 2 * B
+    q = torch.randn((R, NK * D), device=dev, generator=g)
+    k = torch.randn((R, NK * D), device=dev, generator=g)
+    q = (q.view(R, NK, D) / q.view(R, NK, D).norm(dim=-1, keepdim=True)).view(R, NK * D).contiguous()
+    k = (k.view(R, NK, D) / k.view(R, NK, D).norm(dim=-1, keepdim=True)).view(R, NK * D).contiguous()
+    v = torch.randn((R, NV * D), device=dev, generator=g)
+    a = torch.sigmoid(torch.randn((R, NV), device=dev, generator=g) + 2.0)
+    bt = torch.sigmoid(torch.randn((R, NV), device=dev, generator=g))
+    o = torch.empty((R, NV * D), device=dev)
+    s = time_fn(torch, stream, lambda: gdn.gdn_decode_chunk2(S, M, q, k, v, a, bt, o, batch=B, nk=NK, nv=NV, d=D,
+                                                             stream=stream.cuda_stream), 50)
+    by = B * NV * D * D * 4 * 3 + R * (2 * NK * D + 2 * NV * D + 2 * NV) * 4
+    del S, M, q, k, v, a, bt, o
+    torch.cuda.empty_cache()
+    return {"chunk2_verify": {"config": "B=32 NK=16 NV=48 D=128 fp32, two tokens per launch",
+                              "us_per_launch": s * 1e6, "token_heads_per_s": R * NV / s,
+                              "achieved_gbs": by / s / 1e9, "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"],
+                              "algorithmic_bytes": by}}
 
 
 def row_fp16_pool(torch, gdn, dev, stream, pk, want):
@@ -469,18 +526,19 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
 
     s = time_fn(torch, stream, pf, 3, warm=1)
     th = PB * NV * T
-    io = (2 * R * NK * D + 2 * R * NV * D + 2 * R * NV) * 4 + 2 * PB * NV * D * D * 4
-    lane_ops = th * D * D * 4           # per state element: u FMA, alpha*S, update FMA, o FMA
+    io = (2 * R * NK * D + R * NV * D * 2 + 2 * R * NV) * 4 + 2 * PB * NV * D * D * 4
+    fma = th * D * D * 3                # per token-head: S.k, the rank-1 write, S.q (D^2 FMA each)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     clk = (pk.get("sm_max_mhz") or 2070.0) * 1e6
-    fp32_peak = sms * 128 * clk         # FP32 lanes x clock: lane-operations per second
+    fma_peak = sms * 128 * clk          # FP32 FMA lanes x max clock: FMA per second
     del q, k, v, a, bt, o, S
     torch.cuda.empty_cache()
     return {"prefill": {"config": f"B=8 T={T} NK=16 NV=48 D=128 fp32, state on chip",
                         "ms": s * 1e3, "token_heads_per_s": th / s,
-                        "fp32_lane_ops_per_s": lane_ops / s, "fp32_peak_lane_ops_per_s": fp32_peak,
-                        "frac_of_fp32_peak": lane_ops / s / fp32_peak,
-                        "achieved_gbs": io / s / 1e9, "bound": "alu"}}
+                        "roofline": {"bound": "alu", "achieved": fma / s / 1e12, "peak": fma_peak / 1e12,
+                                     "unit": "T FP32 FMA/s", "frac": fma / s / fma_peak,
+                                     "peak_basis": f"{sms} SMs x 128 FP32 lanes x {clk / 1e6:.0f} MHz"},
+                        "achieved_gbs": io / s / 1e9}}
 
 
 # ------------------------------------------------------------------ oracle (CPU) timing
