@@ -13,16 +13,15 @@
 //
 // GB300 design.  The state is ~99% of the bytes and is touched exactly once
 // (one read, one write per element), so the kernel is an HBM stream:
-//  * one CTA owns one (sequence, head) -- 4 warps x 32 rows (fp32) or 8 warps
-//    x 16 rows (fp16) -- so the norm's reduction over the head's D outputs
-//    needs a single __syncthreads;
+//  * one CTA owns one (sequence, head) -- 8 warps x 16 rows -- so the norm's
+//    reduction over the head's D outputs needs a single __syncthreads;
 //  * every state access is a 16-byte vector: an fp32 row (512 B) is one
 //    warp-wide load, an fp16 row (256 B) half of one, so a warp touches whole
 //    128-byte lines and stores never leave partial sectors;
 //  * each lane's state loads are issued in batches, the next batch in flight
-//    while the current one is computed and written back, with 4 CTAs per SM:
-//    about 64 KB of loads outstanding per SM, enough to cover HBM latency at
-//    full bandwidth while the stores of earlier rows drain;
+//    while the current one is computed and written back, with 3-4 CTAs per
+//    SM: some 50-100 KB of loads outstanding per SM, enough to cover HBM
+//    latency at full bandwidth while the stores of earlier rows drain;
 //  * k and q are read as this lane's own 16-byte columns, v/z/gn as one
 //    coalesced read per warp (a float per row) that lanes broadcast by shuffle;
 //  * the three dot products are butterfly shuffles inside the group of lanes
@@ -41,10 +40,10 @@ constexpr int kD = 128;
 // each); each lane's state loads are issued in NB batches, batch b + 1 in
 // flight while batch b is computed (NB == 1: everything in flight at once).
 // Chosen by measurement on GB300 (48-layer fp32 workload, 256-slot fp16 pool):
-// fp32 4 warps x 32 rows, 4 batches of 8 loads, 4 CTAs per SM; fp16 8 warps x
+// fp32 8 warps x 16 rows, 4 batches of 4 loads, 3 CTAs per SM; fp16 8 warps x
 // 16 rows, 2 batches of 4 loads, 4 CTAs per SM.
 template <typename TS> struct FastShape {
-    static constexpr int kWarps = 4, kBatches = 4, kMinBlocks = 4;
+    static constexpr int kWarps = 8, kBatches = 4, kMinBlocks = 3;
 };
 template <> struct FastShape<__half> {
     static constexpr int kWarps = 8, kBatches = 2, kMinBlocks = 4;

@@ -7,11 +7,12 @@
 // is logicaffeine_compile/codegen_cuda/gdn.rs, kernel `gdn_step`.
 //
 // Rows of S never interact: row a needs only k, q, alpha, beta of the token
-// and its own v[a].  So the GB300 kernel gives each THREAD one whole state row
-// (128 fp32 registers) for all tokens:
-//  * u = S[a].k and o[a] = S_new[a].q are thread-local dot products (no
-//    shuffles at all); k and q come from shared memory as broadcast 16-byte
-//    reads, the same address for every lane;
+// and its own v[a].  So the GB300 kernel keeps the state in registers, 128
+// fp32 per thread, for all tokens: each thread holds two rows x half of the
+// columns, so
+//  * every broadcast 16-byte shared-memory read of k or q feeds both rows
+//    (half the shared loads of one-row-per-thread), and u = S[a].k,
+//    o[a] = S_new[a].q need one shuffle each to add the two halves;
 //  * o is read out of the updated state, o = S_new q / sqrt(D), which equals
 //    (alpha w + coef kq)/sqrt(D) and needs no per-token k.q;
 //  * the decay is deferred: the row is held as S = gam * R with a per-row
@@ -125,33 +126,39 @@ prefill_d128(const PrefillParams p)
     __shared__ Stage ring[2];
 
     const int lane = threadIdx.x;
-    const int blocks_per_head = kD / kRows;           // 4
-    const int head = blockIdx.x / blocks_per_head;    // (sequence, value head)
+    const int half = lane >> 4;                        // which half of the columns
+    const int pr = lane & 15;                          // which pair of rows
+    const int blocks_per_head = kD / kRows;            // 4
+    const int head = blockIdx.x / blocks_per_head;     // (sequence, value head)
     const int r0 = (blockIdx.x - head * blocks_per_head) * kRows;
     const int seq = head / p.nv;
     const int h = head - seq * p.nv;
     const int g = h % p.nk;
-    const int a = r0 + lane;                           // this thread's state row
+    const int a0 = r0 + 2 * pr;                        // this thread's rows: a0, a0 + 1
 
     const int T = p.seq_len;
     const int nchunks = (T + kTC - 1) / kTC;
-    stage_chunk(ring[0], p, seq, h, g, r0, 0, min(kTC, T), lane);   // before S is live
+    stage_chunk(ring[0], p, seq, h, g, r0, 0, min(kTC, T), lane);   // before the state is live
     cp_async_commit();
 
-    // The row is kept as S = gam * R: the decay multiplies the scalar gam, and the
-    // rank-1 write adds (coef / gam_new) k to R -- one fused multiply-add per element.
-    // Before gam could underflow it is folded back into R.
-    float *row = p.state + seq * p.pitch + (int64_t)h * kD * kD + (int64_t)a * kD;
-    float2 R[kD / 2];
+    // Two rows x 64 columns per thread: columns 4c..4c+3 for c = 2 jj + half, jj = 0..15, so a
+    // warp-wide 16-byte shared load serves both rows of a thread and touches two distinct
+    // 16-byte chunks in different banks.  Rows are held as S = gam * R (deferred decay).
+    float *row = p.state + seq * p.pitch + (int64_t)h * kD * kD + (int64_t)a0 * kD;
+    float2 R[2][kD / 4];
 #pragma unroll
-    for (int j = 0; j < kD / 4; ++j) {
-        const float4 t = *reinterpret_cast<const float4 *>(row + 4 * j);
-        R[2 * j] = make_float2(t.x, t.y);
-        R[2 * j + 1] = make_float2(t.z, t.w);
+    for (int rr = 0; rr < 2; ++rr) {
+#pragma unroll
+        for (int jj = 0; jj < kD / 8; ++jj) {
+            const float4 t = *reinterpret_cast<const float4 *>(row + rr * kD + 4 * (2 * jj + half));
+            R[rr][2 * jj] = make_float2(t.x, t.y);
+            R[rr][2 * jj + 1] = make_float2(t.z, t.w);
+        }
     }
     float gam = 1.0f;
 
-    float *orow = p.o + (int64_t)seq * T * p.o_stride + (int64_t)h * kD + a;
+    float *orow = p.o + (int64_t)seq * T * p.o_stride + (int64_t)h * kD + a0 + half;
+    const unsigned lane_off = 16u * half;
     for (int c = 0; c < nchunks; ++c) {
         if (c + 1 < nchunks) {
             const int t1 = (c + 1) * kTC;
@@ -164,57 +171,85 @@ prefill_d128(const PrefillParams p)
         __syncwarp();
         const Stage &st = ring[c & 1];
         const int n = min(kTC, T - c * kTC);
-        const unsigned k_s = (unsigned)__cvta_generic_to_shared(st.k[0]);
-        const unsigned q_s = (unsigned)__cvta_generic_to_shared(st.q[0]);
+        const unsigned k_s = (unsigned)__cvta_generic_to_shared(st.k[0]) + lane_off;
+        const unsigned q_s = (unsigned)__cvta_generic_to_shared(st.q[0]) + lane_off;
         for (int tt = 0; tt < n; ++tt) {
             const unsigned kt = k_s + tt * (kD * 4), qt = q_s + tt * (kD * 4);
-            float2 u0 = make_float2(0.f, 0.f), u1 = u0;
+            float2 ua0 = make_float2(0.f, 0.f), ua1 = ua0, ub0 = ua0, ub1 = ua0;
 #pragma unroll
-            for (int j = 0; j < kD / 4; ++j) {
-                const float4 kk = lds128(kt + 16 * j);
-                u0 = ffma2(R[2 * j], make_float2(kk.x, kk.y), u0);
-                u1 = ffma2(R[2 * j + 1], make_float2(kk.z, kk.w), u1);
+            for (int jj = 0; jj < kD / 8; ++jj) {
+                const float4 kk = lds128(kt + 32 * jj);
+                const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
+                ua0 = ffma2(R[0][2 * jj], k01, ua0);
+                ua1 = ffma2(R[0][2 * jj + 1], k23, ua1);
+                ub0 = ffma2(R[1][2 * jj], k01, ub0);
+                ub1 = ffma2(R[1][2 * jj + 1], k23, ub1);
             }
-            const float u = gam * ((u0.x + u0.y) + (u1.x + u1.y));
+            float pa = (ua0.x + ua0.y) + (ua1.x + ua1.y);
+            float pb = (ub0.x + ub0.y) + (ub1.x + ub1.y);
+            pa += __shfl_xor_sync(kFull, pa, 16);
+            pb += __shfl_xor_sync(kFull, pb, 16);
             const float alpha = st.alpha[tt], beta = st.beta[tt];
-            const float coef = beta * (st.v[tt][lane] - alpha * u);
+            const float coef_a = beta * (st.v[tt][2 * pr] - alpha * (gam * pa));
+            const float coef_b = beta * (st.v[tt][2 * pr + 1] - alpha * (gam * pb));
             const float gnew = alpha * gam;
-            const unsigned k2 = after(kt, coef, p.zero), q2 = after(qt, coef, p.zero);
-            float2 o0 = make_float2(0.f, 0.f), o1 = o0;
+            const unsigned k2 = after(kt, coef_a, p.zero), q2 = after(qt, coef_b, p.zero);
+            float2 oa0 = make_float2(0.f, 0.f), oa1 = oa0, ob0 = oa0, ob1 = oa0;
             if (gnew >= kMinScale) {            // warp-uniform: one head per warp
-                const float cs = coef / gnew;
-                const float2 c2 = make_float2(cs, cs);
+                const float ca = coef_a / gnew, cb = coef_b / gnew;
+                const float2 ca2 = make_float2(ca, ca), cb2 = make_float2(cb, cb);
 #pragma unroll
-                for (int j = 0; j < kD / 4; ++j) {
-                    const float4 kk = lds128(k2 + 16 * j), qq = lds128(q2 + 16 * j);
-                    R[2 * j] = ffma2(c2, make_float2(kk.x, kk.y), R[2 * j]);
-                    R[2 * j + 1] = ffma2(c2, make_float2(kk.z, kk.w), R[2 * j + 1]);
-                    o0 = ffma2(R[2 * j], make_float2(qq.x, qq.y), o0);
-                    o1 = ffma2(R[2 * j + 1], make_float2(qq.z, qq.w), o1);
+                for (int jj = 0; jj < kD / 8; ++jj) {
+                    const float4 kk = lds128(k2 + 32 * jj), qq = lds128(q2 + 32 * jj);
+                    const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
+                    const float2 q01 = make_float2(qq.x, qq.y), q23 = make_float2(qq.z, qq.w);
+                    R[0][2 * jj] = ffma2(ca2, k01, R[0][2 * jj]);
+                    R[0][2 * jj + 1] = ffma2(ca2, k23, R[0][2 * jj + 1]);
+                    R[1][2 * jj] = ffma2(cb2, k01, R[1][2 * jj]);
+                    R[1][2 * jj + 1] = ffma2(cb2, k23, R[1][2 * jj + 1]);
+                    oa0 = ffma2(R[0][2 * jj], q01, oa0);
+                    oa1 = ffma2(R[0][2 * jj + 1], q23, oa1);
+                    ob0 = ffma2(R[1][2 * jj], q01, ob0);
+                    ob1 = ffma2(R[1][2 * jj + 1], q23, ob1);
                 }
                 gam = gnew;
             } else {
-                const float2 g2 = make_float2(gnew, gnew), c2 = make_float2(coef, coef);
+                const float2 g2 = make_float2(gnew, gnew);
+                const float2 ca2 = make_float2(coef_a, coef_a), cb2 = make_float2(coef_b, coef_b);
 #pragma unroll
-                for (int j = 0; j < kD / 4; ++j) {
-                    const float4 kk = lds128(k2 + 16 * j), qq = lds128(q2 + 16 * j);
-                    R[2 * j] = ffma2(c2, make_float2(kk.x, kk.y), fmul2(g2, R[2 * j]));
-                    R[2 * j + 1] = ffma2(c2, make_float2(kk.z, kk.w), fmul2(g2, R[2 * j + 1]));
-                    o0 = ffma2(R[2 * j], make_float2(qq.x, qq.y), o0);
-                    o1 = ffma2(R[2 * j + 1], make_float2(qq.z, qq.w), o1);
+                for (int jj = 0; jj < kD / 8; ++jj) {
+                    const float4 kk = lds128(k2 + 32 * jj), qq = lds128(q2 + 32 * jj);
+                    const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
+                    const float2 q01 = make_float2(qq.x, qq.y), q23 = make_float2(qq.z, qq.w);
+                    R[0][2 * jj] = ffma2(ca2, k01, fmul2(g2, R[0][2 * jj]));
+                    R[0][2 * jj + 1] = ffma2(ca2, k23, fmul2(g2, R[0][2 * jj + 1]));
+                    R[1][2 * jj] = ffma2(cb2, k01, fmul2(g2, R[1][2 * jj]));
+                    R[1][2 * jj + 1] = ffma2(cb2, k23, fmul2(g2, R[1][2 * jj + 1]));
+                    oa0 = ffma2(R[0][2 * jj], q01, oa0);
+                    oa1 = ffma2(R[0][2 * jj + 1], q23, oa1);
+                    ob0 = ffma2(R[1][2 * jj], q01, ob0);
+                    ob1 = ffma2(R[1][2 * jj + 1], q23, ob1);
                 }
                 gam = 1.0f;
             }
-            const float o = gam * ((o0.x + o0.y) + (o1.x + o1.y));
+            float sa = (oa0.x + oa0.y) + (oa1.x + oa1.y);
+            float sb = (ob0.x + ob0.y) + (ob1.x + ob1.y);
+            sa += __shfl_xor_sync(kFull, sa, 16);
+            sb += __shfl_xor_sync(kFull, sb, 16);
+            const float o = gam * (half ? sb : sa);     // lane pr stores row a0, lane 16 + pr row a0 + 1
             __stcs(orow + (int64_t)(c * kTC + tt) * p.o_stride, o * p.inv_sqrt_d);
         }
         __syncwarp();
     }
 
 #pragma unroll
-    for (int j = 0; j < kD / 4; ++j)
-        *reinterpret_cast<float4 *>(row + 4 * j) =
-            make_float4(gam * R[2 * j].x, gam * R[2 * j].y, gam * R[2 * j + 1].x, gam * R[2 * j + 1].y);
+    for (int rr = 0; rr < 2; ++rr) {
+#pragma unroll
+        for (int jj = 0; jj < kD / 8; ++jj)
+            *reinterpret_cast<float4 *>(row + rr * kD + 4 * (2 * jj + half)) =
+                make_float4(gam * R[rr][2 * jj].x, gam * R[rr][2 * jj].y,
+                            gam * R[rr][2 * jj + 1].x, gam * R[rr][2 * jj + 1].y);
+    }
 }
 
 // Any D <= 256 and any alignment: one CTA per (sequence, head), one warp per
