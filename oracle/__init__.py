@@ -66,6 +66,14 @@ def bind(path):
     lib.orc_f32_to_f16_array.restype = None
     lib.orc_f16_to_f32_array.argtypes = [P, P, u64]
     lib.orc_f16_to_f32_array.restype = None
+    lib.orc_conv_silu.argtypes = [i32, i32, P, P, P, P]
+    lib.orc_conv_silu.restype = None
+    lib.orc_l2norm_heads.argtypes = [i32, i32, P, f64]
+    lib.orc_l2norm_heads.restype = None
+    lib.orc_gates.argtypes = [i32, P, P, P, P, P, P]
+    lib.orc_gates.restype = None
+    lib.orc_decode_f64.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
+    lib.orc_decode_f64.restype = None
     return lib
 
 
@@ -162,6 +170,55 @@ def f16_to_f32_bits(h):
     dst = np.empty(src.shape, dtype=np.uint32)
     lib.orc_f16_to_f32_array(_ptr(src), _ptr(dst), src.size)
     return dst
+
+
+def conv_silu(ring, x, w):
+    """One token through the depthwise causal conv with silu, per channel.
+
+    ring: [taps][C] float32, shift register (updated in place, newest entry last);
+    x: [C] float32; w: [taps][C] float32.  Returns y: [C] float64."""
+    lib = _load()
+    assert ring.dtype == np.float32 and ring.flags.c_contiguous and ring.ndim == 2
+    taps, C = ring.shape
+    x, w = _c(x, np.float32), _c(w, np.float32)
+    assert x.size == C and w.size == taps * C
+    y = np.empty(C, dtype=np.float64)
+    lib.orc_conv_silu(taps, C, _ptr(ring), _ptr(x), _ptr(w), _ptr(y))
+    return y
+
+
+def l2norm_heads(y, d, eps):
+    """Per-head y / sqrt(sum y^2 + eps) over consecutive heads of d (fp64, returns a copy)."""
+    lib = _load()
+    y = np.array(y, dtype=np.float64, order="C")
+    assert y.size % d == 0
+    lib.orc_l2norm_heads(y.size // d, d, _ptr(y), float(eps))
+    return y
+
+
+def gates(br, ar, dt, rate):
+    """beta = sigmoid(br), alpha = (1 + e^(ar + dt))^rate, elementwise (fp64)."""
+    lib = _load()
+    br, ar, dt, rate = (_c(a, np.float32) for a in (br, ar, dt, rate))
+    n = br.size
+    assert ar.size == n and dt.size == n and rate.size == n
+    beta = np.empty(br.shape, dtype=np.float64)
+    alpha = np.empty(br.shape, dtype=np.float64)
+    lib.orc_gates(n, _ptr(br), _ptr(ar), _ptr(dt), _ptr(rate), _ptr(beta), _ptr(alpha))
+    return beta, alpha
+
+
+def decode_f64(S, q, k, v, alpha, beta, nk):
+    """decode() with fp64 token inputs (same layouts)."""
+    lib = _load()
+    assert S.dtype == np.float64 and S.flags.c_contiguous and S.ndim == 4
+    B, nv, d, _ = S.shape
+    q, k, v, alpha, beta = (_c(a, np.float64) for a in (q, k, v, alpha, beta))
+    assert q.size == B * nk * d and k.size == B * nk * d and v.size == B * nv * d
+    assert alpha.size == B * nv and beta.size == B * nv
+    o = np.empty((B, nv * d), dtype=np.float64)
+    lib.orc_decode_f64(B, nk, nv, d, _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o))
+    return o
 
 
 def parallel_map(fn, items, threads=None):

@@ -202,3 +202,72 @@ void orc_f16_to_f32_array(const uint16_t *src, uint32_t *dst, uint64_t n)
 {
     for (uint64_t i = 0; i < n; ++i) dst[i] = orc_f16_to_f32_bits(src[i]);
 }
+
+/* ---------------------------------------------------------------------------
+ * Producers upstream of the recurrence, for the fused decode from projections
+ * (ssm_gdn_a.rs `gdn_decode_f32_conv_norm`; gdn.rs `gk_conv_silu_l2`,
+ * `gk_gdn_gates`).
+ * ------------------------------------------------------------------------- */
+
+/* Depthwise causal conv over `channels` channels with a `taps`-deep ring
+ * ([gdn.rs] `gk_conv_silu`): the ring is a shift register, ring[t][c] for
+ * t = 0..taps-1, entry taps-1 the newest.  Shift every channel up by one,
+ * append this token's x, reduce with the per-channel taps w[t][c], apply
+ * silu(a) = a / (1 + e^-a).  The ring is updated in place. */
+void orc_conv_silu(int taps, int channels, float *ring, const float *x,
+                   const float *w, double *y)
+{
+    for (int c = 0; c < channels; ++c) {
+        for (int t = 0; t + 1 < taps; ++t)
+            ring[(int64_t)t * channels + c] = ring[(int64_t)(t + 1) * channels + c];
+        ring[(int64_t)(taps - 1) * channels + c] = x[c];
+        double acc = 0.0;
+        for (int t = 0; t < taps; ++t)
+            acc += (double)ring[(int64_t)t * channels + c] * (double)w[(int64_t)t * channels + c];
+        y[c] = acc / (1.0 + exp(-acc));
+    }
+}
+
+/* Per-head L2 normalisation ([gdn.rs] `gk_conv_silu_l2`, q and k heads):
+ * y / sqrt(sum_head y^2 + eps), eps added to the sum (not the mean). */
+void orc_l2norm_heads(int heads, int d, double *y, double eps)
+{
+    for (int h = 0; h < heads; ++h) {
+        double ss = 0.0;
+        for (int i = 0; i < d; ++i) ss += y[(int64_t)h * d + i] * y[(int64_t)h * d + i];
+        double den = sqrt(ss + eps);
+        for (int i = 0; i < d; ++i) y[(int64_t)h * d + i] /= den;
+    }
+}
+
+/* The two gates of a value head ([gdn.rs] `gk_gdn_gates`): write strength
+ * beta = sigmoid(br) and decay alpha = (1 + e^(ar + dt))^rate, where `rate`
+ * already holds the negative decay rate, so alpha = exp(rate * softplus(ar + dt)). */
+void orc_gates(int n, const float *br, const float *ar, const float *dt,
+               const float *rate, double *beta, double *alpha)
+{
+    for (int i = 0; i < n; ++i) {
+        beta[i] = 1.0 / (1.0 + exp(-(double)br[i]));
+        alpha[i] = pow(1.0 + exp((double)ar[i] + (double)dt[i]), (double)rate[i]);
+    }
+}
+
+/* orc_decode with fp64 token inputs (for inputs the oracle itself computed,
+ * e.g. by orc_conv_silu / orc_l2norm_heads / orc_gates), same layouts. */
+void orc_decode_f64(int batch, int nk, int nv, int d, double *S,
+                    const double *q, const double *k, const double *v,
+                    const double *alpha, const double *beta, double *o)
+{
+    double *work = malloc(sizeof(double) * d);
+    for (int b = 0; b < batch; ++b) {
+        for (int h = 0; h < nv; ++h) {
+            int g = h % nk;
+            head_step(d, S + ((int64_t)b * nv + h) * d * d,
+                      q + ((int64_t)b * nk + g) * d, k + ((int64_t)b * nk + g) * d,
+                      v + ((int64_t)b * nv + h) * d,
+                      alpha[(int64_t)b * nv + h], beta[(int64_t)b * nv + h],
+                      o + ((int64_t)b * nv + h) * d, work);
+        }
+    }
+    free(work);
+}

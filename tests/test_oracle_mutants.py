@@ -17,7 +17,7 @@ from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "gdn_oracle.c")
 
-# (name, original text, replacement) -- every original must occur exactly once.
+# (name, original text, replacement) -- every occurrence of the original is replaced.
 MUTANTS = [
     ("dropped alpha in the correction", "beta * (v[a] - alpha * work[a])", "beta * (v[a] - work[a])"),
     ("sign of the correction", "beta * (v[a] - alpha * work[a])", "beta * (v[a] + alpha * work[a])"),
@@ -38,6 +38,14 @@ MUTANTS = [
     ("truncating rounding", "if (rem > half || (rem == half && (n & 1u))) n += 1;", "(void)half;"),
     ("overflow saturates", "if (E > 15) return (uint16_t)(sign | 0x7c00u);", "if (E > 15) return (uint16_t)(sign | 0x7bffu);"),
     ("widened subnormal exponent off by one", "int32_t E = -14;\n        while", "int32_t E = -15;\n        while"),
+    ("conv ring not shifted", "ring[(int64_t)t * channels + c] = ring[(int64_t)(t + 1) * channels + c];",
+     "ring[(int64_t)t * channels + c] = ring[(int64_t)t * channels + c];"),
+    ("conv newest tap at the front", "ring[(int64_t)(taps - 1) * channels + c] = x[c];", "ring[c] = x[c];"),
+    ("conv without silu", "y[c] = acc / (1.0 + exp(-acc));", "y[c] = acc;"),
+    ("l2 eps on the mean", "double den = sqrt(ss + eps);", "double den = sqrt(ss / d + eps);"),
+    ("gate rate applied twice", "pow(1.0 + exp((double)ar[i] + (double)dt[i]), (double)rate[i])",
+     "pow(1.0 + exp((double)ar[i] + (double)dt[i]), -exp((double)rate[i]))"),
+    ("beta not a sigmoid", "beta[i] = 1.0 / (1.0 + exp(-(double)br[i]));", "beta[i] = (double)br[i];"),
     ("widening drops the sign", "return sign | (ex - 15u + 127u) << 23 | (fr << 13);", "return (ex - 15u + 127u) << 23 | (fr << 13);"),
 ]
 
@@ -63,7 +71,7 @@ def _pin_calls():
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(name, old, new, tmp_path):
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation anchor not unique/absent: {old!r}"
+    assert src.count(old) >= 1, f"mutation anchor absent: {old!r}"
     mut = tmp_path / "mut.c"
     mut.write_text(src.replace(old, new))
     so = tmp_path / "mut.so"

@@ -392,3 +392,66 @@ def test_f16_to_f32_exhaustive():
     # round trip binary16 -> binary32 -> binary16 is the identity on every non-NaN pattern
     back = oracle.f32_to_f16_bits(got)
     assert np.array_equal(back[~nan], h[~nan])
+
+
+# ---------------------------------------------------------------- producers (conv, L2, gates)
+
+def test_conv_is_causal_convolution_then_silu():
+    """Fed a stream from a zero ring, the conv pre-activation is numpy's full convolution with the
+    taps reversed (newest tap last), and the output is that through silu (scipy's logistic)."""
+    rng = np.random.default_rng(41)
+    taps, C, n = 4, 7, 12
+    w = rng.normal(size=(taps, C)).astype(np.float32)
+    xs = rng.normal(size=(n, C)).astype(np.float32)
+    ring = np.zeros((taps, C), np.float32)
+    ys = np.stack([oracle.conv_silu(ring, xs[t], w) for t in range(n)])
+    for c in range(C):
+        pre = np.convolve(xs[:, c].astype(np.float64), w[::-1, c].astype(np.float64))[:n]
+        np.testing.assert_allclose(ys[:, c], pre * expit(pre), rtol=1e-12, atol=1e-14)
+    # the ring holds the last `taps` inputs, oldest first
+    np.testing.assert_array_equal(ring, xs[-taps:])
+
+
+def test_conv_with_a_unit_newest_tap_is_silu_of_the_input():
+    taps, C = 4, 5
+    w = np.zeros((taps, C), np.float32)
+    w[taps - 1] = 1.0
+    ring = np.full((taps, C), 3.0, np.float32)
+    x = np.array([-2.0, -0.5, 0.0, 0.5, 2.0], np.float32)
+    y = oracle.conv_silu(ring, x, w)
+    np.testing.assert_allclose(y, x * expit(x.astype(np.float64)), rtol=1e-14)
+
+
+def test_l2norm_heads():
+    rng = np.random.default_rng(42)
+    y = rng.normal(size=(3, 8))
+    out = oracle.l2norm_heads(y.reshape(-1), 8, 0.0).reshape(3, 8)
+    np.testing.assert_allclose(np.linalg.norm(out, axis=1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(out * np.linalg.norm(y, axis=1, keepdims=True), y, rtol=1e-13)
+    # eps is added to the sum of squares: (3, 4) with eps 11 -> (3, 4) / 6
+    np.testing.assert_allclose(oracle.l2norm_heads(np.array([3.0, 4.0]), 2, 11.0), [0.5, 4.0 / 6.0], rtol=1e-15)
+
+
+def test_gates_closed_forms():
+    rng = np.random.default_rng(43)
+    n = 64
+    br, ar, dt = (rng.normal(size=n).astype(np.float32) for _ in range(3))
+    rate = (-np.exp(rng.normal(size=n) - 3.0)).astype(np.float32)   # negative rates, |rate| < 0.1 typical
+    beta, alpha = oracle.gates(br, ar, dt, rate)
+    np.testing.assert_allclose(beta, expit(br.astype(np.float64)), rtol=1e-14)
+    # alpha = exp(rate * softplus(ar + dt)), softplus from numpy's logaddexp
+    sp = np.logaddexp(0.0, ar.astype(np.float64) + dt.astype(np.float64))
+    np.testing.assert_allclose(alpha, np.exp(rate.astype(np.float64) * sp), rtol=1e-13)
+    assert np.all((alpha > 0) & (alpha < 1))
+    # rate = -1, ar + dt = 0: alpha = 1/2 exactly
+    b1, a1 = oracle.gates(*(np.array([v], np.float32) for v in (0.0, 0.0, 0.0, -1.0)))
+    assert a1[0] == 0.5 and b1[0] == 0.5
+
+
+def test_decode_f64_matches_decode_on_f32_representable_inputs():
+    S, q, k, v, a, b = rand_case(2, 2, 3, 8)
+    S2 = S.copy()
+    o1 = oracle.decode(S, q, k, v, a, b, 2)
+    o2 = oracle.decode_f64(S2, q.astype(np.float64), k.astype(np.float64), v.astype(np.float64),
+                           a.astype(np.float64), b.astype(np.float64), 2)
+    assert np.array_equal(S, S2) and np.array_equal(o1, o2)
