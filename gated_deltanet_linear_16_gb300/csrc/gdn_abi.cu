@@ -183,6 +183,61 @@ GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
                         out_stride, true, stream);
 }
 
+GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pitch,
+                                 float *conv_state, int64_t conv_pitch, int taps,
+                                 const float *x, const float *conv_w,
+                                 const float *br, const float *ar, const float *dt, const float *rate,
+                                 const float *z, const float *gn, float l2_eps, float eps,
+                                 uint16_t *out,
+                                 int batch, int nk, int nv, int d,
+                                 int64_t x_stride, int64_t gate_stride, int64_t z_stride,
+                                 int64_t out_stride, void *stream)
+{
+    int st = check_common(batch, nk, nv, d, state_pitch, state_dtype);
+    if (st != GDN_OK) return st;
+    if (nv % nk != 0) return GDN_ERR_UNSUPPORTED;
+    if (taps < 1 || taps > 8) return GDN_ERR_ARG;
+    if (!(eps >= 0.0f && std::isfinite(eps)) || !(l2_eps >= 0.0f && std::isfinite(l2_eps))) return GDN_ERR_ARG;
+    const int repeat = nv / nk;
+    // the general kernel keeps q, k, every value head's v, o and the gates in shared memory
+    if ((size_t)(3 + repeat) * d * 4 + 8 * (size_t)repeat > 48 * 1024) return GDN_ERR_UNSUPPORTED;
+    const int64_t selem = state_dtype == GDN_STATE_F16 ? 2 : 4;
+    const int64_t B = batch, hv = (int64_t)nv * d, C = (int64_t)(2 * nk + nv) * d;
+    if (conv_pitch < taps * C) return GDN_ERR_ARG;
+    Operand ops[12] = {
+        {state, B, (int64_t)nv * d * d, state_pitch, selem},
+        {conv_state, B, taps * C, conv_pitch, 4},
+        {out, B, hv, out_stride, 2},
+        {x, B, C, x_stride, 4},
+        {conv_w, 1, taps * C, taps * C, 4},
+        {br, B, nv, gate_stride, 4},
+        {ar, B, nv, gate_stride, 4},
+        {dt, 1, nv, nv, 4},
+        {rate, 1, nv, nv, 4},
+        {z, B, hv, z_stride, 4},
+        {gn, 1, d, d, 4},
+    };
+    const int n_ops = 11;
+    if (batch == 0) {
+        for (int i = 0; i < n_ops; ++i) if (ops[i].p == nullptr) return GDN_ERR_ARG;
+        return GDN_OK;
+    }
+    st = check_operands(ops, n_ops, 3);
+    if (st != GDN_OK) return st;
+
+    ConvNormParams p{};
+    p.state = state; p.pitch = state_pitch;
+    p.ring = conv_state; p.ring_pitch = conv_pitch;
+    p.x = x; p.x_stride = x_stride; p.w = conv_w;
+    p.br = br; p.ar = ar; p.gate_stride = gate_stride; p.dt = dt; p.rate = rate;
+    p.z = z; p.gn = gn; p.out = out; p.z_stride = z_stride; p.out_stride = out_stride;
+    p.batch = batch; p.nk = nk; p.nv = nv; p.d = d; p.taps = taps; p.repeat = repeat;
+    p.l2_eps = l2_eps; p.eps = eps; p.inv_sqrt_d = inv_sqrt(d);
+    // D == 128 cluster kernel: 16-byte state rows, at most 8 value heads per key head (cluster size)
+    const bool fast = d == 128 && repeat <= 8 && vec16(state) && (state_pitch * selem) % 16 == 0;
+    return cuda_status(launch_conv_norm(p, state_dtype == GDN_STATE_F16, fast, (cudaStream_t)stream));
+}
+
 GDN_API int gdn_decode_chunk2(void *state, int state_dtype, int64_t state_pitch,
                               void *state_mid, int64_t mid_pitch,
                               const float *q, const float *k, const float *v,

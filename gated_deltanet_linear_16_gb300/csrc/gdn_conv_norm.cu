@@ -1,0 +1,355 @@
+// gdn_conv_norm.cu -- one decode token from the projection outputs to the
+// normed bf16 output in a single launch: the depthwise causal conv ring update
+// with silu on q, k and v, the per-head L2 normalisation of q and k, the two
+// gates from their logits, the gated delta rule step and the gated RMS norm.
+//
+// Follows metrale_model_layers/layers/ops/ssm_gdn_a.rs, launcher
+// `gdn_decode_f32_conv_norm` (conv update, L2 norm, recurrence and gated norm
+// in one decode launch; each ring row has exactly one writer), and
+// logicaffeine_compile/codegen_cuda/gdn.rs: `gk_conv_silu_l2` (shift the ring
+// by one, append the token, reduce with the taps, silu; L2 of the q/k heads
+// with den = sqrt(sum x^2 + eps)), `gk_gdn_gates` (beta = sigmoid(br), alpha
+// = (1 + e^(ar + dt))^rate with rate the stored negative decay rate),
+// `gdn_step` and `gdn_gate_norm`.
+//
+// GB300 design.  The page's launcher gives one block to a key head and its
+// NV/NK value heads.  Here the value heads keep one CTA each -- the decode
+// kernel's shape (8 warps x 16 rows), so the 64 KB-per-head state stream is
+// unchanged -- and the NV/NK CTAs of a key head form a thread-block cluster:
+//  * every CTA issues its state loads first, then updates the ring rows of its
+//    own value head's v channels and computes v (one writer per ring row);
+//  * cluster rank 0 also computes the key head's q and k (conv, silu, L2) into
+//    its shared memory and updates their ring rows;
+//  * after one cluster barrier every CTA reads q and k from rank 0's shared
+//    memory (distributed shared memory), a second barrier lets rank 0 retire,
+//    and the step + norm run as in the decode kernel.
+// Cluster barriers are hardware barriers (no spin loop on a flag).
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kWarps = 8;
+constexpr int kRowsPerWarp = kD / kWarps;   // 16
+
+__device__ __forceinline__ unsigned cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of `p` (this CTA's shared memory) in the shared memory of cluster rank `rank`.
+__device__ __forceinline__ unsigned map_to_rank(const void *p, unsigned rank) {
+    const unsigned local = (unsigned)__cvta_generic_to_shared(p);
+    unsigned remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    return remote;
+}
+__device__ __forceinline__ float4 ld_cluster4(unsigned addr) {
+    float4 r;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr) : "memory");
+    return r;
+}
+
+// One channel through the conv ring: shift up by one, append x, reduce with the
+// taps, silu.  The caller is the only thread touching this channel.
+__device__ __forceinline__ float conv_silu_channel(float *ring, const float *x, const float *w,
+                                                   int64_t c, int64_t C, int taps) {
+    float acc = 0.f;
+    for (int t = 0; t + 1 < taps; ++t) {
+        const float val = ring[(int64_t)(t + 1) * C + c];
+        ring[(int64_t)t * C + c] = val;
+        acc = fmaf(val, __ldg(w + (int64_t)t * C + c), acc);
+    }
+    const float xv = __ldg(x + c);
+    ring[(int64_t)(taps - 1) * C + c] = xv;
+    acc = fmaf(xv, __ldg(w + (int64_t)(taps - 1) * C + c), acc);
+    return silu(acc);
+}
+
+__device__ __forceinline__ void gates(const ConvNormParams &p, int seq, int h, float &alpha, float &beta) {
+    const float br = __ldg(p.br + seq * p.gate_stride + h);
+    const float ar = __ldg(p.ar + seq * p.gate_stride + h);
+    beta = 1.0f / (1.0f + expf(-br));
+    alpha = powf(1.0f + expf(ar + __ldg(p.dt + h)), __ldg(p.rate + h));
+}
+
+template <typename TS, int NB, int MINB>
+__global__ void __launch_bounds__(kWarps * 32, MINB)
+conv_norm_d128(const ConvNormParams p)
+{
+    using V = Vec16<TS>;
+    constexpr int EPV = V::N;
+    constexpr int LPR = kD / EPV;
+    constexpr int RPL = 32 / LPR;
+    constexpr int NLD = kRowsPerWarp / RPL;
+    constexpr int LPB = NLD / NB;
+    static_assert(NLD % NB == 0, "shape");
+
+    __shared__ __align__(16) float q_s[kD];
+    __shared__ __align__(16) float k_s[kD];
+    __shared__ float v_s[kD];
+    __shared__ float red_q[4], red_k[4], red[kWarps];
+    __shared__ float gate_s[2];
+
+    const unsigned rank = cluster_rank();               // which value head of the key head
+    const int cl = blockIdx.x / p.repeat;               // (sequence, key head)
+    const int seq = cl / p.nk;
+    const int kh = cl - seq * p.nk;
+    const int h = kh + (int)rank * p.nk;                // tiled pairing: h mod NK == kh
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int sub = lane / LPR;
+    const int col = (lane % LPR) * EPV;
+    const int row0 = warp * kRowsPerWarp;
+    const int64_t C = (int64_t)(2 * p.nk + p.nv) * kD;
+
+    TS *rowp = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD +
+               (int64_t)(row0 + sub) * kD + col;
+
+    // 1. state loads in flight before the producers run
+    uint4 raw[NB > 1 ? 2 : 1][LPB];
+#pragma unroll
+    for (int i = 0; i < LPB; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
+
+    // 2. producers: v of this head (threads 0..127); q and k of the key head on rank 0 (128..255)
+    float *ring = p.ring + seq * p.ring_pitch;
+    const float *x = p.x + seq * p.x_stride;
+    if (tid < kD) {
+        v_s[tid] = conv_silu_channel(ring, x, p.w, 2 * (int64_t)p.nk * kD + (int64_t)h * kD + tid, C, p.taps);
+    } else if (rank == 0) {
+        const int i = tid - kD;
+        const float qv = conv_silu_channel(ring, x, p.w, (int64_t)kh * kD + i, C, p.taps);
+        const float kv = conv_silu_channel(ring, x, p.w, (int64_t)(p.nk + kh) * kD + i, C, p.taps);
+        const float sq = group_sum<32>(qv * qv), sk = group_sum<32>(kv * kv);
+        if (lane == 0) { red_q[warp - 4] = sq; red_k[warp - 4] = sk; }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four producer warps
+        const float tq = (red_q[0] + red_q[1]) + (red_q[2] + red_q[3]);
+        const float tk = (red_k[0] + red_k[1]) + (red_k[2] + red_k[3]);
+        q_s[i] = qv / sqrtf(tq + p.l2_eps);
+        k_s[i] = kv / sqrtf(tk + p.l2_eps);
+    }
+    if (tid == 0) gates(p, seq, h, gate_s[0], gate_s[1]);
+    __syncthreads();
+    cluster_sync_all();                                  // rank 0's q, k visible cluster-wide
+
+    // 3. this lane's columns of q and k from rank 0's shared memory
+    float kx[EPV], qx[EPV];
+    {
+        const unsigned ka = map_to_rank(k_s + col, 0), qa = map_to_rank(q_s + col, 0);
+#pragma unroll
+        for (int j = 0; j < EPV; j += 4) {
+            const float4 a = ld_cluster4(ka + 4 * j), b = ld_cluster4(qa + 4 * j);
+            kx[j] = a.x; kx[j + 1] = a.y; kx[j + 2] = a.z; kx[j + 3] = a.w;
+            qx[j] = b.x; qx[j + 1] = b.y; qx[j + 2] = b.z; qx[j + 3] = b.w;
+        }
+    }
+    cluster_sync_all();                                  // every CTA has read rank 0's q, k
+
+    const bool row_lane = lane < kRowsPerWarp;
+    const float v_l = row_lane ? v_s[row0 + lane] : 0.f;
+    float z_l = 0.f, gn_l = 0.f;
+    if (row_lane) {
+        z_l = __ldg(p.z + seq * p.z_stride + (int64_t)h * kD + row0 + lane);
+        gn_l = __ldg(p.gn + row0 + lane);
+    }
+    const float alpha = gate_s[0], beta = gate_s[1];
+    float kq = 0.f;
+#pragma unroll
+    for (int j = 0; j < EPV; ++j) kq = fmaf(kx[j], qx[j], kq);
+    kq = group_sum<LPR>(kq);
+
+    // 4. the step, as in the decode kernel
+    float o_keep = 0.f;
+#pragma unroll
+    for (int bt = 0; bt < NB; ++bt) {
+        if (bt + 1 < NB) {
+#pragma unroll
+            for (int i = 0; i < LPB; ++i)
+                raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * LPB + i) * RPL * kD);
+        }
+#pragma unroll
+        for (int ii = 0; ii < LPB; ++ii) {
+            const int i = bt * LPB + ii;
+            float s[EPV];
+            V::unpack(raw[bt & 1][ii], s);
+            float u = 0.f, w = 0.f;
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
+            u = group_sum<LPR>(u);
+            w = group_sum<LPR>(w);
+            const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
+            const float coef = beta * (va - alpha * u);
+            const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
+            st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
+            if constexpr (RPL == 1) {
+                if (lane == i) o_keep = oa;
+            } else {
+#pragma unroll
+                for (int r = 0; r < RPL; ++r) {
+                    const float orr = __shfl_sync(kFull, oa, r * LPR);
+                    if (lane == i * RPL + r) o_keep = orr;
+                }
+            }
+        }
+    }
+
+    // 5. gated RMS norm over the head's outputs
+    const float ss = group_sum<32>(o_keep * o_keep);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) tot += red[i];
+    const float rstd = rsqrtf(tot * (1.0f / kD) + p.eps);
+    if (row_lane) {
+        const float y = gn_l * o_keep * rstd * silu(z_l);
+        p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
+    }
+}
+
+// Any 1 <= D <= 256, any alignment, any NV/NK: one CTA per (sequence, key
+// head); the producers for the key head and all of its value heads go to
+// shared memory, then the value heads are stepped one after the other (warp
+// per row) and normed.
+constexpr int kGenWarps = 4;
+constexpr int kMaxD = 256;
+
+template <typename TS>
+__global__ void __launch_bounds__(kGenWarps * 32)
+conv_norm_generic(const ConvNormParams p)
+{
+    constexpr int MAXV = kMaxD / 32;
+    extern __shared__ float dyn[];               // q[D], k[D], v[repeat][D], o[D], gates[2 repeat]
+    __shared__ float red[kGenWarps], red2[kGenWarps];
+
+    const int D = p.d, R = p.repeat;
+    const int seq = blockIdx.x / p.nk;
+    const int kh = blockIdx.x - seq * p.nk;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t C = (int64_t)(2 * p.nk + p.nv) * D;
+    float *q_s = dyn, *k_s = dyn + D, *v_s = dyn + 2 * D, *o_s = dyn + (2 + R) * D, *g_s = o_s + D;
+
+    float *ring = p.ring + seq * p.ring_pitch;
+    const float *x = p.x + seq * p.x_stride;
+    for (int i = tid; i < D; i += kGenWarps * 32) {
+        q_s[i] = conv_silu_channel(ring, x, p.w, (int64_t)kh * D + i, C, p.taps);
+        k_s[i] = conv_silu_channel(ring, x, p.w, (int64_t)(p.nk + kh) * D + i, C, p.taps);
+    }
+    for (int i = tid; i < R * D; i += kGenWarps * 32) {
+        const int r = i / D, j = i - r * D;
+        const int h = kh + r * p.nk;
+        v_s[i] = conv_silu_channel(ring, x, p.w, 2 * (int64_t)p.nk * D + (int64_t)h * D + j, C, p.taps);
+    }
+    if (tid < R) gates(p, seq, kh + tid * p.nk, g_s[2 * tid], g_s[2 * tid + 1]);
+    __syncthreads();
+    {   // L2 of q and k
+        float sq = 0.f, sk = 0.f;
+        for (int i = tid; i < D; i += kGenWarps * 32) { sq += q_s[i] * q_s[i]; sk += k_s[i] * k_s[i]; }
+        sq = group_sum<32>(sq); sk = group_sum<32>(sk);
+        if (lane == 0) { red[warp] = sq; red2[warp] = sk; }
+        __syncthreads();
+        float tq = 0.f, tk = 0.f;
+#pragma unroll
+        for (int i = 0; i < kGenWarps; ++i) { tq += red[i]; tk += red2[i]; }
+        const float dq = sqrtf(tq + p.l2_eps), dk = sqrtf(tk + p.l2_eps);
+        __syncthreads();
+        for (int i = tid; i < D; i += kGenWarps * 32) { q_s[i] = q_s[i] / dq; k_s[i] = k_s[i] / dk; }
+        __syncthreads();
+    }
+    float kreg[MAXV], qreg[MAXV];
+    float kq = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+        const int c = lane + 32 * j;
+        kreg[j] = c < D ? k_s[c] : 0.f;
+        qreg[j] = c < D ? q_s[c] : 0.f;
+        kq = fmaf(kreg[j], qreg[j], kq);
+    }
+    kq = group_sum<32>(kq);
+
+    for (int r = 0; r < R; ++r) {
+        const int h = kh + r * p.nk;
+        const float alpha = g_s[2 * r], beta = g_s[2 * r + 1];
+        TS *S = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * D * D;
+        for (int a = warp; a < D; a += kGenWarps) {
+            TS *row = S + (int64_t)a * D;
+            float s[MAXV];
+            float u = 0.f, w = 0.f;
+#pragma unroll
+            for (int j = 0; j < MAXV; ++j) {
+                const int c = lane + 32 * j;
+                s[j] = c < D ? to_f32<TS>(row[c]) : 0.f;
+                u = fmaf(s[j], kreg[j], u);
+                w = fmaf(s[j], qreg[j], w);
+            }
+            u = group_sum<32>(u);
+            w = group_sum<32>(w);
+            const float coef = beta * (v_s[r * D + a] - alpha * u);
+            const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
+#pragma unroll
+            for (int j = 0; j < MAXV; ++j) {
+                const int c = lane + 32 * j;
+                if (c < D) row[c] = from_f32<TS>(fmaf(coef, kreg[j], alpha * s[j]));
+            }
+            if (lane == 0) o_s[a] = oa;
+        }
+        __syncthreads();
+        float ss = 0.f;
+        for (int a = tid; a < D; a += kGenWarps * 32) ss += o_s[a] * o_s[a];
+        ss = group_sum<32>(ss);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int i = 0; i < kGenWarps; ++i) tot += red[i];
+        const float rstd = rsqrtf(tot / (float)D + p.eps);
+        const float *zp = p.z + seq * p.z_stride + (int64_t)h * D;
+        uint16_t *op = p.out + seq * p.out_stride + (int64_t)h * D;
+        for (int a = tid; a < D; a += kGenWarps * 32)
+            op[a] = bf16_bits_rn(p.gn[a] * o_s[a] * rstd * silu(zp[a]));
+        __syncthreads();                          // o_s and red reused by the next head
+    }
+}
+
+template <typename TS> struct ConvShape { static constexpr int kBatches = 4, kMinBlocks = 3; };
+template <> struct ConvShape<__half> { static constexpr int kBatches = 2, kMinBlocks = 3; };
+
+template <typename TS>
+cudaError_t launch_typed(const ConvNormParams &p, bool fast, cudaStream_t s)
+{
+    if (fast) {
+        using F = ConvShape<TS>;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((int64_t)p.batch * p.nv), 1, 1);
+        cfg.blockDim = dim3(kWarps * 32, 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)p.repeat;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, conv_norm_d128<TS, F::kBatches, F::kMinBlocks>, p);
+    }
+    const size_t smem = sizeof(float) * ((size_t)(3 + p.repeat) * p.d + 2 * (size_t)p.repeat);
+    conv_norm_generic<TS><<<(unsigned)((int64_t)p.batch * p.nk), kGenWarps * 32, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_conv_norm(const ConvNormParams &p, bool f16_state, bool fast, cudaStream_t s)
+{
+    return f16_state ? launch_typed<__half>(p, fast, s) : launch_typed<float>(p, fast, s);
+}
+
+}  // namespace gdn

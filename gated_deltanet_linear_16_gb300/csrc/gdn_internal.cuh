@@ -41,12 +41,33 @@ struct PrefillParams {
     unsigned zero;          // always 0; see prefill_d128 (orders shared loads)
 };
 
+// The fused decode from projections: conv ring update + silu, L2 of q/k,
+// gates from logits, the recurrence and the gated norm.
+struct ConvNormParams {
+    void *state;
+    int64_t pitch;
+    float *ring;            // [batch] slots of taps * C, [tap][channel], newest tap last
+    int64_t ring_pitch;
+    const float *x;         // [batch] rows of C = 2*NK*D + NV*D: [q heads | k heads | v heads]
+    int64_t x_stride;
+    const float *w;         // [taps][C]
+    const float *br, *ar;   // [batch] rows of NV gate logits
+    int64_t gate_stride;
+    const float *dt, *rate; // [NV]
+    const float *z, *gn;
+    uint16_t *out;
+    int64_t z_stride, out_stride;
+    int batch, nk, nv, d, taps, repeat;   // repeat = NV / NK value heads per key head
+    float l2_eps, eps, inv_sqrt_d;
+};
+
 // Launchers (one per translation unit family).  They pick the kernel variant
 // (fast D == 128 path when the alignment allows it, general otherwise) and
 // return the launch status.
 cudaError_t launch_decode(const DecodeParams &p, bool f16_state, bool norm, bool fast, cudaStream_t s);
 cudaError_t launch_decode_chunk2(const DecodeParams &p, bool f16_state, bool fast, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, bool fast, cudaStream_t s);
+cudaError_t launch_conv_norm(const ConvNormParams &p, bool f16_state, bool fast, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, bool vec, cudaStream_t s);
 cudaError_t launch_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, bool vec, cudaStream_t s);
 

@@ -44,7 +44,7 @@ import numpy as np
 __all__ = [
     "GAMMA", "mix64", "key_of", "stream_u64", "normals",
     "TENSOR_IDS", "decode_inputs", "prefill_inputs", "norm_weight",
-    "state_heads", "head_normals",
+    "state_heads", "head_normals", "conv_decode_inputs",
 ]
 
 GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -52,7 +52,8 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 # One id per drawn tensor, so streams of different tensors never coincide.
-TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "z": 4, "alpha": 5, "beta": 6, "gn": 7, "state": 8}
+TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "z": 4, "alpha": 5, "beta": 6, "gn": 7, "state": 8,
+              "x": 9, "ring": 10, "conv_w": 11, "br": 12, "ar": 13, "dt": 14, "a_log": 15}
 
 
 def mix64(z):
@@ -165,3 +166,28 @@ def state_heads(seed, seqs, heads, d, layer=0, std=0.02, dtype=np.float32):
     x = head_normals(seed, "state", layer, 0, seqs, heads, d * d) * std
     x = x.reshape(len(seqs), len(heads), d, d)
     return x.astype(dtype)
+
+
+def conv_decode_inputs(seed, batch, nk, nv, d, taps=4, layer=0, step=0):
+    """Inputs of the fused decode from projections (conv, L2, gates, step, norm), fp32.
+
+    x: [B][C] projection of this token, C = 2*NK*D + NV*D laid out [q heads | k heads | v heads],
+    ~ N(0,1); ring: [B][taps][C] conv state (the previous tokens' projections) ~ N(0,1);
+    conv_w: [taps][C] ~ N(0, 0.5^2); br, ar: [B][NV] gate logits ~ N(0,1);
+    dt: [NV] ~ N(0,1); rate: [NV] = -exp(a_log), a_log ~ N(-3, 1) (a negative decay rate, as a
+    checkpoint stores it); z: [B][NV*D] ~ N(0,1).
+    """
+    C = 2 * nk * d + nv * d
+    seqs = np.arange(batch)
+    one = np.arange(1)
+    x = head_normals(seed, "x", layer, step, seqs, one, C)[:, 0]
+    ring = head_normals(seed, "ring", layer, step, seqs, one, taps * C)[:, 0].reshape(batch, taps, C)
+    w = 0.5 * head_normals(seed, "conv_w", layer, 0, one, one, taps * C)[0, 0].reshape(taps, C)
+    br = head_normals(seed, "br", layer, step, seqs, np.arange(nv), 1)[..., 0]
+    ar = head_normals(seed, "ar", layer, step, seqs, np.arange(nv), 1)[..., 0]
+    dt = head_normals(seed, "dt", layer, 0, one, np.arange(nv), 1)[0, :, 0]
+    rate = -np.exp(head_normals(seed, "a_log", layer, 0, one, np.arange(nv), 1)[0, :, 0] - 3.0)
+    z = head_normals(seed, "z", layer, step, seqs, np.arange(nv), d).reshape(batch, nv * d)
+    f32 = np.float32
+    return {"x": x.astype(f32), "ring": ring.astype(f32), "conv_w": w.astype(f32), "br": br.astype(f32),
+            "ar": ar.astype(f32), "dt": dt.astype(f32), "rate": rate.astype(f32), "z": z.astype(f32)}

@@ -119,6 +119,42 @@ GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
                             int64_t z_stride, int64_t out_stride, void *stream);
 
 /*
+ * gdn_decode_conv_norm -- one token from the projection outputs to the normed
+ * bf16 output in one launch: the depthwise causal conv ring update with silu
+ * on q, k and v, the per-head L2 normalisation of q and k, the gates from
+ * their logits, the recurrence and the gated RMS norm.
+ *   Defined by: ssm_gdn_a.rs, launcher `gdn_decode_f32_conv_norm` (conv
+ *   update, L2 norm, recurrence and gated norm in one decode launch);
+ *   gdn.rs `gk_conv_silu_l2` (ring shifted by one, the token appended,
+ *   reduced with the taps, silu; q/k heads divided by sqrt(sum y^2 +
+ *   l2_eps)), `gk_gdn_gates` (beta = sigmoid(br), alpha = (1 + e^(ar +
+ *   dt))^rate, rate the stored negative decay rate), `gdn_step`,
+ *   `gdn_gate_norm`.
+ *   C            conv channels = 2*NK*D + NV*D, ordered [q heads | k heads |
+ *                v heads] (value head h's v channels at 2*NK*D + h*D).
+ *   conv_state   [batch] slots of taps*C fp32, slot pitch conv_pitch >= taps*C
+ *                elements, [tap][channel] with tap taps-1 the newest; updated
+ *                in place (shifted by one, this token appended).
+ *   taps         1..8.
+ *   x            [batch] rows of C fp32: this token's projection.
+ *   conv_w       [taps][C] fp32 conv taps.
+ *   br, ar       [batch] rows of NV gate logits.  dt, rate: [NV].
+ *   z, gn, eps, out as gdn_decode_norm; l2_eps >= 0 for the q/k norm.
+ *   NV must be a multiple of NK (the value heads of a key head are h = kh +
+ *   r*NK, r < NV/NK).  State and output as gdn_decode_norm.
+ *   Errors as gdn_decode_norm; GDN_ERR_UNSUPPORTED if NV % NK != 0.
+ */
+GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pitch,
+                                 float *conv_state, int64_t conv_pitch, int taps,
+                                 const float *x, const float *conv_w,
+                                 const float *br, const float *ar, const float *dt, const float *rate,
+                                 const float *z, const float *gn, float l2_eps, float eps,
+                                 uint16_t *out,
+                                 int batch, int nk, int nv, int d,
+                                 int64_t x_stride, int64_t gate_stride, int64_t z_stride,
+                                 int64_t out_stride, void *stream);
+
+/*
  * gdn_decode_chunk2 -- two tokens per sequence through the recurrence in one
  * launch (the verify step of speculative decoding), keeping the state after
  * the first token so that a rejected draft token can be rolled back.
