@@ -53,7 +53,10 @@ REF_LAYERS_PER_STEP = 4      # oracle sample per step of the reference arm
 # Per-launch DRAM traffic of the decode kernel from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), valid only while the kernel source is the one it was taken on.
 NCU_TRAFFIC = {
-    "decode_norm_f32": {"bytes_per_launch": None, "src_sha256": None},
+    # mean of three mid-sequence launches of the full 48-layer workload, ncu --cache-control none
+    # (reads 102.8 MB, writes 97.3-99.8 MB); see profiles/decode_d128_f32_norm_batched48.md
+    "decode_norm_f32": {"bytes_per_launch": 201655381,
+                        "src_sha256": "03ba002784052c17ff9e4746f11b9cc402d8f6bf5298c982a72bbbc6f1980afa"},
 }
 
 
@@ -405,7 +408,7 @@ def time_fn(torch, stream, fn, reps, warm=2):
 
 
 def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096, graph=True):
-    want = set(only.split(",")) if only else {"fp16", "conv", "latency", "prefill", "chunk2"}
+    want = set(only.split(",")) if only else {"fp16", "conv", "latency", "prefill", "chunk2", "convnorm"}
     rows = {}
     torch.cuda.empty_cache()
     if want & {"fp16", "conv"}:
@@ -414,9 +417,39 @@ def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096, graph=
         rows.update(row_latency(torch, gdn, dev, stream, graph))
     if "chunk2" in want:
         rows.update(row_chunk2(torch, gdn, dev, stream, pk))
+    if "convnorm" in want:
+        rows.update(row_conv_norm(torch, gdn, dev, stream, pk))
     if "prefill" in want:
         rows.update(row_prefill(torch, gdn, dev, stream, pk, prefill_tokens))
     return rows
+
+
+def row_conv_norm(torch, gdn, dev, stream, pk, taps=4):
+    """Fused decode from projections on one layer at batch 32 (fp32 state): conv ring update +
+    silu, q/k L2 norm, gates from logits, the step and the gated norm in one launch."""
+    import gdn_synth as gs
+    x = gs.conv_decode_inputs(SEED, B, NK, NV, D, taps)
+    t = {k: torch.from_numpy(v).to(dev) for k, v in x.items()}
+    C = (2 * NK + NV) * D
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    S = torch.empty((B, NV, D, D), device=dev).normal_(0.0, 0.02, generator=g)
+    ring = t["ring"].reshape(B, taps * C).contiguous()
+    gn = torch.from_numpy(gs.norm_weight(SEED, D)).to(dev)
+    out = torch.empty((B, NV * D), dtype=torch.int16, device=dev)
+    s = time_fn(torch, stream, lambda: gdn.gdn_decode_conv_norm(
+        S, ring, t["x"], t["conv_w"], t["br"], t["ar"], t["dt"], t["rate"], t["z"], gn, out,
+        batch=B, nk=NK, nv=NV, d=D, taps=taps, stream=stream.cuda_stream), 50)
+    # state read + write; ring: taps-1 entries read, all taps written; x, z read; w, dt, rate, gn once;
+    # gate logits read; bf16 out written
+    by = (B * NV * D * D * 4 * 2 + B * ((taps - 1) + taps + 1) * C * 4 + taps * C * 4
+          + B * NV * D * 4 + B * NV * 2 * 4 + 2 * NV * 4 + D * 4 + B * NV * D * 2)
+    del S, ring, gn, out, t
+    torch.cuda.empty_cache()
+    return {"conv_norm_from_projections": {
+        "config": "B=32 NK=16 NV=48 D=128 fp32, 4-tap conv, clusters of 3 CTAs", "us_per_launch": s * 1e6,
+        "token_heads_per_s": B * NV / s, "achieved_gbs": by / s / 1e9,
+        "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}}
 
 
 def row_chunk2(torch, gdn, dev, stream, pk):
