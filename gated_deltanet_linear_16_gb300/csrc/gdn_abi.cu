@@ -291,12 +291,12 @@ GDN_API int gdn_prefill_seq(void *state, int state_dtype, int64_t state_pitch,
 {
     int st = check_common(batch, nk, nv, d, state_pitch, state_dtype);
     if (st != GDN_OK) return st;
-    if (state_dtype != GDN_STATE_F32) return GDN_ERR_UNSUPPORTED;
     if (seq_len < 0) return GDN_ERR_ARG;
+    const int64_t selem = state_dtype == GDN_STATE_F16 ? 2 : 4;
     const int64_t B = batch, R = (int64_t)batch * seq_len;
     const int64_t hv = (int64_t)nv * d, hk = (int64_t)nk * d;
     Operand ops[7] = {
-        {state, B, (int64_t)nv * d * d, state_pitch, 4},
+        {state, B, (int64_t)nv * d * d, state_pitch, selem},
         {o, R, hv, o_stride, 4},
         {q, R, hk, qk_stride, 4},
         {k, R, hk, qk_stride, 4},
@@ -312,17 +312,17 @@ GDN_API int gdn_prefill_seq(void *state, int state_dtype, int64_t state_pitch,
     if (st != GDN_OK) return st;
 
     PrefillParams p{};
-    p.state = (float *)state; p.pitch = state_pitch;
+    p.state = state; p.pitch = state_pitch;
     p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.o = o;
     p.qk_stride = qk_stride; p.v_stride = v_stride; p.gb_stride = gb_stride; p.o_stride = o_stride;
     p.batch = batch; p.seq_len = seq_len; p.nk = nk; p.nv = nv; p.d = d;
     p.inv_sqrt_d = inv_sqrt(d);
     p.zero = 0;
     // D == 128 path: 16-byte state rows, 16-byte k/q rows and 16-byte v row blocks
-    const bool fast = d == 128 && vec16(state) && (state_pitch * 4) % 16 == 0 &&
+    const bool fast = d == 128 && vec16(state) && (state_pitch * selem) % 16 == 0 &&
                       vec16(q) && vec16(k) && (qk_stride * 4) % 16 == 0 &&
                       vec16(v) && (v_stride * 4) % 16 == 0;
-    return cuda_status(launch_prefill(p, fast, (cudaStream_t)stream));
+    return cuda_status(launch_prefill(p, state_dtype == GDN_STATE_F16, fast, (cudaStream_t)stream));
 }
 
 GDN_API int gdn_h_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, void *stream)

@@ -31,7 +31,7 @@ struct DecodeParams {
 };
 
 struct PrefillParams {
-    float *state;
+    void *state;            // float* or __half*
     int64_t pitch;
     const float *q, *k, *v, *alpha, *beta;
     float *o;
@@ -66,7 +66,7 @@ struct ConvNormParams {
 // return the launch status.
 cudaError_t launch_decode(const DecodeParams &p, bool f16_state, bool norm, bool fast, cudaStream_t s);
 cudaError_t launch_decode_chunk2(const DecodeParams &p, bool f16_state, bool fast, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillParams &p, bool fast, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams &p, bool f16_state, bool fast, cudaStream_t s);
 cudaError_t launch_conv_norm(const ConvNormParams &p, bool f16_state, bool fast, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, bool vec, cudaStream_t s);
 cudaError_t launch_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, bool vec, cudaStream_t s);

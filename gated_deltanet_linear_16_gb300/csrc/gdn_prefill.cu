@@ -27,6 +27,8 @@
 //    an SM holds 11-12 such warps, and one-warp CTAs let the block scheduler
 //    spread the B*NV*D/32 warps evenly over the SMs (a 4-warp CTA per head
 //    would leave some SMs with 3 heads and others with 2);
+//  * an fp16 state is widened once when loaded and rounded to fp16 (nearest
+//    even) once when stored: across the tokens it is carried in fp32;
 //  * per-token inputs stream through a two-stage cp.async ring in shared
 //    memory (8 tokens per stage), so the next chunk's loads overlap this
 //    chunk's arithmetic.  cp.async waits are hardware group waits (no spin
@@ -117,9 +119,23 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
     return *reinterpret_cast<float2 *>(&rd);
 }
 
+// Four consecutive state elements <-> fp32 (fp16: one 8-byte access, rounded to
+// nearest even on the store).
+__device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 load4(const __half *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = Vec16<__half>::h2f(u.x), b = Vec16<__half>::h2f(u.y);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void store4(__half *p, float4 v) {
+    *reinterpret_cast<uint2 *>(p) = make_uint2(Vec16<__half>::f2h(v.x, v.y), Vec16<__half>::f2h(v.z, v.w));
+}
+
 // Smallest scale kept deferred before it is folded back into the stored row.
 constexpr float kMinScale = 0x1p-32f;
 
+template <typename TS>
 __global__ void __launch_bounds__(kRows, 12)
 prefill_d128(const PrefillParams p)
 {
@@ -144,13 +160,13 @@ prefill_d128(const PrefillParams p)
     // Two rows x 64 columns per thread: columns 4c..4c+3 for c = 2 jj + half, jj = 0..15, so a
     // warp-wide 16-byte shared load serves both rows of a thread and touches two distinct
     // 16-byte chunks in different banks.  Rows are held as S = gam * R (deferred decay).
-    float *row = p.state + seq * p.pitch + (int64_t)h * kD * kD + (int64_t)a0 * kD;
+    TS *row = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD + (int64_t)a0 * kD;
     float2 R[2][kD / 4];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
 #pragma unroll
         for (int jj = 0; jj < kD / 8; ++jj) {
-            const float4 t = *reinterpret_cast<const float4 *>(row + rr * kD + 4 * (2 * jj + half));
+            const float4 t = load4(row + rr * kD + 4 * (2 * jj + half));
             R[rr][2 * jj] = make_float2(t.x, t.y);
             R[rr][2 * jj + 1] = make_float2(t.z, t.w);
         }
@@ -246,9 +262,9 @@ prefill_d128(const PrefillParams p)
     for (int rr = 0; rr < 2; ++rr) {
 #pragma unroll
         for (int jj = 0; jj < kD / 8; ++jj)
-            *reinterpret_cast<float4 *>(row + rr * kD + 4 * (2 * jj + half)) =
-                make_float4(gam * R[rr][2 * jj].x, gam * R[rr][2 * jj].y,
-                            gam * R[rr][2 * jj + 1].x, gam * R[rr][2 * jj + 1].y);
+            store4(row + rr * kD + 4 * (2 * jj + half),
+                   make_float4(gam * R[rr][2 * jj].x, gam * R[rr][2 * jj].y,
+                               gam * R[rr][2 * jj + 1].x, gam * R[rr][2 * jj + 1].y));
     }
 }
 
@@ -258,6 +274,7 @@ prefill_d128(const PrefillParams p)
 constexpr int kGenWarps = 4;
 constexpr int kMaxD = 256;
 
+template <typename TS>
 __global__ void __launch_bounds__(kGenWarps * 32)
 prefill_generic(const PrefillParams p)
 {
@@ -270,12 +287,12 @@ prefill_generic(const PrefillParams p)
     const int T = p.seq_len;
 
     for (int a = warp; a < D; a += kGenWarps) {
-        float *row = p.state + seq * p.pitch + (int64_t)h * D * D + (int64_t)a * D;
+        TS *row = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * D * D + (int64_t)a * D;
         float s[MAXV];
 #pragma unroll
         for (int j = 0; j < MAXV; ++j) {
             const int c = lane + 32 * j;
-            s[j] = c < D ? row[c] : 0.f;
+            s[j] = c < D ? to_f32<TS>(row[c]) : 0.f;
         }
         for (int t = 0; t < T; ++t) {
             const int64_t tok = (int64_t)seq * T + t;
@@ -306,22 +323,28 @@ prefill_generic(const PrefillParams p)
 #pragma unroll
         for (int j = 0; j < MAXV; ++j) {
             const int c = lane + 32 * j;
-            if (c < D) row[c] = s[j];
+            if (c < D) row[c] = from_f32<TS>(s[j]);
         }
     }
 }
 
-}  // namespace
-
-cudaError_t launch_prefill(const PrefillParams &p, bool fast, cudaStream_t s)
+template <typename TS>
+cudaError_t launch_typed(const PrefillParams &p, bool fast, cudaStream_t s)
 {
     const int64_t heads = (int64_t)p.batch * p.nv;
     if (fast) {
-        prefill_d128<<<(unsigned)(heads * (kD / kRows)), kRows, 0, s>>>(p);
+        prefill_d128<TS><<<(unsigned)(heads * (kD / kRows)), kRows, 0, s>>>(p);
     } else {
-        prefill_generic<<<(unsigned)heads, kGenWarps * 32, 0, s>>>(p);
+        prefill_generic<TS><<<(unsigned)heads, kGenWarps * 32, 0, s>>>(p);
     }
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams &p, bool f16_state, bool fast, cudaStream_t s)
+{
+    return f16_state ? launch_typed<__half>(p, fast, s) : launch_typed<float>(p, fast, s);
 }
 
 }  // namespace gdn

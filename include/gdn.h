@@ -189,8 +189,9 @@ GDN_API int gdn_decode_chunk2(void *state, int state_dtype, int64_t state_pitch,
  *   Defined by: ssm_gdn_a.rs, launcher `gdn_prefill_regresident`
  *   (token-sequential prefill with the state in registers); the step is
  *   gdn.rs `gdn_step`.
- *   state        as gdn_decode; only GDN_STATE_F32 (GDN_ERR_UNSUPPORTED
- *                otherwise).
+ *   state        as gdn_decode.  An fp16 state is widened to fp32 once when
+ *                loaded, carried in fp32 across the tokens and rounded to
+ *                fp16 (nearest even) once when stored.
  *   q, k         [batch * seq_len] rows of NK*D, row b*seq_len + t.
  *   v            [batch * seq_len] rows of NV*D.
  *   alpha, beta  [batch * seq_len] rows of NV.

@@ -188,19 +188,20 @@ def check_decode(res, f16, norm):
 
 
 def run_prefill_case(B, NK, NV, D, T, *, seed=0, init="zero", pad=(0, 0, 0, 0), pitch_pad=0, misalign=0,
-                     splits=None, alpha=None, beta=None):
+                     splits=None, alpha=None, beta=None, f16=False):
     """Prefill of T tokens on the GPU (one call, or per-sequence calls over `splits`)
     and in the oracle; returns error metrics."""
+    sdt = np.float16 if f16 else np.float32
     if init == "zero":
-        S0 = np.zeros((B, NV, D, D), np.float32)
+        S0 = np.zeros((B, NV, D, D), sdt)
     else:
-        S0 = gs.state_heads(seed, range(B), range(NV), D)
+        S0 = gs.state_heads(seed, range(B), range(NV), D, dtype=sdt)
     x = gs.prefill_inputs(seed, B, T, NK, NV, D)
     if alpha is not None:          # host-side override of the drawn gates (array or scalar)
         x["alpha"][...] = alpha
     if beta is not None:
         x["beta"][...] = beta
-    pool = state_pool(B, NV, D, False, pitch_pad, misalign)
+    pool = state_pool(B, NV, D, f16, pitch_pad, misalign)
     pool.write(S0.reshape(B, -1))
     R = B * T
     qb = Rows(R, NK * D, NK * D + pad[0], misalign=misalign)
@@ -211,17 +212,18 @@ def run_prefill_case(B, NK, NV, D, T, *, seed=0, init="zero", pad=(0, 0, 0, 0), 
     ob = Rows(R, NV * D, NV * D + pad[3])
     qb.write(x["q"].reshape(R, -1)); kb.write(x["k"].reshape(R, -1)); vb.write(x["v"].reshape(R, -1))
     ab.write(x["alpha"].reshape(R, -1)); bb.write(x["beta"].reshape(R, -1))
-    common = dict(nk=NK, nv=NV, d=D, state_pitch=pool.stride, state_dtype=gdn.GDN_STATE_F32,
+    common = dict(nk=NK, nv=NV, d=D, state_pitch=pool.stride,
+                  state_dtype=gdn.GDN_STATE_F16 if f16 else gdn.GDN_STATE_F32,
                   qk_stride=qb.stride, v_stride=vb.stride, gb_stride=ab.stride, o_stride=ob.stride)
     if splits is None:
         gdn.gdn_prefill_seq(pool.ptr, qb.ptr, kb.ptr, vb.ptr, ab.ptr, bb.ptr, ob.ptr, batch=B, seq_len=T, **common)
     else:
-        e32, e16 = 4, 2
+        e32, es = 4, (2 if f16 else 4)
         for b in range(B):
             t0 = 0
             for n in splits:
                 row = b * T + t0
-                gdn.gdn_prefill_seq(pool.ptr + b * pool.stride * e32,
+                gdn.gdn_prefill_seq(pool.ptr + b * pool.stride * es,
                                     qb.ptr + row * qb.stride * e32, kb.ptr + row * kb.stride * e32,
                                     vb.ptr + row * vb.stride * e32, ab.ptr + row * ab.stride * e32,
                                     bb.ptr + row * bb.stride * e32, ob.ptr + row * ob.stride * e32,
@@ -232,10 +234,12 @@ def run_prefill_case(B, NK, NV, D, T, *, seed=0, init="zero", pad=(0, 0, 0, 0), 
     o_ref = oracle.prefill(ref, x["q"], x["k"], x["v"], x["alpha"], x["beta"], NK)
     torch.cuda.synchronize()
     o_gpu = ob.read().astype(np.float64).reshape(B, T, NV * D)
-    S_gpu = to_f64_state(pool, B, NV, D, False)
+    S_gpu = to_f64_state(pool, B, NV, D, f16)
     return {
         "state_max_rel": max_rel_err(S_gpu, ref),
+        "state_rel_l2": rel_l2(S_gpu, ref),
         "o_max_rel": max_rel_err(o_gpu, o_ref),
+        "o_rel_l2": rel_l2(o_gpu, o_ref),
         "intact": all(b.intact() for b in (pool, qb, kb, vb, ab, bb, ob)),
         "S_gpu": S_gpu, "S_ref": ref,
     }

@@ -176,7 +176,7 @@ def test_decode_norm_rejects(lib, kw, want):
 
 
 @pytest.mark.parametrize("kw,want", [
-    (dict(dt=1), UNSUP), (dict(T=-1), ARG), (dict(o=None), ARG),
+    (dict(dt=2), UNSUP), (dict(T=-1), ARG), (dict(o=None), ARG), (dict(state=A + 1, dt=1), ALIGN),
     (dict(os=10), ARG), (dict(o=A + 100), ALIAS),
 ])
 def test_prefill_rejects(lib, kw, want):

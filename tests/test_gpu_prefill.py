@@ -70,6 +70,37 @@ def test_many_warps():
     check(run_prefill_case(4, 16, 80, 128, 5, seed=15, init="normal"))
 
 
+def check_f16(r, split=False):
+    """fp16 state: carried in fp32 across the tokens of a call and rounded once when stored, so the
+    final state is within a binary16 rounding or two of the reference (fp16-state bar, relative L2),
+    and o of a single call, computed from the fp32-carried state, meets the fp32 bar.  After a split
+    the second call starts from the rounded state, so its o is held to the fp16-state bar."""
+    assert r["intact"], "guard band or padding overwritten"
+    assert r["state_rel_l2"] <= TOL_REL_L2, r["state_rel_l2"]
+    assert r["state_max_rel"] <= 2.0 ** -10, r["state_max_rel"]
+    if split:
+        assert r["o_rel_l2"] <= TOL_REL_L2, r["o_rel_l2"]
+    else:
+        assert r["o_max_rel"] <= TOL_F32, r["o_max_rel"]
+
+
+@pytest.mark.parametrize("T", [1, 9, 40])
+def test_f16_state_d128(T):
+    check_f16(run_prefill_case(2, 2, 3, 128, T, seed=90 + T, init="normal", f16=True, pitch_pad=4096))
+
+
+def test_f16_state_split_calls():
+    """Split calls round the state to fp16 at each call boundary; with one split the result stays
+    within the fp16-state bar."""
+    check_f16(run_prefill_case(2, 2, 3, 128, 24, seed=95, init="normal", f16=True, splits=(10, 14)), split=True)
+
+
+@pytest.mark.parametrize("D,misalign", [(64, 0), (128, 1), (5, 0)])
+def test_f16_state_general_kernel(D, misalign):
+    check_f16(run_prefill_case(2, 2, 3, D, 13, seed=97 + D, init="normal", f16=True, misalign=misalign,
+                               pad=(1 if misalign else 0, 0, 0, 0)))
+
+
 def test_empty_sequence_is_a_no_op():
     st = state_pool(1, 2, 128, False)
     before = st.raw.clone()
