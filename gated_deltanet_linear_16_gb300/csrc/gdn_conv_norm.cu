@@ -18,11 +18,12 @@
 // unchanged -- and the NV/NK CTAs of a key head form a thread-block cluster:
 //  * every CTA issues its state loads first, then updates the ring rows of its
 //    own value head's v channels and computes v (one writer per ring row);
-//  * cluster rank 0 also computes the key head's q and k (conv, silu, L2) into
-//    its shared memory and updates their ring rows;
-//  * after one cluster barrier every CTA reads q and k from rank 0's shared
-//    memory (distributed shared memory), a second barrier lets rank 0 retire,
-//    and the step + norm run as in the decode kernel.
+//  * every CTA also computes the key head's q and k (conv, silu, L2: 256
+//    channels) from the ring as it was, without writing it, so no CTA waits
+//    for another before its step;
+//  * the cluster barrier is split: each CTA arrives once it has read the ring,
+//    runs its step and norm, then waits; only then does cluster rank 0 write
+//    the key head's q/k ring rows (kept in shared memory meanwhile).
 // Cluster barriers are hardware barriers (no spin loop on a flag).
 #include "gdn_internal.cuh"
 
@@ -38,24 +39,6 @@ __device__ __forceinline__ unsigned cluster_rank() {
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Address of `p` (this CTA's shared memory) in the shared memory of cluster rank `rank`.
-__device__ __forceinline__ unsigned map_to_rank(const void *p, unsigned rank) {
-    const unsigned local = (unsigned)__cvta_generic_to_shared(p);
-    unsigned remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-    return remote;
-}
-__device__ __forceinline__ float4 ld_cluster4(unsigned addr) {
-    float4 r;
-    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr) : "memory");
-    return r;
-}
-
 // One channel through the conv ring: shift up by one, append x, reduce with the
 // taps, silu.  The caller is the only thread touching this channel.
 __device__ __forceinline__ float conv_silu_channel(float *ring, const float *x, const float *w,
@@ -70,6 +53,31 @@ __device__ __forceinline__ float conv_silu_channel(float *ring, const float *x, 
     ring[(int64_t)(taps - 1) * C + c] = xv;
     acc = fmaf(xv, __ldg(w + (int64_t)(taps - 1) * C + c), acc);
     return silu(acc);
+}
+
+// The same channel computed from the ring without writing it; the shifted
+// entries (the ring's new contents) go to `keep` (taps entries, stride kstride)
+// for the owner to store later.
+__device__ __forceinline__ float conv_silu_channel_ro(const float *ring, const float *x, const float *w,
+                                                      int64_t c, int64_t C, int taps,
+                                                      float *keep, int kstride) {
+    float acc = 0.f;
+    for (int t = 0; t + 1 < taps; ++t) {
+        const float val = ring[(int64_t)(t + 1) * C + c];
+        keep[t * kstride] = val;
+        acc = fmaf(val, __ldg(w + (int64_t)t * C + c), acc);
+    }
+    const float xv = __ldg(x + c);
+    keep[(taps - 1) * kstride] = xv;
+    acc = fmaf(xv, __ldg(w + (int64_t)(taps - 1) * C + c), acc);
+    return silu(acc);
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void gates(const ConvNormParams &p, int seq, int h, float &alpha, float &beta) {
@@ -96,6 +104,7 @@ conv_norm_d128(const ConvNormParams p)
     __shared__ float v_s[kD];
     __shared__ float red_q[4], red_k[4], red[kWarps];
     __shared__ float gate_s[2];
+    __shared__ float ring_new[2][8][kD];                 // rank 0: the key head's new q/k ring rows
 
     const unsigned rank = cluster_rank();               // which value head of the key head
     const int cl = blockIdx.x / p.repeat;               // (sequence, key head)
@@ -116,15 +125,17 @@ conv_norm_d128(const ConvNormParams p)
 #pragma unroll
     for (int i = 0; i < LPB; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
 
-    // 2. producers: v of this head (threads 0..127); q and k of the key head on rank 0 (128..255)
+    // 2. producers: v of this head (threads 0..127, ring rows written now: their only writer);
+    //    q and k of the key head (threads 128..255) from the ring as it was, not written yet
     float *ring = p.ring + seq * p.ring_pitch;
     const float *x = p.x + seq * p.x_stride;
     if (tid < kD) {
         v_s[tid] = conv_silu_channel(ring, x, p.w, 2 * (int64_t)p.nk * kD + (int64_t)h * kD + tid, C, p.taps);
-    } else if (rank == 0) {
+    } else {
         const int i = tid - kD;
-        const float qv = conv_silu_channel(ring, x, p.w, (int64_t)kh * kD + i, C, p.taps);
-        const float kv = conv_silu_channel(ring, x, p.w, (int64_t)(p.nk + kh) * kD + i, C, p.taps);
+        const float qv = conv_silu_channel_ro(ring, x, p.w, (int64_t)kh * kD + i, C, p.taps, &ring_new[0][0][i], kD);
+        const float kv = conv_silu_channel_ro(ring, x, p.w, (int64_t)(p.nk + kh) * kD + i, C, p.taps,
+                                              &ring_new[1][0][i], kD);
         const float sq = group_sum<32>(qv * qv), sk = group_sum<32>(kv * kv);
         if (lane == 0) { red_q[warp - 4] = sq; red_k[warp - 4] = sk; }
         asm volatile("bar.sync 1, 128;" ::: "memory");  // the four producer warps
@@ -135,20 +146,16 @@ conv_norm_d128(const ConvNormParams p)
     }
     if (tid == 0) gates(p, seq, h, gate_s[0], gate_s[1]);
     __syncthreads();
-    cluster_sync_all();                                  // rank 0's q, k visible cluster-wide
+    cluster_arrive();                                    // this CTA is done reading the q/k ring rows
 
-    // 3. this lane's columns of q and k from rank 0's shared memory
     float kx[EPV], qx[EPV];
-    {
-        const unsigned ka = map_to_rank(k_s + col, 0), qa = map_to_rank(q_s + col, 0);
 #pragma unroll
-        for (int j = 0; j < EPV; j += 4) {
-            const float4 a = ld_cluster4(ka + 4 * j), b = ld_cluster4(qa + 4 * j);
-            kx[j] = a.x; kx[j + 1] = a.y; kx[j + 2] = a.z; kx[j + 3] = a.w;
-            qx[j] = b.x; qx[j + 1] = b.y; qx[j + 2] = b.z; qx[j + 3] = b.w;
-        }
+    for (int j = 0; j < EPV; j += 4) {
+        const float4 a = *reinterpret_cast<const float4 *>(k_s + col + j);
+        const float4 b = *reinterpret_cast<const float4 *>(q_s + col + j);
+        kx[j] = a.x; kx[j + 1] = a.y; kx[j + 2] = a.z; kx[j + 3] = a.w;
+        qx[j] = b.x; qx[j + 1] = b.y; qx[j + 2] = b.z; qx[j + 3] = b.w;
     }
-    cluster_sync_all();                                  // every CTA has read rank 0's q, k
 
     const bool row_lane = lane < kRowsPerWarp;
     const float v_l = row_lane ? v_s[row0 + lane] : 0.f;
@@ -211,6 +218,16 @@ conv_norm_d128(const ConvNormParams p)
     if (row_lane) {
         const float y = gn_l * o_keep * rstd * silu(z_l);
         p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
+    }
+
+    // 6. every CTA of the cluster has read the old q/k ring rows: rank 0 writes the new ones
+    cluster_wait();
+    if (rank == 0 && tid >= kD) {
+        const int i = tid - kD;
+        for (int t = 0; t < p.taps; ++t) {
+            ring[(int64_t)t * C + (int64_t)kh * kD + i] = ring_new[0][t][i];
+            ring[(int64_t)t * C + (int64_t)(p.nk + kh) * kD + i] = ring_new[1][t][i];
+        }
     }
 }
 
