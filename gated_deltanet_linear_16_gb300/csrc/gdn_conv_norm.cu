@@ -34,11 +34,6 @@ constexpr int kD = 128;
 constexpr int kWarps = 8;
 constexpr int kRowsPerWarp = kD / kWarps;   // 16
 
-__device__ __forceinline__ unsigned cluster_rank() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
 // One channel through the conv ring: shift up by one, append x, reduce with the
 // taps, silu.  The caller is the only thread touching this channel.
 __device__ __forceinline__ float conv_silu_channel(float *ring, const float *x, const float *w,
@@ -73,12 +68,6 @@ __device__ __forceinline__ float conv_silu_channel_ro(const float *ring, const f
     return silu(acc);
 }
 
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 __device__ __forceinline__ void gates(const ConvNormParams &p, int seq, int h, float &alpha, float &beta) {
     const float br = __ldg(p.br + seq * p.gate_stride + h);

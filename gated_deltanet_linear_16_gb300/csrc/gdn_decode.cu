@@ -42,14 +42,17 @@ constexpr int kD = 128;
 // Chosen by measurement on GB300 (48-layer fp32 workload, 256-slot fp16 pool):
 // fp32 8 warps x 16 rows, 4 batches of 4 loads, 3 CTAs per SM; fp16 8 warps x
 // 16 rows, 2 batches of 4 loads, 4 CTAs per SM.
+// kSplit > 1 spreads a head over a cluster of kSplit CTAs (shorter CTAs, a
+// shorter drain at the end of a launch); the fused norm then adds the CTAs'
+// partial sums of squares over distributed shared memory in rank order.
 template <typename TS> struct FastShape {
-    static constexpr int kWarps = 8, kBatches = 4, kMinBlocks = 3;
+    static constexpr int kWarps = 8, kBatches = 4, kMinBlocks = 3, kSplit = 1;
 };
 template <> struct FastShape<__half> {
-    static constexpr int kWarps = 8, kBatches = 2, kMinBlocks = 4;
+    static constexpr int kWarps = 8, kBatches = 2, kMinBlocks = 4, kSplit = 1;
 };
 
-template <typename TS, bool NORM, int WARPS, int NB, int MINB>
+template <typename TS, bool NORM, int WARPS, int NB, int MINB, int SPLIT>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 decode_d128(const DecodeParams p)
 {
@@ -57,12 +60,13 @@ decode_d128(const DecodeParams p)
     constexpr int EPV = V::N;                  // state elements per 16-byte vector
     constexpr int LPR = kD / EPV;              // lanes per state row: 32 fp32, 16 fp16
     constexpr int RPL = 32 / LPR;              // rows per warp-wide load: 1 fp32, 2 fp16
-    constexpr int RPW = kD / WARPS;            // rows per warp
+    constexpr int RPW = kD / (WARPS * SPLIT);  // rows per warp
     constexpr int NLD = RPW / RPL;             // 16-byte state loads per lane
     constexpr int LPB = NLD / NB;              // loads per batch
-    static_assert(RPW <= 32 && NLD % NB == 0, "shape");
+    static_assert(RPW <= 32 && NLD % NB == 0 && NLD >= NB, "shape");
 
-    const int unit = blockIdx.x;               // (sequence, value head)
+    const int unit = blockIdx.x / SPLIT;       // (sequence, value head)
+    const int part = blockIdx.x - unit * SPLIT;  // which rows of the head (cluster rank)
     const int seq = unit / p.nv;
     const int h = unit - seq * p.nv;
     const int g = h % p.nk;                    // tiled key-head pairing
@@ -70,7 +74,7 @@ decode_d128(const DecodeParams p)
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR;                // which row of a warp-wide load
     const int col = (lane % LPR) * EPV;        // first column this lane owns
-    const int row0 = warp * RPW;
+    const int row0 = part * (kD / SPLIT) + warp * RPW;
 
     TS *S = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD;
     TS *rowp = S + (int64_t)(row0 + sub) * kD + col;
@@ -145,19 +149,30 @@ decode_d128(const DecodeParams p)
     if constexpr (!NORM) {
         if (row_lane) p.o[seq * p.o_stride + (int64_t)h * kD + row0 + lane] = o_keep;
     } else {
-        // 4. gated RMS norm over the head's 128 outputs, in this CTA
+        // 4. gated RMS norm over the head's 128 outputs, in this CTA (and its cluster peers)
         __shared__ float red[WARPS];
+        __shared__ float part_sum;
         const float ss = group_sum<32>(o_keep * o_keep);   // lanes >= RPW hold 0
         if (lane == 0) red[warp] = ss;
         __syncthreads();
         float tot = 0.f;
 #pragma unroll
         for (int i = 0; i < WARPS; ++i) tot += red[i];
+        if constexpr (SPLIT > 1) {
+            if (threadIdx.x == 0) part_sum = tot;
+            cluster_arrive();
+            cluster_wait();                    // every CTA's partial sum is written
+            tot = 0.f;
+#pragma unroll
+            for (int r = 0; r < SPLIT; ++r) tot += ld_cluster_f32(&part_sum, r);
+            cluster_arrive();                  // done reading the peers' shared memory
+        }
         const float rstd = rsqrtf(tot * (1.0f / kD) + p.eps);
         if (row_lane) {
             const float y = gn_l * o_keep * rstd * silu(z_l);
             p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
         }
+        if constexpr (SPLIT > 1) cluster_wait();   // no CTA leaves while a peer may read it
     }
 }
 
@@ -252,7 +267,25 @@ cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
 {
     const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
     using F = FastShape<TS>;
-    if (fast) decode_d128<TS, NORM, F::kWarps, F::kBatches, F::kMinBlocks><<<grid, F::kWarps * 32, 0, s>>>(p);
+    if (fast) {
+        auto kern = decode_d128<TS, NORM, F::kWarps, F::kBatches, F::kMinBlocks, F::kSplit>;
+        if (F::kSplit == 1) {
+            kern<<<grid, F::kWarps * 32, 0, s>>>(p);
+        } else {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(grid * F::kSplit, 1, 1);
+            cfg.blockDim = dim3(F::kWarps * 32, 1, 1);
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = F::kSplit;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelEx(&cfg, kern, p);
+        }
+    }
     else decode_generic<TS, NORM><<<grid, kGenWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }

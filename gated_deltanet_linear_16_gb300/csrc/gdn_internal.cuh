@@ -105,6 +105,28 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
     return *reinterpret_cast<uint16_t *>(&b);
 }
 
+// Thread-block cluster helpers (hardware barriers; distributed shared memory).
+__device__ __forceinline__ unsigned cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A float in the shared memory of cluster rank `rank`, at the offset of `p` in this CTA's.
+__device__ __forceinline__ float ld_cluster_f32(const float *p, unsigned rank) {
+    const unsigned local = (unsigned)__cvta_generic_to_shared(p);
+    unsigned remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 // A 16-byte vector of state elements, widened to / narrowed from fp32.
 template <typename TS> struct Vec16;
 

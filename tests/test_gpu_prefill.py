@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import gated_deltanet_linear_16_gb300 as gdn
-from tests.gpu_helpers import TOL_F32, Rows, run_prefill_case, state_pool
+from tests.gpu_helpers import TOL_F32, TOL_REL_L2, Rows, run_prefill_case, state_pool
 
 pytestmark = pytest.mark.gpu
 
