@@ -459,17 +459,18 @@ def row_conv_norm(torch, gdn, dev, stream, pk, taps=4):
     ring = t["ring"].reshape(B, taps * C).contiguous()
     gn = torch.from_numpy(gs.norm_weight(SEED, D)).to(dev)
     out = torch.empty((B, NV * D), dtype=torch.int16, device=dev)
+    ws = torch.zeros(B * NK, dtype=torch.int32, device=dev)
     s = time_fn(torch, stream, lambda: gdn.gdn_decode_conv_norm(
-        S, ring, t["x"], t["conv_w"], t["br"], t["ar"], t["dt"], t["rate"], t["z"], gn, out,
+        S, ring, t["x"], t["conv_w"], t["br"], t["ar"], t["dt"], t["rate"], t["z"], gn, out, ws,
         batch=B, nk=NK, nv=NV, d=D, taps=taps, stream=stream.cuda_stream), 50)
     # state read + write; ring: taps-1 entries read, all taps written; x, z read; w, dt, rate, gn once;
     # gate logits read; bf16 out written
     by = (B * NV * D * D * 4 * 2 + B * ((taps - 1) + taps + 1) * C * 4 + taps * C * 4
           + B * NV * D * 4 + B * NV * 2 * 4 + 2 * NV * 4 + D * 4 + B * NV * D * 2)
-    del S, ring, gn, out, t
+    del S, ring, gn, out, t, ws
     torch.cuda.empty_cache()
     return {"conv_norm_from_projections": {
-        "config": "B=32 NK=16 NV=48 D=128 fp32, 4-tap conv, clusters of 3 CTAs", "us_per_launch": s * 1e6,
+        "config": "B=32 NK=16 NV=48 D=128 fp32, 4-tap conv", "us_per_launch": s * 1e6,
         "token_heads_per_s": B * NV / s, "achieved_gbs": by / s / 1e9,
         "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}}
 

@@ -58,7 +58,7 @@ def _declare(lib):
     lib.gdn_decode.argtypes = [P, i32, i64, P, P, P, P, P, P, i32, i32, i32, i32, i64, i64, i64, i64, P]
     lib.gdn_decode_norm.argtypes = [P, i32, i64, P, P, P, P, P, P, P, f32, P, i32, i32, i32, i32,
                                     i64, i64, i64, i64, i64, P]
-    lib.gdn_decode_conv_norm.argtypes = [P, i32, i64, P, i64, i32, P, P, P, P, P, P, P, P, f32, f32, P,
+    lib.gdn_decode_conv_norm.argtypes = [P, i32, i64, P, i64, i32, P, P, P, P, P, P, P, P, f32, f32, P, P,
                                          i32, i32, i32, i32, i64, i64, i64, i64, P]
     lib.gdn_decode_chunk2.argtypes = [P, i32, i64, P, i64, P, P, P, P, P, P, i32, i32, i32, i32,
                                       i64, i64, i64, i64, P]
@@ -168,11 +168,13 @@ def gdn_decode_norm(state, q, k, v, alpha, beta, z, gn, out, *, batch, nk, nv, d
     _check("gdn_decode_norm", st)
 
 
-def gdn_decode_conv_norm(state, conv_state, x, conv_w, br, ar, dt, rate, z, gn, out, *, batch, nk, nv, d,
-                         taps, eps=1e-6, l2_eps=1e-6, state_pitch=None, conv_pitch=None, state_dtype=None,
-                         x_stride=None, gate_stride=None, z_stride=None, out_stride=None, stream=None):
+def gdn_decode_conv_norm(state, conv_state, x, conv_w, br, ar, dt, rate, z, gn, out, workspace, *, batch, nk,
+                         nv, d, taps, eps=1e-6, l2_eps=1e-6, state_pitch=None, conv_pitch=None,
+                         state_dtype=None, x_stride=None, gate_stride=None, z_stride=None, out_stride=None,
+                         stream=None):
     """One token from the projections (conv ring + silu, q/k L2 norm, gates from logits, the step,
-    the gated norm) in one launch; bf16 out.  See include/gdn.h for the layouts."""
+    the gated norm) in one launch; bf16 out.  workspace: batch*nk int32, zero before the first call
+    and left zero.  See include/gdn.h for the layouts."""
     lib = load()
     sd = _state_dtype(state, state_dtype)
     C = (2 * nk + nv) * d
@@ -180,7 +182,7 @@ def gdn_decode_conv_norm(state, conv_state, x, conv_w, br, ar, dt, rate, z, gn, 
         _ptr(state), sd, state_pitch if state_pitch is not None else nv * d * d,
         _ptr(conv_state), conv_pitch if conv_pitch is not None else taps * C, taps,
         _ptr(x), _ptr(conv_w), _ptr(br), _ptr(ar), _ptr(dt), _ptr(rate), _ptr(z), _ptr(gn),
-        float(l2_eps), float(eps), _ptr(out), batch, nk, nv, d,
+        float(l2_eps), float(eps), _ptr(out), _ptr(workspace), batch, nk, nv, d,
         x_stride if x_stride is not None else C,
         gate_stride if gate_stride is not None else nv,
         z_stride if z_stride is not None else nv * d,

@@ -188,7 +188,7 @@ GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pit
                                  const float *x, const float *conv_w,
                                  const float *br, const float *ar, const float *dt, const float *rate,
                                  const float *z, const float *gn, float l2_eps, float eps,
-                                 uint16_t *out,
+                                 uint16_t *out, int32_t *workspace,
                                  int batch, int nk, int nv, int d,
                                  int64_t x_stride, int64_t gate_stride, int64_t z_stride,
                                  int64_t out_stride, void *stream)
@@ -208,6 +208,7 @@ GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pit
         {state, B, (int64_t)nv * d * d, state_pitch, selem},
         {conv_state, B, taps * C, conv_pitch, 4},
         {out, B, hv, out_stride, 2},
+        {workspace, 1, B * nk, B * nk, 4},
         {x, B, C, x_stride, 4},
         {conv_w, 1, taps * C, taps * C, 4},
         {br, B, nv, gate_stride, 4},
@@ -217,12 +218,12 @@ GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pit
         {z, B, hv, z_stride, 4},
         {gn, 1, d, d, 4},
     };
-    const int n_ops = 11;
+    const int n_ops = 12;
     if (batch == 0) {
         for (int i = 0; i < n_ops; ++i) if (ops[i].p == nullptr) return GDN_ERR_ARG;
         return GDN_OK;
     }
-    st = check_operands(ops, n_ops, 3);
+    st = check_operands(ops, n_ops, 4);
     if (st != GDN_OK) return st;
 
     ConvNormParams p{};
@@ -231,10 +232,11 @@ GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pit
     p.x = x; p.x_stride = x_stride; p.w = conv_w;
     p.br = br; p.ar = ar; p.gate_stride = gate_stride; p.dt = dt; p.rate = rate;
     p.z = z; p.gn = gn; p.out = out; p.z_stride = z_stride; p.out_stride = out_stride;
+    p.counters = workspace;
     p.batch = batch; p.nk = nk; p.nv = nv; p.d = d; p.taps = taps; p.repeat = repeat;
     p.l2_eps = l2_eps; p.eps = eps; p.inv_sqrt_d = inv_sqrt(d);
-    // D == 128 cluster kernel: 16-byte state rows, at most 8 value heads per key head (cluster size)
-    const bool fast = d == 128 && repeat <= 8 && vec16(state) && (state_pitch * selem) % 16 == 0;
+    // D == 128 kernel: 16-byte state rows
+    const bool fast = d == 128 && vec16(state) && (state_pitch * selem) % 16 == 0;
     return cuda_status(launch_conv_norm(p, state_dtype == GDN_STATE_F16, fast, (cudaStream_t)stream));
 }
 

@@ -13,18 +13,20 @@
 // `gdn_step` and `gdn_gate_norm`.
 //
 // GB300 design.  The page's launcher gives one block to a key head and its
-// NV/NK value heads.  Here the value heads keep one CTA each -- the decode
+// NV/NK value heads.  Here every value head keeps one CTA -- the decode
 // kernel's shape (8 warps x 16 rows), so the 64 KB-per-head state stream is
-// unchanged -- and the NV/NK CTAs of a key head form a thread-block cluster:
+// unchanged and no CTA waits for another:
 //  * every CTA issues its state loads first, then updates the ring rows of its
 //    own value head's v channels and computes v (one writer per ring row);
 //  * every CTA also computes the key head's q and k (conv, silu, L2: 256
-//    channels) from the ring as it was, without writing it, so no CTA waits
-//    for another before its step;
-//  * the cluster barrier is split: each CTA arrives once it has read the ring,
-//    runs its step and norm, then waits; only then does cluster rank 0 write
-//    the key head's q/k ring rows (kept in shared memory meanwhile).
-// Cluster barriers are hardware barriers (no spin loop on a flag).
+//    channels) from the ring as it was, without writing it, and keeps the
+//    shifted rows in shared memory;
+//  * after reading, a CTA counts itself in a per-(sequence, key head) counter
+//    (fence + atomic add); the CTA that completes the count is the last reader
+//    of those ring rows, so it writes them and resets the counter to zero.
+// No barrier spans CTAs and nothing spins.  (Thread-block clusters, tried
+// first for this exchange, cost ~30 % on GB300: co-scheduling the cluster's
+// CTAs left SM slots idle.)
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -93,10 +95,11 @@ conv_norm_d128(const ConvNormParams p)
     __shared__ float v_s[kD];
     __shared__ float red_q[4], red_k[4], red[kWarps];
     __shared__ float gate_s[2];
-    __shared__ float ring_new[2][8][kD];                 // rank 0: the key head's new q/k ring rows
+    __shared__ float ring_new[2][8][kD];                 // the key head's new q/k ring rows
+    __shared__ int last_reader;
 
-    const unsigned rank = cluster_rank();               // which value head of the key head
     const int cl = blockIdx.x / p.repeat;               // (sequence, key head)
+    const int rank = blockIdx.x - cl * p.repeat;        // which value head of the key head
     const int seq = cl / p.nk;
     const int kh = cl - seq * p.nk;
     const int h = kh + (int)rank * p.nk;                // tiled pairing: h mod NK == kh
@@ -134,8 +137,13 @@ conv_norm_d128(const ConvNormParams p)
         k_s[i] = kv / sqrtf(tk + p.l2_eps);
     }
     if (tid == 0) gates(p, seq, h, gate_s[0], gate_s[1]);
-    __syncthreads();
-    cluster_arrive();                                    // this CTA is done reading the q/k ring rows
+    __syncthreads();                                     // this CTA is done reading the q/k ring rows
+    if (tid == 0) {
+        __threadfence();                                 // the reads above come before the count
+        const int seen = atomicAdd(p.counters + cl, 1);
+        last_reader = seen == p.repeat - 1;
+        if (last_reader) __threadfence();                // every other reader's count came first
+    }
 
     float kx[EPV], qx[EPV];
 #pragma unroll
@@ -209,14 +217,16 @@ conv_norm_d128(const ConvNormParams p)
         p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
     }
 
-    // 6. every CTA of the cluster has read the old q/k ring rows: rank 0 writes the new ones
-    cluster_wait();
-    if (rank == 0 && tid >= kD) {
-        const int i = tid - kD;
-        for (int t = 0; t < p.taps; ++t) {
-            ring[(int64_t)t * C + (int64_t)kh * kD + i] = ring_new[0][t][i];
-            ring[(int64_t)t * C + (int64_t)(p.nk + kh) * kD + i] = ring_new[1][t][i];
+    // 6. the last reader of the key head's q/k ring rows writes their new contents
+    if (last_reader) {                                   // read after the __syncthreads of step 5
+        if (tid >= kD) {
+            const int i = tid - kD;
+            for (int t = 0; t < p.taps; ++t) {
+                ring[(int64_t)t * C + (int64_t)kh * kD + i] = ring_new[0][t][i];
+                ring[(int64_t)t * C + (int64_t)(p.nk + kh) * kD + i] = ring_new[1][t][i];
+            }
         }
+        if (tid == 0) p.counters[cl] = 0;               // ready for the next call
     }
 }
 
@@ -332,19 +342,9 @@ cudaError_t launch_typed(const ConvNormParams &p, bool fast, cudaStream_t s)
 {
     if (fast) {
         using F = ConvShape<TS>;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)((int64_t)p.batch * p.nv), 1, 1);
-        cfg.blockDim = dim3(kWarps * 32, 1, 1);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)p.repeat;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, conv_norm_d128<TS, F::kBatches, F::kMinBlocks>, p);
+        conv_norm_d128<TS, F::kBatches, F::kMinBlocks>
+            <<<(unsigned)((int64_t)p.batch * p.nv), kWarps * 32, 0, s>>>(p);
+        return cudaGetLastError();
     }
     const size_t smem = sizeof(float) * ((size_t)(3 + p.repeat) * p.d + 2 * (size_t)p.repeat);
     conv_norm_generic<TS><<<(unsigned)((int64_t)p.batch * p.nk), kGenWarps * 32, smem, s>>>(p);

@@ -56,6 +56,7 @@ struct ConvNormParams {
     const float *dt, *rate; // [NV]
     const float *z, *gn;
     uint16_t *out;
+    int *counters;          // [batch * NK] readers of each key head's q/k ring rows; zero between calls
     int64_t z_stride, out_stride;
     int batch, nk, nv, d, taps, repeat;   // repeat = NV / NK value heads per key head
     float l2_eps, eps, inv_sqrt_d;

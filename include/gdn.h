@@ -140,6 +140,12 @@ GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
  *   conv_w       [taps][C] fp32 conv taps.
  *   br, ar       [batch] rows of NV gate logits.  dt, rate: [NV].
  *   z, gn, eps, out as gdn_decode_norm; l2_eps >= 0 for the q/k norm.
+ *   workspace    [batch*NK] int32 counters owned by the caller: zero before
+ *                the first call (e.g. cudaMemsetAsync); every call leaves
+ *                them zero.  The value heads of a key head each read its
+ *                q/k ring rows, and the counters let the last reader write
+ *                them.  Calls that can overlap on the GPU need separate
+ *                workspaces (and separate conv states).
  *   NV must be a multiple of NK (the value heads of a key head are h = kh +
  *   r*NK, r < NV/NK).  State and output as gdn_decode_norm.
  *   Errors as gdn_decode_norm; GDN_ERR_UNSUPPORTED if NV % NK != 0.
@@ -149,7 +155,7 @@ GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pit
                                  const float *x, const float *conv_w,
                                  const float *br, const float *ar, const float *dt, const float *rate,
                                  const float *z, const float *gn, float l2_eps, float eps,
-                                 uint16_t *out,
+                                 uint16_t *out, int32_t *workspace,
                                  int batch, int nk, int nv, int d,
                                  int64_t x_stride, int64_t gate_stride, int64_t z_stride,
                                  int64_t out_stride, void *stream);

@@ -106,12 +106,12 @@ def conv_norm(lib, **kw):
     C = (2 * nk + nv) * d
     a = dict(state=A, dt=0, pitch=nv * d * d, ring=A + (9 << 30), rpitch=taps * C, taps=taps, x=A + (1 << 30),
              w=A + (2 << 30), br=A + (3 << 30), ar=A + (4 << 30), dtb=A + (5 << 30), rate=A + (5 << 30) + 4096,
-             z=A + (7 << 30), gn=A + (8 << 30), l2=1e-6, eps=1e-6, out=A + (6 << 30), batch=2, nk=nk, nv=nv, d=d,
-             xs=C, gs=nv, zs=nv * d, outs=nv * d)
+             z=A + (7 << 30), gn=A + (8 << 30), l2=1e-6, eps=1e-6, out=A + (6 << 30), ws=A + (10 << 30),
+             batch=2, nk=nk, nv=nv, d=d, xs=C, gs=nv, zs=nv * d, outs=nv * d)
     a.update(kw)
     return lib.gdn_decode_conv_norm(a["state"], a["dt"], a["pitch"], a["ring"], a["rpitch"], a["taps"], a["x"], a["w"],
                                     a["br"], a["ar"], a["dtb"], a["rate"], a["z"], a["gn"], a["l2"], a["eps"],
-                                    a["out"], a["batch"], a["nk"], a["nv"], a["d"], a["xs"], a["gs"], a["zs"],
+                                    a["out"], a["ws"], a["batch"], a["nk"], a["nv"], a["d"], a["xs"], a["gs"], a["zs"],
                                     a["outs"], None)
 
 
@@ -123,6 +123,7 @@ def conv_norm(lib, **kw):
     (dict(ring=A + 8192), ALIAS),                         # conv state inside the h-state
     (dict(out=A + (9 << 30) + 64), ALIAS),                # output inside the conv state
     (dict(ring=A + (9 << 30) + 2), ALIGN),
+    (dict(ws=None), ARG), (dict(ws=A + (10 << 30) + 2), ALIGN), (dict(ws=A + (6 << 30)), ALIAS),
 ])
 def test_conv_norm_rejects(lib, kw, want):
     assert conv_norm(lib, **kw) == want
