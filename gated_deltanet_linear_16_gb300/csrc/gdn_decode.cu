@@ -18,10 +18,13 @@
 //  * every state access is a 16-byte vector: an fp32 row (512 B) is one
 //    warp-wide load, an fp16 row (256 B) half of one, so a warp touches whole
 //    128-byte lines and stores never leave partial sectors;
-//  * each lane's state loads are issued in batches, the next batch in flight
-//    while the current one is computed and written back, with 3-4 CTAs per
-//    SM: some 50-100 KB of loads outstanding per SM, enough to cover HBM
-//    latency at full bandwidth while the stores of earlier rows drain;
+//  * the whole head is staged in shared memory by cp.async (64 KB fp32,
+//    32 KB fp16): each lane issues every 16-byte load of its slice at once,
+//    in four commit groups, and computes group g while groups > g land.  The
+//    loads hold no registers while in flight, so 3 (fp32) or 4 (fp16) CTAs
+//    per SM keep 128-192 KB of reads outstanding per SM -- enough to cover
+//    HBM latency at full bandwidth while the stores of earlier rows drain.
+//    Each lane reads back only the vectors it copied itself;
 //  * k and q are read as this lane's own 16-byte columns, v/z/gn as one
 //    coalesced read per warp (a float per row) that lanes broadcast by shuffle;
 //  * the three dot products are butterfly shuffles inside the group of lanes
@@ -36,53 +39,58 @@ constexpr int kD = 128;
 
 // ------------------------------------------------------------------ D == 128
 
-// Shape of the D == 128 kernel: WARPS warps share one head (128 / WARPS rows
-// each); each lane's state loads are issued in NB batches, batch b + 1 in
-// flight while batch b is computed (NB == 1: everything in flight at once).
-// Chosen by measurement on GB300 (48-layer fp32 workload, 256-slot fp16 pool):
-// fp32 8 warps x 16 rows, 4 batches of 4 loads, 3 CTAs per SM; fp16 8 warps x
-// 16 rows, 2 batches of 4 loads, 4 CTAs per SM.
-// kSplit > 1 spreads a head over a cluster of kSplit CTAs (shorter CTAs, a
-// shorter drain at the end of a launch); the fused norm then adds the CTAs'
-// partial sums of squares over distributed shared memory in rank order.
-template <typename TS> struct FastShape {
-    static constexpr int kWarps = 8, kBatches = 4, kMinBlocks = 3, kSplit = 1;
-};
-template <> struct FastShape<__half> {
-    static constexpr int kWarps = 8, kBatches = 2, kMinBlocks = 4, kSplit = 1;
-};
+// Shape of the D == 128 kernel: 8 warps x 16 rows share one head; kMinBlocks
+// CTAs per SM (fp32 3 x 64 KB, fp16 4 x 32 KB of staged state).  Chosen by
+// measurement on GB300 (48-layer fp32 workload, 256-slot fp16 pool) against
+// register-batched loads and other occupancies.
+constexpr int kWarps = 8;
+constexpr int kGroups = 4;                     // cp.async commit groups per lane
+template <typename TS> struct FastShape { static constexpr int kMinBlocks = 3; };
+template <> struct FastShape<__half> { static constexpr int kMinBlocks = 4; };
 
-template <typename TS, bool NORM, int WARPS, int NB, int MINB, int SPLIT>
-__global__ void __launch_bounds__(WARPS * 32, MINB)
+template <typename TS>
+constexpr int stage_bytes() { return kD * kD * (int)sizeof(TS); }
+
+template <typename TS, bool NORM, int MINB>
+__global__ void __launch_bounds__(kWarps * 32, MINB)
 decode_d128(const DecodeParams p)
 {
     using V = Vec16<TS>;
     constexpr int EPV = V::N;                  // state elements per 16-byte vector
     constexpr int LPR = kD / EPV;              // lanes per state row: 32 fp32, 16 fp16
-    constexpr int RPL = 32 / LPR;              // rows per warp-wide load: 1 fp32, 2 fp16
-    constexpr int RPW = kD / (WARPS * SPLIT);  // rows per warp
-    constexpr int NLD = RPW / RPL;             // 16-byte state loads per lane
-    constexpr int LPB = NLD / NB;              // loads per batch
-    static_assert(RPW <= 32 && NLD % NB == 0 && NLD >= NB, "shape");
+    constexpr int RPL = 32 / LPR;              // rows per warp-wide access: 1 fp32, 2 fp16
+    constexpr int RPW = kD / kWarps;           // rows per warp
+    constexpr int NLD = RPW / RPL;             // 16-byte state vectors per lane
+    constexpr int PER = NLD / kGroups;         // vectors per commit group
+    constexpr int VPR = kD * (int)sizeof(TS) / 16;   // vectors per state row
+    static_assert(NLD % kGroups == 0 && RPW <= 32, "shape");
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint4 *stage = reinterpret_cast<uint4 *>(smem_raw);   // [kD rows][VPR], the head as stored
 
-    const int unit = blockIdx.x / SPLIT;       // (sequence, value head)
-    const int part = blockIdx.x - unit * SPLIT;  // which rows of the head (cluster rank)
+    const int unit = blockIdx.x;               // (sequence, value head)
     const int seq = unit / p.nv;
     const int h = unit - seq * p.nv;
     const int g = h % p.nk;                    // tiled key-head pairing
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int sub = lane / LPR;                // which row of a warp-wide load
+    const int sub = lane / LPR;                // which row of a warp-wide access
     const int col = (lane % LPR) * EPV;        // first column this lane owns
-    const int row0 = part * (kD / SPLIT) + warp * RPW;
+    const int row0 = warp * RPW;
 
-    TS *S = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD;
-    TS *rowp = S + (int64_t)(row0 + sub) * kD + col;
+    TS *rowp = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD
+             + (int64_t)(row0 + sub) * kD + col;
+    uint4 *mine = stage + (row0 + sub) * VPR + (lane % LPR);
 
-    // 1. the first batch of this lane's state slice, in flight before anything else
-    uint4 raw[NB > 1 ? 2 : 1][LPB];
+    // 1. every state vector of this lane's slice in flight before anything else
 #pragma unroll
-    for (int i = 0; i < LPB; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
+    for (int gi = 0; gi < kGroups; ++gi) {
+#pragma unroll
+        for (int ii = 0; ii < PER; ++ii) {
+            const int i = gi * PER + ii;
+            cp_async16(mine + i * RPL * VPR, rowp + (int64_t)i * RPL * kD);
+        }
+        cp_async_commit();
+    }
 
     // 2. token inputs
     const float *kp = p.k + seq * p.qk_stride + (int64_t)g * kD + col;
@@ -109,20 +117,20 @@ decode_d128(const DecodeParams p)
     for (int j = 0; j < EPV; ++j) kq = fmaf(kx[j], qx[j], kq);
     kq = group_sum<LPR>(kq);
 
-    // 3. per row: two dot products, the delta coefficient, output, write-back
+    // 3. per row, as its group lands: two dot products, the delta coefficient,
+    //    output, write-back
     float o_keep = 0.f;                        // lane r keeps o of row row0 + r
 #pragma unroll
-    for (int bt = 0; bt < NB; ++bt) {
-        if (bt + 1 < NB) {
+    for (int gi = 0; gi < kGroups; ++gi) {
+        if (gi == 0) cp_async_wait<kGroups - 1>();
+        else if (gi == 1) cp_async_wait<kGroups - 2>();
+        else if (gi == 2) cp_async_wait<kGroups - 3>();
+        else cp_async_wait<0>();
 #pragma unroll
-            for (int i = 0; i < LPB; ++i)
-                raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * LPB + i) * RPL * kD);
-        }
-#pragma unroll
-        for (int ii = 0; ii < LPB; ++ii) {
-            const int i = bt * LPB + ii;       // load index within the lane's slice
+        for (int ii = 0; ii < PER; ++ii) {
+            const int i = gi * PER + ii;       // vector index within the lane's slice
             float s[EPV];
-            V::unpack(raw[bt & 1][ii], s);
+            V::unpack(mine[i * RPL * VPR], s);
             float u = 0.f, w = 0.f;
 #pragma unroll
             for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
@@ -149,30 +157,19 @@ decode_d128(const DecodeParams p)
     if constexpr (!NORM) {
         if (row_lane) p.o[seq * p.o_stride + (int64_t)h * kD + row0 + lane] = o_keep;
     } else {
-        // 4. gated RMS norm over the head's 128 outputs, in this CTA (and its cluster peers)
-        __shared__ float red[WARPS];
-        __shared__ float part_sum;
+        // 4. gated RMS norm over the head's 128 outputs, in this CTA
+        __shared__ float red[kWarps];
         const float ss = group_sum<32>(o_keep * o_keep);   // lanes >= RPW hold 0
         if (lane == 0) red[warp] = ss;
         __syncthreads();
         float tot = 0.f;
 #pragma unroll
-        for (int i = 0; i < WARPS; ++i) tot += red[i];
-        if constexpr (SPLIT > 1) {
-            if (threadIdx.x == 0) part_sum = tot;
-            cluster_arrive();
-            cluster_wait();                    // every CTA's partial sum is written
-            tot = 0.f;
-#pragma unroll
-            for (int r = 0; r < SPLIT; ++r) tot += ld_cluster_f32(&part_sum, r);
-            cluster_arrive();                  // done reading the peers' shared memory
-        }
+        for (int i = 0; i < kWarps; ++i) tot += red[i];
         const float rstd = rsqrtf(tot * (1.0f / kD) + p.eps);
         if (row_lane) {
             const float y = gn_l * o_keep * rstd * silu(z_l);
             p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
         }
-        if constexpr (SPLIT > 1) cluster_wait();   // no CTA leaves while a peer may read it
     }
 }
 
@@ -266,27 +263,14 @@ template <typename TS, bool NORM>
 cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
 {
     const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
-    using F = FastShape<TS>;
     if (fast) {
-        auto kern = decode_d128<TS, NORM, F::kWarps, F::kBatches, F::kMinBlocks, F::kSplit>;
-        if (F::kSplit == 1) {
-            kern<<<grid, F::kWarps * 32, 0, s>>>(p);
-        } else {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(grid * F::kSplit, 1, 1);
-            cfg.blockDim = dim3(F::kWarps * 32, 1, 1);
-            cfg.stream = s;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = F::kSplit;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            return cudaLaunchKernelEx(&cfg, kern, p);
-        }
+        constexpr auto kern = decode_d128<TS, NORM, FastShape<TS>::kMinBlocks>;
+        const cudaError_t e = allow_dynamic_smem<kern>(stage_bytes<TS>());
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kWarps * 32, stage_bytes<TS>(), s>>>(p);
+    } else {
+        decode_generic<TS, NORM><<<grid, kGenWarps * 32, 0, s>>>(p);
     }
-    else decode_generic<TS, NORM><<<grid, kGenWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace gdn {
 
 constexpr unsigned kFull = 0xffffffffu;
@@ -75,6 +77,23 @@ cudaError_t launch_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, bool 
 // Number of SMs of the current device (cached per device id).
 int sm_count();
 
+// Raise kernel Kern's dynamic shared-memory limit to `bytes` (above the 48 KB
+// default).  The attribute belongs to the current device's context, so it is
+// set once per device (ids below 64; others every call).
+template <auto Kern>
+cudaError_t allow_dynamic_smem(int bytes)
+{
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 // ---------------------------------------------------------------- device helpers
 
 // Streaming 16-byte global load / store: the state is touched once per call,
@@ -106,27 +125,14 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
     return *reinterpret_cast<uint16_t *>(&b);
 }
 
-// Thread-block cluster helpers (hardware barriers; distributed shared memory).
-__device__ __forceinline__ unsigned cluster_rank() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
+// cp.async (global -> shared, bypassing L1) and its hardware group waits.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
 }
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// A float in the shared memory of cluster rank `rank`, at the offset of `p` in this CTA's.
-__device__ __forceinline__ float ld_cluster_f32(const float *p, unsigned rank) {
-    const unsigned local = (unsigned)__cvta_generic_to_shared(p);
-    unsigned remote;
-    float v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 // A 16-byte vector of state elements, widened to / narrowed from fp32.
 template <typename TS> struct Vec16;
