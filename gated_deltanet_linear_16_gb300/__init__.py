@@ -23,11 +23,13 @@ __all__ = [
     "GdnError", "load", "build", "library_path",
     "GDN_STATE_F32", "GDN_STATE_F16", "STATUS",
     "gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
+    "gdn_decode_conv_norm_noalloc", "GDN_NOALLOC_MAX_KEY_HEADS",
     "gdn_h_f32_to_f16", "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error",
 ]
 
 GDN_STATE_F32 = 0
 GDN_STATE_F16 = 1
+GDN_NOALLOC_MAX_KEY_HEADS = 16384     # batch * NK limit of gdn_decode_conv_norm_noalloc
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIGN",
           4: "GDN_ERR_ALIAS", 5: "GDN_ERR_CUDA"}
 
@@ -60,6 +62,8 @@ def _declare(lib):
                                     i64, i64, i64, i64, i64, P]
     lib.gdn_decode_conv_norm.argtypes = [P, i32, i64, P, i64, i32, P, P, P, P, P, P, P, P, f32, f32, P, P,
                                          i32, i32, i32, i32, i64, i64, i64, i64, P]
+    lib.gdn_decode_conv_norm_noalloc.argtypes = [P, i32, i64, P, i64, i32, P, P, P, P, P, P, P, P, f32, f32, P,
+                                                 i32, i32, i32, i32, i64, i64, i64, i64, P]
     lib.gdn_decode_chunk2.argtypes = [P, i32, i64, P, i64, P, P, P, P, P, P, i32, i32, i32, i32,
                                       i64, i64, i64, i64, P]
     lib.gdn_prefill_seq.argtypes = [P, i32, i64, P, P, P, P, P, P, i32, i32, i32, i32, i32,
@@ -67,7 +71,7 @@ def _declare(lib):
     lib.gdn_h_f32_to_f16.argtypes = [P, P, u64, P]
     lib.gdn_h_f16_to_f32.argtypes = [P, P, u64, P]
     for fn in ("gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
-               "gdn_h_f32_to_f16",
+               "gdn_decode_conv_norm_noalloc", "gdn_h_f32_to_f16",
                "gdn_h_f16_to_f32"):
         getattr(lib, fn).restype = i32
     lib.gdn_status_str.argtypes = [i32]
@@ -189,6 +193,29 @@ def gdn_decode_conv_norm(state, conv_state, x, conv_w, br, ar, dt, rate, z, gn, 
         out_stride if out_stride is not None else nv * d,
         _stream(stream))
     _check("gdn_decode_conv_norm", st)
+
+
+def gdn_decode_conv_norm_noalloc(state, conv_state, x, conv_w, br, ar, dt, rate, z, gn, out, *, batch, nk,
+                                 nv, d, taps, eps=1e-6, l2_eps=1e-6, state_pitch=None, conv_pitch=None,
+                                 state_dtype=None, x_stride=None, gate_stride=None, z_stride=None,
+                                 out_stride=None, stream=None):
+    """gdn_decode_conv_norm without a workspace: the counters live in the library's static device
+    memory (batch*nk <= GDN_NOALLOC_MAX_KEY_HEADS; calls that may overlap on one device race).
+    See include/gdn.h."""
+    lib = load()
+    sd = _state_dtype(state, state_dtype)
+    C = (2 * nk + nv) * d
+    st = lib.gdn_decode_conv_norm_noalloc(
+        _ptr(state), sd, state_pitch if state_pitch is not None else nv * d * d,
+        _ptr(conv_state), conv_pitch if conv_pitch is not None else taps * C, taps,
+        _ptr(x), _ptr(conv_w), _ptr(br), _ptr(ar), _ptr(dt), _ptr(rate), _ptr(z), _ptr(gn),
+        float(l2_eps), float(eps), _ptr(out), batch, nk, nv, d,
+        x_stride if x_stride is not None else C,
+        gate_stride if gate_stride is not None else nv,
+        z_stride if z_stride is not None else nv * d,
+        out_stride if out_stride is not None else nv * d,
+        _stream(stream))
+    _check("gdn_decode_conv_norm_noalloc", st)
 
 
 def gdn_decode_chunk2(state, state_mid, q, k, v, alpha, beta, o, *, batch, nk, nv, d,

@@ -27,7 +27,8 @@ NVCC_FLAGS = ARCH + [
     "-I" + INCLUDE, "-I" + CSRC,
 ]
 LINK_FLAGS = ARCH + ["-shared", "-cudart", "static"]
-SOURCES = ["gdn_abi.cu", "gdn_decode.cu", "gdn_chunk2.cu", "gdn_conv_norm.cu", "gdn_prefill.cu", "gdn_convert.cu"]
+SOURCES = ["gdn_abi.cu", "gdn_decode.cu", "gdn_chunk2.cu", "gdn_conv_norm.cu", "gdn_prefill.cu", "gdn_convert.cu",
+           "gdn_noalloc.cu"]
 
 
 def nvcc() -> str:

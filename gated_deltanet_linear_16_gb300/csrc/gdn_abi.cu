@@ -151,6 +151,9 @@ int decode_entry(void *state, int state_dtype, int64_t state_pitch,
 }
 
 }  // namespace
+
+int report_cuda_error(cudaError_t e) { return cuda_status(e); }
+
 }  // namespace gdn
 
 using namespace gdn;

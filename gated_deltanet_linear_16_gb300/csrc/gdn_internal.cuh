@@ -77,6 +77,10 @@ cudaError_t launch_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, bool 
 // Number of SMs of the current device (cached per device id).
 int sm_count();
 
+// GDN_OK for cudaSuccess; otherwise records e for gdn_last_cuda_error() on
+// this host thread and returns GDN_ERR_CUDA.
+int report_cuda_error(cudaError_t e);
+
 // Raise kernel Kern's dynamic shared-memory limit to `bytes` (above the 48 KB
 // default).  The attribute belongs to the current device's context, so it is
 // set once per device (ids below 64; others every call).

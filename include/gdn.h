@@ -161,6 +161,38 @@ GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pit
                                  int64_t out_stride, void *stream);
 
 /*
+ * gdn_decode_conv_norm_noalloc -- gdn_decode_conv_norm without a workspace
+ * argument, for callers that cannot provide device memory beyond the inputs
+ * and outputs (no allocator of their own, a fixed memory plan, or no device
+ * synchronisation allowed on the decode path).  None of the source pages has
+ * a counterpart: it is an addition of this library.
+ *   The counters live in a static array inside the library, one copy per
+ *   device, GDN_NOALLOC_MAX_KEY_HEADS int32 long.  The first call on a device
+ *   (with that device current) looks up its address once; make that first
+ *   call before any stream capture begins.  The array is zero when the
+ *   library is loaded and every completed call leaves it zero; nothing needs
+ *   clearing by the caller.  The call allocates and frees nothing.
+ *   Calls that can run on the GPU at the same time on one device (streams
+ *   with no ordering between them) share the array and race: results are
+ *   then undefined.  Calls ordered on one stream are fine.
+ *   Arguments, layouts and results as gdn_decode_conv_norm (without
+ *   workspace).
+ *   Errors as gdn_decode_conv_norm; GDN_ERR_UNSUPPORTED if batch * NK >
+ *   GDN_NOALLOC_MAX_KEY_HEADS (checked first); GDN_ERR_CUDA if the address
+ *   lookup fails.
+ */
+#define GDN_NOALLOC_MAX_KEY_HEADS 16384
+GDN_API int gdn_decode_conv_norm_noalloc(void *state, int state_dtype, int64_t state_pitch,
+                                         float *conv_state, int64_t conv_pitch, int taps,
+                                         const float *x, const float *conv_w,
+                                         const float *br, const float *ar, const float *dt, const float *rate,
+                                         const float *z, const float *gn, float l2_eps, float eps,
+                                         uint16_t *out,
+                                         int batch, int nk, int nv, int d,
+                                         int64_t x_stride, int64_t gate_stride, int64_t z_stride,
+                                         int64_t out_stride, void *stream);
+
+/*
  * gdn_decode_chunk2 -- two tokens per sequence through the recurrence in one
  * launch (the verify step of speculative decoding), keeping the state after
  * the first token so that a rejected draft token can be rolled back.

@@ -41,7 +41,7 @@ def lib(built):
 def test_exports_match_header(built):
     want = declared_symbols()
     assert want == sorted(["gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm",
-                           "gdn_prefill_seq", "gdn_h_f32_to_f16",
+                           "gdn_decode_conv_norm_noalloc", "gdn_prefill_seq", "gdn_h_f32_to_f16",
                            "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error"])
     out = subprocess.run(["nm", "-D", "--defined-only", gdn.library_path()], capture_output=True, text=True,
                          check=True).stdout
@@ -131,6 +131,31 @@ def test_conv_norm_rejects(lib, kw, want):
 
 def test_conv_norm_empty_is_ok(lib):
     assert conv_norm(lib, batch=0) == OK
+
+
+def conv_norm_noalloc(lib, **kw):
+    nk, nv, d, taps = 2, 6, 128, 4
+    C = (2 * nk + nv) * d
+    a = dict(state=A, dt=0, pitch=nv * d * d, ring=A + (9 << 30), rpitch=taps * C, taps=taps, x=A + (1 << 30),
+             w=A + (2 << 30), br=A + (3 << 30), ar=A + (4 << 30), dtb=A + (5 << 30), rate=A + (5 << 30) + 4096,
+             z=A + (7 << 30), gn=A + (8 << 30), l2=1e-6, eps=1e-6, out=A + (6 << 30),
+             batch=2, nk=nk, nv=nv, d=d, xs=C, gs=nv, zs=nv * d, outs=nv * d)
+    a.update(kw)
+    return lib.gdn_decode_conv_norm_noalloc(a["state"], a["dt"], a["pitch"], a["ring"], a["rpitch"], a["taps"],
+                                            a["x"], a["w"], a["br"], a["ar"], a["dtb"], a["rate"], a["z"], a["gn"],
+                                            a["l2"], a["eps"], a["out"], a["batch"], a["nk"], a["nv"], a["d"],
+                                            a["xs"], a["gs"], a["zs"], a["outs"], None)
+
+
+def test_conv_norm_noalloc_rejects_beyond_static_counters(lib):
+    """batch * NK above the static counter array is refused first, before any CUDA call."""
+    assert conv_norm_noalloc(lib, batch=gdn.GDN_NOALLOC_MAX_KEY_HEADS // 2 + 1) == UNSUP
+
+
+def test_conv_norm_noalloc_without_device_reports_cuda_error(lib):
+    """On a host without a GPU the per-device set-up fails and says so (GDN_ERR_CUDA)."""
+    assert conv_norm_noalloc(lib) == CUDA
+    assert lib.gdn_last_cuda_error() != 0
 
 
 def prefill(lib, **kw):
