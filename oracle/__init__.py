@@ -17,7 +17,8 @@ Passages followed (page title, section):
   * same page, kernel ``gdn_gate_norm`` -- RMS norm then silu(z) gate;
   * metrale_model_layers/layers/ops/ssm_gdn_a.rs, ``gdn_prefill_regresident``
     -- token-sequential prefill; ``ssm_h_state_f32_to_f16`` /
-    ``ssm_h_state_f16_to_f32`` -- round-to-nearest-even converters.
+    ``ssm_h_state_f16_to_f32`` -- round-to-nearest-even converters;
+  * gdn.rs, kernel ``gdn_gate_norm_q`` -- int8 activation groups of 32.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
 forms, invariants, a textbook special case (D = 1 scalar recurrence), the
@@ -74,6 +75,8 @@ def bind(path):
     lib.orc_gates.restype = None
     lib.orc_decode_f64.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
     lib.orc_decode_f64.restype = None
+    lib.orc_quant_q8_groups.argtypes = [i64, P, P, P]
+    lib.orc_quant_q8_groups.restype = None
     return lib
 
 
@@ -219,6 +222,20 @@ def decode_f64(S, q, k, v, alpha, beta, nk):
     o = np.empty((B, nv * d), dtype=np.float64)
     lib.orc_decode_f64(B, nk, nv, d, _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o))
     return o
+
+
+def quant_q8(y):
+    """Int8 groups of 32 (gdn.rs `gdn_gate_norm_q`): fp32 values -> (int8 codes, fp32 scales);
+    scale = max|y| / 127 over the group (1 if all zero), code = y / scale rounded half to even,
+    all decisions in fp32 as the page takes them.  len(y) must be a multiple of 32."""
+    yy = _c(np.asarray(y).reshape(-1), np.float32)
+    n = yy.size
+    if n % 32:
+        raise ValueError("quant_q8: length must be a multiple of 32")
+    code = np.empty(n, dtype=np.int8)
+    scale = np.empty(n // 32, dtype=np.float32)
+    _load().orc_quant_q8_groups(n, _ptr(yy), _ptr(code), _ptr(scale))
+    return code, scale
 
 
 def parallel_map(fn, items, threads=None):

@@ -271,3 +271,41 @@ void orc_decode_f64(int batch, int nk, int nv, int d, double *S,
     }
     free(work);
 }
+
+/* ---------------------------------------------------------------------------
+ * Int8 activation groups of the normed output ([gdn.rs] `gdn_gate_norm_q`,
+ * the gate norm with the activation quantisation fused in for the int8
+ * o-projection that follows).  The output vector of a token is cut into
+ * groups of 32 consecutive values (a head's D outputs hold D/32 groups).  A
+ * group's scale is its largest magnitude divided by 127, or 1 when the group
+ * is all zero; each value's code is value / scale rounded to the nearest
+ * integer, ties to even.  The page takes these decisions in fp32 on the fp32
+ * output, so this function does the same: fp32 division on the given fp32
+ * values (IEEE, correctly rounded), then the rounding rule below, written
+ * out in double (exact for fp32 operands).
+ * ------------------------------------------------------------------------- */
+static double round_half_even(double r)
+{
+    double f = floor(r);
+    double frac = r - f;
+    if (frac > 0.5 || (frac == 0.5 && fmod(f, 2.0) != 0.0)) f += 1.0;
+    return f;
+}
+
+/* n values (a multiple of 32) -> n codes and n/32 scales. */
+void orc_quant_q8_groups(int64_t n, const float *y, int8_t *code, float *scale)
+{
+    for (int64_t g0 = 0; g0 < n; g0 += 32) {
+        float am = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            float m = fabsf(y[g0 + i]);
+            if (m > am) am = m;
+        }
+        float sc = am > 0.0f ? am / 127.0f : 1.0f;
+        scale[g0 / 32] = sc;
+        for (int i = 0; i < 32; ++i) {
+            float r = y[g0 + i] / sc;
+            code[g0 + i] = (int8_t)round_half_even((double)r);
+        }
+    }
+}

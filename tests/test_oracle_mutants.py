@@ -46,6 +46,12 @@ MUTANTS = [
     ("gate rate applied twice", "pow(1.0 + exp((double)ar[i] + (double)dt[i]), (double)rate[i])",
      "pow(1.0 + exp((double)ar[i] + (double)dt[i]), -exp((double)rate[i]))"),
     ("beta not a sigmoid", "beta[i] = 1.0 / (1.0 + exp(-(double)br[i]));", "beta[i] = (double)br[i];"),
+    ("q8 scale over 128", "am > 0.0f ? am / 127.0f : 1.0f", "am > 0.0f ? am / 128.0f : 1.0f"),
+    ("q8 ties rounded away from zero", "(frac > 0.5 || (frac == 0.5 && fmod(f, 2.0) != 0.0))", "(frac >= 0.5)"),
+    ("q8 truncation", "if (frac > 0.5 || (frac == 0.5 && fmod(f, 2.0) != 0.0)) f += 1.0;", "(void)frac;"),
+    ("q8 group max over half the group", "for (int i = 0; i < 32; ++i) {\n            float m = fabsf",
+     "for (int i = 0; i < 16; ++i) {\n            float m = fabsf"),
+    ("q8 zero group scale 0", "am > 0.0f ? am / 127.0f : 1.0f", "am / 127.0f"),
     ("widening drops the sign", "return sign | (ex - 15u + 127u) << 23 | (fr << 13);", "return (ex - 15u + 127u) << 23 | (fr << 13);"),
 ]
 

@@ -455,3 +455,56 @@ def test_decode_f64_matches_decode_on_f32_representable_inputs():
     o2 = oracle.decode_f64(S2, q.astype(np.float64), k.astype(np.float64), v.astype(np.float64),
                            a.astype(np.float64), b.astype(np.float64), 2)
     assert np.array_equal(S, S2) and np.array_equal(o1, o2)
+
+
+# ---- int8 activation groups (gdn.rs `gdn_gate_norm_q`) -------------------------------------
+
+def test_q8_ties_round_to_even_at_unit_scale():
+    """A group whose largest magnitude is 127 has scale exactly 1, so the codes are the values
+    rounded half to even: 63.5 -> 64, 0.5 -> 0, 1.5 -> 2, 2.5 -> 2, 126.5 -> 126."""
+    y = np.zeros(32, np.float32)
+    y[:10] = [127, 63.5, -63.5, 0.5, 1.5, 2.5, -2.5, 126.5, -0.5, 3.25]
+    code, scale = oracle.quant_q8(y)
+    assert scale.tolist() == [1.0]
+    assert code[:10].tolist() == [127, 64, -64, 0, 2, 2, -2, 126, 0, 3]
+    assert not code[10:].any()
+
+
+def test_q8_scale_is_group_max_over_127():
+    """Largest magnitude 254 (negative here) gives scale 2: 3 -> 1.5 -> 2, 5 -> 2.5 -> 2,
+    -7 -> -3.5 -> -4, and the largest value itself maps to -127."""
+    y = np.zeros(32, np.float32)
+    y[:4] = [3, 5, -7, -254]
+    code, scale = oracle.quant_q8(y)
+    assert scale.tolist() == [2.0]
+    assert code[:4].tolist() == [2, 2, -4, -127]
+
+
+def test_q8_zero_group_has_unit_scale():
+    code, scale = oracle.quant_q8(np.zeros(64, np.float32))
+    assert scale.tolist() == [1.0, 1.0] and not code.any()
+
+
+def test_q8_groups_are_32_consecutive_values():
+    """Each group of 32 gets its own scale: a large value in the second group leaves the first
+    group's codes alone."""
+    y = np.zeros(96, np.float32)
+    y[5], y[40], y[70] = 12.7, -1270.0, 0.127
+    code, scale = oracle.quant_q8(y)
+    assert np.allclose(scale, [0.1, 10.0, 0.001], rtol=1e-6)
+    assert (code[5], code[40], code[70]) == (127, -127, 127)
+
+
+def test_q8_bounds_on_random_groups():
+    """Any group: |code| <= 127, the largest magnitude maps to +-127, and code * scale is within
+    half a step of the value."""
+    rng = np.random.default_rng(3)
+    y = (rng.standard_normal(32 * 200) * rng.choice([1e-3, 1.0, 50.0], size=32 * 200)).astype(np.float32)
+    code, scale = oracle.quant_q8(y)
+    g = y.reshape(-1, 32).astype(np.float64)
+    c = code.reshape(-1, 32).astype(np.int64)
+    s = scale.astype(np.float64)[:, None]
+    assert np.abs(c).max() <= 127
+    top = np.argmax(np.abs(g), axis=1)
+    assert np.all(np.abs(c[np.arange(len(top)), top]) == 127)
+    assert np.all(np.abs(c * s - g) <= 0.5 * s * (1 + 1e-6))
