@@ -36,17 +36,25 @@ constexpr int kD = 128;
 constexpr int kWarps = 8;
 constexpr int kRowsPerWarp = kD / kWarps;   // 16
 
+constexpr int kMaxTaps = 8;                 // the host rejects more
+
 // One channel through the conv ring: shift up by one, append x, reduce with the
-// taps, silu.  The caller is the only thread touching this channel.
+// taps, silu.  The caller is the only thread touching this channel.  All stored
+// entries are read before any is written (one load latency, not one per tap).
 __device__ __forceinline__ float conv_silu_channel(float *ring, const float *x, const float *w,
                                                    int64_t c, int64_t C, int taps) {
-    float acc = 0.f;
-    for (int t = 0; t + 1 < taps; ++t) {
-        const float val = ring[(int64_t)(t + 1) * C + c];
-        ring[(int64_t)t * C + c] = val;
-        acc = fmaf(val, __ldg(w + (int64_t)t * C + c), acc);
-    }
+    float val[kMaxTaps - 1];
+#pragma unroll
+    for (int t = 0; t + 1 < kMaxTaps; ++t) val[t] = t + 1 < taps ? ring[(int64_t)(t + 1) * C + c] : 0.f;
     const float xv = __ldg(x + c);
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t + 1 < kMaxTaps; ++t) {
+        if (t + 1 < taps) {
+            ring[(int64_t)t * C + c] = val[t];
+            acc = fmaf(val[t], __ldg(w + (int64_t)t * C + c), acc);
+        }
+    }
     ring[(int64_t)(taps - 1) * C + c] = xv;
     acc = fmaf(xv, __ldg(w + (int64_t)(taps - 1) * C + c), acc);
     return silu(acc);
@@ -58,13 +66,18 @@ __device__ __forceinline__ float conv_silu_channel(float *ring, const float *x, 
 __device__ __forceinline__ float conv_silu_channel_ro(const float *ring, const float *x, const float *w,
                                                       int64_t c, int64_t C, int taps,
                                                       float *keep, int kstride) {
-    float acc = 0.f;
-    for (int t = 0; t + 1 < taps; ++t) {
-        const float val = ring[(int64_t)(t + 1) * C + c];
-        keep[t * kstride] = val;
-        acc = fmaf(val, __ldg(w + (int64_t)t * C + c), acc);
-    }
+    float val[kMaxTaps - 1];
+#pragma unroll
+    for (int t = 0; t + 1 < kMaxTaps; ++t) val[t] = t + 1 < taps ? ring[(int64_t)(t + 1) * C + c] : 0.f;
     const float xv = __ldg(x + c);
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t + 1 < kMaxTaps; ++t) {
+        if (t + 1 < taps) {
+            keep[t * kstride] = val[t];
+            acc = fmaf(val[t], __ldg(w + (int64_t)t * C + c), acc);
+        }
+    }
     keep[(taps - 1) * kstride] = xv;
     acc = fmaf(xv, __ldg(w + (int64_t)(taps - 1) * C + c), acc);
     return silu(acc);
@@ -78,7 +91,14 @@ __device__ __forceinline__ void gates(const ConvNormParams &p, int seq, int h, f
     alpha = powf(1.0f + expf(ar + __ldg(p.dt + h)), __ldg(p.rate + h));
 }
 
-template <typename TS, int NB, int MINB>
+constexpr int kGroups = 4;                 // cp.async commit groups per lane (staged)
+
+template <typename TS>
+constexpr int stage_bytes() { return kD * kD * (int)sizeof(TS); }
+
+// STAGED: the head's state goes to shared memory by cp.async, every load in
+// flight at once (as the staged decode kernel); otherwise NB register batches.
+template <typename TS, bool STAGED, int NB, int MINB>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
 conv_norm_d128(const ConvNormParams p)
 {
@@ -87,8 +107,10 @@ conv_norm_d128(const ConvNormParams p)
     constexpr int LPR = kD / EPV;
     constexpr int RPL = 32 / LPR;
     constexpr int NLD = kRowsPerWarp / RPL;
-    constexpr int LPB = NLD / NB;
-    static_assert(NLD % NB == 0, "shape");
+    constexpr int VPR = kD * (int)sizeof(TS) / 16;
+    constexpr int NBAT = STAGED ? kGroups : NB;
+    constexpr int PER = NLD / NBAT;
+    static_assert(NLD % NBAT == 0, "shape");
 
     __shared__ __align__(16) float q_s[kD];
     __shared__ __align__(16) float k_s[kD];
@@ -113,9 +135,23 @@ conv_norm_d128(const ConvNormParams p)
                (int64_t)(row0 + sub) * kD + col;
 
     // 1. state loads in flight before the producers run
-    uint4 raw[NB > 1 ? 2 : 1][LPB];
+    extern __shared__ __align__(16) unsigned char smem_raw[];   // staged: [kD rows][VPR]
+    uint4 *mine = reinterpret_cast<uint4 *>(smem_raw) + (row0 + sub) * VPR + (lane % LPR);
+    uint4 raw[STAGED ? 1 : (NB > 1 ? 2 : 1)][STAGED ? 1 : PER];
+    if constexpr (STAGED) {
 #pragma unroll
-    for (int i = 0; i < LPB; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
+        for (int gi = 0; gi < kGroups; ++gi) {
+#pragma unroll
+            for (int ii = 0; ii < PER; ++ii) {
+                const int i = gi * PER + ii;
+                cp_async16(mine + i * RPL * VPR, rowp + (int64_t)i * RPL * kD);
+            }
+            cp_async_commit();
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
+    }
 
     // 2. producers: v of this head (threads 0..127, ring rows written now: their only writer);
     //    q and k of the key head (threads 128..255) from the ring as it was, not written yet
@@ -169,38 +205,47 @@ conv_norm_d128(const ConvNormParams p)
 
     // 4. the step, as in the decode kernel
     float o_keep = 0.f;
+    auto row_step = [&](const uint4 packed, const int i) {
+        float s[EPV];
+        V::unpack(packed, s);
+        float u = 0.f, w = 0.f;
 #pragma unroll
-    for (int bt = 0; bt < NB; ++bt) {
-        if (bt + 1 < NB) {
+        for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
+        u = group_sum<LPR>(u);
+        w = group_sum<LPR>(w);
+        const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
+        const float coef = beta * (va - alpha * u);
+        const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
 #pragma unroll
-            for (int i = 0; i < LPB; ++i)
-                raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * LPB + i) * RPL * kD);
-        }
+        for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
+        st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
+        if constexpr (RPL == 1) {
+            if (lane == i) o_keep = oa;
+        } else {
 #pragma unroll
-        for (int ii = 0; ii < LPB; ++ii) {
-            const int i = bt * LPB + ii;
-            float s[EPV];
-            V::unpack(raw[bt & 1][ii], s);
-            float u = 0.f, w = 0.f;
-#pragma unroll
-            for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
-            u = group_sum<LPR>(u);
-            w = group_sum<LPR>(w);
-            const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
-            const float coef = beta * (va - alpha * u);
-            const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
-#pragma unroll
-            for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
-            st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
-            if constexpr (RPL == 1) {
-                if (lane == i) o_keep = oa;
-            } else {
-#pragma unroll
-                for (int r = 0; r < RPL; ++r) {
-                    const float orr = __shfl_sync(kFull, oa, r * LPR);
-                    if (lane == i * RPL + r) o_keep = orr;
-                }
+            for (int r = 0; r < RPL; ++r) {
+                const float orr = __shfl_sync(kFull, oa, r * LPR);
+                if (lane == i * RPL + r) o_keep = orr;
             }
+        }
+    };
+#pragma unroll
+    for (int bt = 0; bt < NBAT; ++bt) {
+        if constexpr (STAGED) {
+            if (bt == 0) cp_async_wait<kGroups - 1>();
+            else if (bt == 1) cp_async_wait<kGroups - 2>();
+            else if (bt == 2) cp_async_wait<kGroups - 3>();
+            else cp_async_wait<0>();
+#pragma unroll
+            for (int ii = 0; ii < PER; ++ii) row_step(mine[(bt * PER + ii) * RPL * VPR], bt * PER + ii);
+        } else {
+            if (bt + 1 < NBAT) {
+#pragma unroll
+                for (int i = 0; i < PER; ++i)
+                    raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * PER + i) * RPL * kD);
+            }
+#pragma unroll
+            for (int ii = 0; ii < PER; ++ii) row_step(raw[bt & 1][ii], bt * PER + ii);
         }
     }
 
@@ -334,16 +379,30 @@ conv_norm_generic(const ConvNormParams p)
     }
 }
 
-template <typename TS> struct ConvShape { static constexpr int kBatches = 4, kMinBlocks = 3; };
-template <> struct ConvShape<__half> { static constexpr int kBatches = 2, kMinBlocks = 3; };
+// Shapes of the D == 128 kernel, by measurement on GB300 (one layer at batch 32
+// fp32, 256-slot fp16 pool): fp32 register batches (4 x 4 loads, 3 CTAs per
+// SM); fp16 staged in shared memory (32 KB + 10 KB a CTA, 5 CTAs per SM).
+template <typename TS> struct ConvShape {
+    static constexpr bool kStaged = false;
+    static constexpr int kBatches = 4, kMinBlocks = 3;
+};
+template <> struct ConvShape<__half> {
+    static constexpr bool kStaged = true;
+    static constexpr int kBatches = 1, kMinBlocks = 5;
+};
 
 template <typename TS>
 cudaError_t launch_typed(const ConvNormParams &p, bool fast, cudaStream_t s)
 {
     if (fast) {
         using F = ConvShape<TS>;
-        conv_norm_d128<TS, F::kBatches, F::kMinBlocks>
-            <<<(unsigned)((int64_t)p.batch * p.nv), kWarps * 32, 0, s>>>(p);
+        constexpr auto kern = conv_norm_d128<TS, F::kStaged, F::kBatches, F::kMinBlocks>;
+        const int dyn = F::kStaged ? stage_bytes<TS>() : 0;
+        if (F::kStaged) {
+            const cudaError_t e = allow_dynamic_smem<kern>(dyn);
+            if (e != cudaSuccess) return e;
+        }
+        kern<<<(unsigned)((int64_t)p.batch * p.nv), kWarps * 32, dyn, s>>>(p);
         return cudaGetLastError();
     }
     const size_t smem = sizeof(float) * ((size_t)(3 + p.repeat) * p.d + 2 * (size_t)p.repeat);

@@ -32,6 +32,10 @@
 //    warp, not per row.
 #include "gdn_internal.cuh"
 
+#ifndef REG_PATH_MAX_BYTES
+#define REG_PATH_MAX_BYTES (int64_t{32} << 20)
+#endif
+
 namespace gdn {
 namespace {
 
@@ -39,19 +43,29 @@ constexpr int kD = 128;
 
 // ------------------------------------------------------------------ D == 128
 
-// Shape of the D == 128 kernel: 8 warps x 16 rows share one head; kMinBlocks
-// CTAs per SM (fp32 3 x 64 KB, fp16 4 x 32 KB of staged state).  Chosen by
-// measurement on GB300 (48-layer fp32 workload, 256-slot fp16 pool) against
-// register-batched loads and other occupancies.
+// Two ways to bring a lane's 16 (fp32) or 8 (fp16) state vectors in, both with
+// 8 warps x 16 rows per head and the same arithmetic (bitwise-identical
+// results):
+//  * staged: every load in flight at once through cp.async into shared memory
+//    (64 KB fp32 / 32 KB fp16 per CTA), four commit groups each consumed as it
+//    lands.  The loads hold no registers while in flight, so 3 (fp32) or 4
+//    (fp16) CTAs per SM keep 128-192 KB outstanding per SM: best when the state
+//    streams from HBM;
+//  * register-batched: NB batches of loads straight into registers, batch b + 1
+//    in flight while batch b is computed: one hop less per element, which wins
+//    when the state is close (a small call whose state sits in L2).
+// The launcher picks one per call; the shapes and the choice come from
+// measurement on GB300.
 constexpr int kWarps = 8;
-constexpr int kGroups = 4;                     // cp.async commit groups per lane
-template <typename TS> struct FastShape { static constexpr int kMinBlocks = 3; };
-template <> struct FastShape<__half> { static constexpr int kMinBlocks = 4; };
+constexpr int kGroups = 4;                     // cp.async commit groups per lane (staged)
+template <typename TS> struct StagedShape { static constexpr int kMinBlocks = 3; };
+template <> struct StagedShape<__half> { static constexpr int kMinBlocks = 4; };
+template <typename TS> struct RegShape { static constexpr int kBatches = 4, kMinBlocks = 3; };
 
 template <typename TS>
 constexpr int stage_bytes() { return kD * kD * (int)sizeof(TS); }
 
-template <typename TS, bool NORM, int MINB>
+template <typename TS, bool NORM, bool STAGED, int NB, int MINB>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
 decode_d128(const DecodeParams p)
 {
@@ -61,11 +75,10 @@ decode_d128(const DecodeParams p)
     constexpr int RPL = 32 / LPR;              // rows per warp-wide access: 1 fp32, 2 fp16
     constexpr int RPW = kD / kWarps;           // rows per warp
     constexpr int NLD = RPW / RPL;             // 16-byte state vectors per lane
-    constexpr int PER = NLD / kGroups;         // vectors per commit group
     constexpr int VPR = kD * (int)sizeof(TS) / 16;   // vectors per state row
-    static_assert(NLD % kGroups == 0 && RPW <= 32, "shape");
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint4 *stage = reinterpret_cast<uint4 *>(smem_raw);   // [kD rows][VPR], the head as stored
+    constexpr int NBAT = STAGED ? kGroups : NB;      // groups / batches of loads
+    constexpr int PER = NLD / NBAT;                  // vectors per group / batch
+    static_assert(NLD % NBAT == 0 && RPW <= 32, "shape");
 
     const int unit = blockIdx.x;               // (sequence, value head)
     const int seq = unit / p.nv;
@@ -79,17 +92,24 @@ decode_d128(const DecodeParams p)
 
     TS *rowp = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD
              + (int64_t)(row0 + sub) * kD + col;
-    uint4 *mine = stage + (row0 + sub) * VPR + (lane % LPR);
 
-    // 1. every state vector of this lane's slice in flight before anything else
+    // 1. the state loads in flight before anything else
+    extern __shared__ __align__(16) unsigned char smem_raw[];   // staged: [kD rows][VPR], the head as stored
+    uint4 *mine = reinterpret_cast<uint4 *>(smem_raw) + (row0 + sub) * VPR + (lane % LPR);
+    uint4 raw[STAGED ? 1 : (NB > 1 ? 2 : 1)][STAGED ? 1 : PER];
+    if constexpr (STAGED) {
 #pragma unroll
-    for (int gi = 0; gi < kGroups; ++gi) {
+        for (int gi = 0; gi < kGroups; ++gi) {
 #pragma unroll
-        for (int ii = 0; ii < PER; ++ii) {
-            const int i = gi * PER + ii;
-            cp_async16(mine + i * RPL * VPR, rowp + (int64_t)i * RPL * kD);
+            for (int ii = 0; ii < PER; ++ii) {
+                const int i = gi * PER + ii;
+                cp_async16(mine + i * RPL * VPR, rowp + (int64_t)i * RPL * kD);
+            }
+            cp_async_commit();
         }
-        cp_async_commit();
+    } else {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
     }
 
     // 2. token inputs
@@ -117,40 +137,49 @@ decode_d128(const DecodeParams p)
     for (int j = 0; j < EPV; ++j) kq = fmaf(kx[j], qx[j], kq);
     kq = group_sum<LPR>(kq);
 
-    // 3. per row, as its group lands: two dot products, the delta coefficient,
-    //    output, write-back
+    // 3. per row: two dot products, the delta coefficient, output, write-back
     float o_keep = 0.f;                        // lane r keeps o of row row0 + r
+    auto row_step = [&](const uint4 packed, const int i) {   // i: vector index within the lane's slice
+        float s[EPV];
+        V::unpack(packed, s);
+        float u = 0.f, w = 0.f;
 #pragma unroll
-    for (int gi = 0; gi < kGroups; ++gi) {
-        if (gi == 0) cp_async_wait<kGroups - 1>();
-        else if (gi == 1) cp_async_wait<kGroups - 2>();
-        else if (gi == 2) cp_async_wait<kGroups - 3>();
-        else cp_async_wait<0>();
+        for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
+        u = group_sum<LPR>(u);
+        w = group_sum<LPR>(w);
+        const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
+        const float coef = beta * (va - alpha * u);
+        const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
 #pragma unroll
-        for (int ii = 0; ii < PER; ++ii) {
-            const int i = gi * PER + ii;       // vector index within the lane's slice
-            float s[EPV];
-            V::unpack(mine[i * RPL * VPR], s);
-            float u = 0.f, w = 0.f;
+        for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
+        st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
+        if constexpr (RPL == 1) {
+            if (lane == i) o_keep = oa;
+        } else {
 #pragma unroll
-            for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
-            u = group_sum<LPR>(u);
-            w = group_sum<LPR>(w);
-            const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
-            const float coef = beta * (va - alpha * u);
-            const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
-#pragma unroll
-            for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
-            st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
-            if constexpr (RPL == 1) {
-                if (lane == i) o_keep = oa;
-            } else {
-#pragma unroll
-                for (int r = 0; r < RPL; ++r) {
-                    const float orr = __shfl_sync(kFull, oa, r * LPR);
-                    if (lane == i * RPL + r) o_keep = orr;
-                }
+            for (int r = 0; r < RPL; ++r) {
+                const float orr = __shfl_sync(kFull, oa, r * LPR);
+                if (lane == i * RPL + r) o_keep = orr;
             }
+        }
+    };
+#pragma unroll
+    for (int bt = 0; bt < NBAT; ++bt) {
+        if constexpr (STAGED) {
+            if (bt == 0) cp_async_wait<kGroups - 1>();
+            else if (bt == 1) cp_async_wait<kGroups - 2>();
+            else if (bt == 2) cp_async_wait<kGroups - 3>();
+            else cp_async_wait<0>();
+#pragma unroll
+            for (int ii = 0; ii < PER; ++ii) row_step(mine[(bt * PER + ii) * RPL * VPR], bt * PER + ii);
+        } else {
+            if (bt + 1 < NBAT) {
+#pragma unroll
+                for (int i = 0; i < PER; ++i)
+                    raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * PER + i) * RPL * kD);
+            }
+#pragma unroll
+            for (int ii = 0; ii < PER; ++ii) row_step(raw[bt & 1][ii], bt * PER + ii);
         }
     }
 
@@ -259,12 +288,24 @@ decode_generic(const DecodeParams p)
     }
 }
 
+// Register-batched loads for fp32 calls whose whole state is at most this
+// many bytes (it can sit in L2 between calls), staged loads otherwise.
+constexpr int64_t kRegPathMaxStateBytes = REG_PATH_MAX_BYTES;
+
 template <typename TS, bool NORM>
 cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
 {
     const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
+    const int64_t state_bytes = (int64_t)p.batch * p.nv * kD * kD * (int64_t)sizeof(TS);
+    if constexpr (sizeof(TS) == 4) {           // fp16 is faster staged at every size measured
+        if (fast && state_bytes <= kRegPathMaxStateBytes) {
+            using F = RegShape<TS>;
+            decode_d128<TS, NORM, false, F::kBatches, F::kMinBlocks><<<grid, kWarps * 32, 0, s>>>(p);
+            return cudaGetLastError();
+        }
+    }
     if (fast) {
-        constexpr auto kern = decode_d128<TS, NORM, FastShape<TS>::kMinBlocks>;
+        constexpr auto kern = decode_d128<TS, NORM, true, 1, StagedShape<TS>::kMinBlocks>;
         const cudaError_t e = allow_dynamic_smem<kern>(stage_bytes<TS>());
         if (e != cudaSuccess) return e;
         kern<<<grid, kWarps * 32, stage_bytes<TS>(), s>>>(p);
