@@ -76,7 +76,7 @@ def parse():
     ap.add_argument("--prefill-tokens", type=int, default=4096,
                     help="tokens per sequence in the prefill row (smaller for profiling; not a bench line)")
     ap.add_argument("--rows-only", default=None,
-                    help="comma list of secondary rows to run (profiling): fp16,conv,latency,prefill")
+                    help="comma list of secondary rows to run (profiling): fp16,conv,latency,prefill,chunk2,convnorm,q8")
     return ap.parse_args()
 
 
@@ -430,7 +430,7 @@ def time_fn(torch, stream, fn, reps, warm=2):
 
 
 def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096, graph=True):
-    want = set(only.split(",")) if only else {"fp16", "conv", "latency", "prefill", "chunk2", "convnorm"}
+    want = set(only.split(",")) if only else {"fp16", "conv", "latency", "prefill", "chunk2", "convnorm", "q8"}
     rows = {}
     torch.cuda.empty_cache()
     if want & {"fp16", "conv"}:
@@ -441,6 +441,8 @@ def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096, graph=
         rows.update(row_chunk2(torch, gdn, dev, stream, pk))
     if "convnorm" in want:
         rows.update(row_conv_norm(torch, gdn, dev, stream, pk))
+    if "q8" in want:
+        rows.update(row_q8(torch, gdn, dev, stream, pk))
     if "prefill" in want:
         rows.update(row_prefill(torch, gdn, dev, stream, pk, prefill_tokens))
     return rows
@@ -473,6 +475,36 @@ def row_conv_norm(torch, gdn, dev, stream, pk, taps=4):
         "config": "B=32 NK=16 NV=48 D=128 fp32, 4-tap conv", "us_per_launch": s * 1e6,
         "token_heads_per_s": B * NV / s, "achieved_gbs": by / s / 1e9,
         "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}}
+
+
+def row_q8(torch, gdn, dev, stream, pk):
+    """Decode + gated norm with the int8 epilogue (groups of 32, one fp32 scale each) on one
+    layer at batch 32 (fp32 state), next to the bf16 epilogue on the same inputs."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(4)
+    S = torch.empty((B, NV, D, D), device=dev).normal_(0.0, 0.02, generator=g)
+    q = torch.randn((B, NK, D), device=dev, generator=g)
+    q = (q / q.norm(dim=-1, keepdim=True)).view(B, NK * D).contiguous()
+    k = torch.randn((B, NK, D), device=dev, generator=g)
+    k = (k / k.norm(dim=-1, keepdim=True)).view(B, NK * D).contiguous()
+    v = torch.randn((B, NV * D), device=dev, generator=g)
+    z = torch.randn((B, NV * D), device=dev, generator=g)
+    a = torch.sigmoid(torch.randn((B, NV), device=dev, generator=g) + 2.0)
+    bt = torch.sigmoid(torch.randn((B, NV), device=dev, generator=g))
+    gn = torch.ones(D, device=dev)
+    xq = torch.empty((B, NV * D), dtype=torch.int8, device=dev)
+    xs = torch.empty((B, NV * D // 32), device=dev)
+    out = torch.empty((B, NV * D), dtype=torch.int16, device=dev)
+    kw = dict(batch=B, nk=NK, nv=NV, d=D, stream=stream.cuda_stream)
+    s_q8 = time_fn(torch, stream, lambda: gdn.gdn_decode_norm_q8(S, q, k, v, a, bt, z, gn, xq, xs, None, **kw), 50)
+    s_bf = time_fn(torch, stream, lambda: gdn.gdn_decode_norm(S, q, k, v, a, bt, z, gn, out, **kw), 50)
+    by = B * NV * D * D * 4 * 2 + B * (2 * NK * D + 2 * NV * D + 2 * NV) * 4 + D * 4 + B * NV * D * (1 + 4 / 32)
+    del S, q, k, v, z, a, bt, gn, xq, xs, out
+    torch.cuda.empty_cache()
+    return {"decode_norm_int8_epilogue": {
+        "config": "B=32 NK=16 NV=48 D=128 fp32, int8 codes + fp32 scale per 32 outputs", "us_per_launch": s_q8 * 1e6,
+        "bf16_epilogue_us_per_launch": s_bf * 1e6, "achieved_gbs": by / s_q8 / 1e9,
+        "frac_of_hbm_peak": by / s_q8 / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}}
 
 
 def row_chunk2(torch, gdn, dev, stream, pk):

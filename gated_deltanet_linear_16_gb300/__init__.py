@@ -23,7 +23,7 @@ __all__ = [
     "GdnError", "load", "build", "library_path",
     "GDN_STATE_F32", "GDN_STATE_F16", "STATUS",
     "gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
-    "gdn_decode_conv_norm_noalloc", "GDN_NOALLOC_MAX_KEY_HEADS",
+    "gdn_decode_conv_norm_noalloc", "GDN_NOALLOC_MAX_KEY_HEADS", "gdn_decode_norm_q8",
     "gdn_h_f32_to_f16", "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error",
 ]
 
@@ -60,6 +60,8 @@ def _declare(lib):
     lib.gdn_decode.argtypes = [P, i32, i64, P, P, P, P, P, P, i32, i32, i32, i32, i64, i64, i64, i64, P]
     lib.gdn_decode_norm.argtypes = [P, i32, i64, P, P, P, P, P, P, P, f32, P, i32, i32, i32, i32,
                                     i64, i64, i64, i64, i64, P]
+    lib.gdn_decode_norm_q8.argtypes = [P, i32, i64, P, P, P, P, P, P, P, f32, P, P, P, i32, i32, i32, i32,
+                                       i64, i64, i64, i64, i64, i64, i64, P]
     lib.gdn_decode_conv_norm.argtypes = [P, i32, i64, P, i64, i32, P, P, P, P, P, P, P, P, f32, f32, P, P,
                                          i32, i32, i32, i32, i64, i64, i64, i64, P]
     lib.gdn_decode_conv_norm_noalloc.argtypes = [P, i32, i64, P, i64, i32, P, P, P, P, P, P, P, P, f32, f32, P,
@@ -71,7 +73,7 @@ def _declare(lib):
     lib.gdn_h_f32_to_f16.argtypes = [P, P, u64, P]
     lib.gdn_h_f16_to_f32.argtypes = [P, P, u64, P]
     for fn in ("gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
-               "gdn_decode_conv_norm_noalloc", "gdn_h_f32_to_f16",
+               "gdn_decode_conv_norm_noalloc", "gdn_decode_norm_q8", "gdn_h_f32_to_f16",
                "gdn_h_f16_to_f32"):
         getattr(lib, fn).restype = i32
     lib.gdn_status_str.argtypes = [i32]
@@ -170,6 +172,29 @@ def gdn_decode_norm(state, q, k, v, alpha, beta, z, gn, out, *, batch, nk, nv, d
         out_stride if out_stride is not None else nv * d,
         _stream(stream))
     _check("gdn_decode_norm", st)
+
+
+def gdn_decode_norm_q8(state, q, k, v, alpha, beta, z, gn, xq, xs, y=None, *, batch, nk, nv, d, eps=1e-6,
+                       state_pitch=None, state_dtype=None, qk_stride=None, v_stride=None, gb_stride=None,
+                       z_stride=None, xq_stride=None, xs_stride=None, y_stride=None, stream=None):
+    """gdn_decode_norm with int8 output groups of 32 (codes xq, fp32 scales xs; y, if given,
+    receives the fp32 normed values).  D must be a multiple of 32."""
+    lib = load()
+    sd = _state_dtype(state, state_dtype)
+    st = lib.gdn_decode_norm_q8(
+        _ptr(state), sd, state_pitch if state_pitch is not None else nv * d * d,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(z), _ptr(gn), float(eps),
+        _ptr(xq), _ptr(xs), _ptr(y) if y is not None else None,
+        batch, nk, nv, d,
+        qk_stride if qk_stride is not None else nk * d,
+        v_stride if v_stride is not None else nv * d,
+        gb_stride if gb_stride is not None else nv,
+        z_stride if z_stride is not None else nv * d,
+        xq_stride if xq_stride is not None else nv * d,
+        xs_stride if xs_stride is not None else nv * d // 32,
+        y_stride if y_stride is not None else nv * d,
+        _stream(stream))
+    _check("gdn_decode_norm_q8", st)
 
 
 def gdn_decode_conv_norm(state, conv_state, x, conv_w, br, ar, dt, rate, z, gn, out, workspace, *, batch, nk,

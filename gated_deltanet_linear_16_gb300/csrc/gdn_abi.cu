@@ -96,26 +96,46 @@ bool vec16(const void *p) { return aligned(p, 16); }
 
 float inv_sqrt(int d) { return (float)(1.0 / std::sqrt((double)d)); }
 
+// What a single-token call writes besides the state: raw fp32 o, the normed
+// output as bf16, or the normed output as int8 groups of 32 (plus, optionally,
+// the fp32 normed values).
+struct Epilogue {
+    int kind;                                   // kEpiRaw, kEpiBf16, kEpiQ8
+    float *o = nullptr;          int64_t o_stride = 0;
+    uint16_t *out = nullptr;     int64_t out_stride = 0;
+    int8_t *xq = nullptr;        int64_t xq_stride = 0;
+    float *xs = nullptr;         int64_t xs_stride = 0;
+    float *y = nullptr;          int64_t y_stride = 0;
+};
+
 int decode_entry(void *state, int state_dtype, int64_t state_pitch,
                  const float *q, const float *k, const float *v,
                  const float *alpha, const float *beta,
                  const float *z, const float *gn, float eps,
-                 float *o, uint16_t *out,
+                 const Epilogue &ep,
                  int batch, int nk, int nv, int d,
                  int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
-                 int64_t z_stride, int64_t o_stride, int64_t out_stride,
-                 bool norm, void *stream)
+                 int64_t z_stride, void *stream)
 {
     int st = check_common(batch, nk, nv, d, state_pitch, state_dtype);
     if (st != GDN_OK) return st;
+    const bool norm = ep.kind != kEpiRaw;
     if (norm && !(eps >= 0.0f && std::isfinite(eps))) return GDN_ERR_ARG;
+    if (ep.kind == kEpiQ8 && d % 32 != 0) return GDN_ERR_UNSUPPORTED;   // groups of 32 inside a head
     const int64_t selem = state_dtype == GDN_STATE_F16 ? 2 : 4;
     const int64_t B = batch, hv = (int64_t)nv * d, hk = (int64_t)nk * d;
-    Operand ops[10];
+    Operand ops[12];
     int n = 0;
     ops[n++] = {state, B, (int64_t)nv * d * d, state_pitch, selem};
-    if (norm) ops[n++] = {out, B, hv, out_stride, 2};
-    else ops[n++] = {o, B, hv, o_stride, 4};
+    if (ep.kind == kEpiBf16) {
+        ops[n++] = {ep.out, B, hv, ep.out_stride, 2};
+    } else if (ep.kind == kEpiQ8) {
+        ops[n++] = {ep.xq, B, hv, ep.xq_stride, 1};
+        ops[n++] = {ep.xs, B, hv / 32, ep.xs_stride, 4};
+        if (ep.y != nullptr) ops[n++] = {ep.y, B, hv, ep.y_stride, 4};
+    } else {
+        ops[n++] = {ep.o, B, hv, ep.o_stride, 4};
+    }
     const int n_out = n;
     ops[n++] = {q, B, hk, qk_stride, 4};
     ops[n++] = {k, B, hk, qk_stride, 4};
@@ -137,9 +157,11 @@ int decode_entry(void *state, int state_dtype, int64_t state_pitch,
     DecodeParams p{};
     p.state = state; p.pitch = state_pitch;
     p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
-    p.z = z; p.gn = gn; p.o = o; p.out = out;
+    p.z = z; p.gn = gn; p.o = ep.o; p.out = ep.out;
+    p.xq = ep.xq; p.xs = ep.xs; p.y = ep.y;
     p.qk_stride = qk_stride; p.v_stride = v_stride; p.gb_stride = gb_stride;
-    p.z_stride = z_stride; p.o_stride = o_stride; p.out_stride = out_stride;
+    p.z_stride = z_stride; p.o_stride = ep.o_stride; p.out_stride = ep.out_stride;
+    p.xq_stride = ep.xq_stride; p.xs_stride = ep.xs_stride; p.y_stride = ep.y_stride;
     p.batch = batch; p.nk = nk; p.nv = nv; p.d = d;
     p.eps = eps; p.inv_sqrt_d = inv_sqrt(d);
 
@@ -147,7 +169,7 @@ int decode_entry(void *state, int state_dtype, int64_t state_pitch,
     // (v, z, gn, alpha, beta, o and out are read/written as scalars.)
     const bool fast = d == 128 && vec16(state) && (state_pitch * selem) % 16 == 0 &&
                       vec16(q) && vec16(k) && (qk_stride * 4) % 16 == 0;
-    return cuda_status(launch_decode(p, state_dtype == GDN_STATE_F16, norm, fast, (cudaStream_t)stream));
+    return cuda_status(launch_decode(p, state_dtype == GDN_STATE_F16, ep.kind, fast, (cudaStream_t)stream));
 }
 
 }  // namespace
@@ -167,9 +189,10 @@ GDN_API int gdn_decode(void *state, int state_dtype, int64_t state_pitch,
                        int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
                        int64_t o_stride, void *stream)
 {
+    Epilogue ep{kEpiRaw};
+    ep.o = o; ep.o_stride = o_stride;
     return decode_entry(state, state_dtype, state_pitch, q, k, v, alpha, beta, nullptr, nullptr, 0.0f,
-                        o, nullptr, batch, nk, nv, d, qk_stride, v_stride, gb_stride, 0, o_stride, 0,
-                        false, stream);
+                        ep, batch, nk, nv, d, qk_stride, v_stride, gb_stride, 0, stream);
 }
 
 GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
@@ -181,9 +204,28 @@ GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
                             int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
                             int64_t z_stride, int64_t out_stride, void *stream)
 {
+    Epilogue ep{kEpiBf16};
+    ep.out = out; ep.out_stride = out_stride;
     return decode_entry(state, state_dtype, state_pitch, q, k, v, alpha, beta, z, gn, eps,
-                        nullptr, out, batch, nk, nv, d, qk_stride, v_stride, gb_stride, z_stride, 0,
-                        out_stride, true, stream);
+                        ep, batch, nk, nv, d, qk_stride, v_stride, gb_stride, z_stride, stream);
+}
+
+GDN_API int gdn_decode_norm_q8(void *state, int state_dtype, int64_t state_pitch,
+                               const float *q, const float *k, const float *v,
+                               const float *alpha, const float *beta,
+                               const float *z, const float *gn, float eps,
+                               int8_t *xq, float *xs, float *y,
+                               int batch, int nk, int nv, int d,
+                               int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                               int64_t z_stride, int64_t xq_stride, int64_t xs_stride,
+                               int64_t y_stride, void *stream)
+{
+    Epilogue ep{kEpiQ8};
+    ep.xq = xq; ep.xq_stride = xq_stride;
+    ep.xs = xs; ep.xs_stride = xs_stride;
+    ep.y = y; ep.y_stride = y_stride;
+    return decode_entry(state, state_dtype, state_pitch, q, k, v, alpha, beta, z, gn, eps,
+                        ep, batch, nk, nv, d, qk_stride, v_stride, gb_stride, z_stride, stream);
 }
 
 GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pitch,

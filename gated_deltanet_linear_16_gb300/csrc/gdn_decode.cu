@@ -32,8 +32,11 @@
 //    warp, not per row.
 #include "gdn_internal.cuh"
 
-#ifndef REG_PATH_MAX_BYTES
-#define REG_PATH_MAX_BYTES (int64_t{32} << 20)
+#ifndef STAGED_MIN_CTAS_PER_SM
+#define STAGED_MIN_CTAS_PER_SM 8
+#endif
+#ifndef DECODE_PATH_FORCE
+#define DECODE_PATH_FORCE -1
 #endif
 
 namespace gdn {
@@ -43,32 +46,32 @@ constexpr int kD = 128;
 
 // ------------------------------------------------------------------ D == 128
 
-// Two ways to bring a lane's 16 (fp32) or 8 (fp16) state vectors in, both with
-// 8 warps x 16 rows per head and the same arithmetic (bitwise-identical
+// Three ways to bring a lane's 16 (fp32) or 8 (fp16) state vectors in, all
+// with 8 warps x 16 rows per head and the same arithmetic (bitwise-identical
 // results):
 //  * staged: every load in flight at once through cp.async into shared memory
 //    (64 KB fp32 / 32 KB fp16 per CTA), four commit groups each consumed as it
 //    lands.  The loads hold no registers while in flight, so 3 (fp32) or 4
-//    (fp16) CTAs per SM keep 128-192 KB outstanding per SM: best when the state
-//    streams from HBM;
-//  * register-batched: NB batches of loads straight into registers, batch b + 1
-//    in flight while batch b is computed: one hop less per element, which wins
-//    when the state is close (a small call whose state sits in L2).
-// The launcher picks one per call; the shapes and the choice come from
-// measurement on GB300.
+//    (fp16) CTAs per SM keep 128-192 KB outstanding per SM: for large calls;
+//  * register batches (NB > 1): batch b + 1 in flight while batch b is
+//    computed, one hop less per element than staging;
+//  * all in registers (NB == 1): every load in flight at once, for grids of at
+//    most one CTA per SM, where occupancy does not matter.
+// The launcher picks one per call (pick_path below).
 constexpr int kWarps = 8;
 constexpr int kGroups = 4;                     // cp.async commit groups per lane (staged)
 template <typename TS> struct StagedShape { static constexpr int kMinBlocks = 3; };
 template <> struct StagedShape<__half> { static constexpr int kMinBlocks = 4; };
-template <typename TS> struct RegShape { static constexpr int kBatches = 4, kMinBlocks = 3; };
+template <typename TS> struct RegShape { static constexpr int kBatches = 4, kMinBlocks = 3; };   // fp32 only
 
 template <typename TS>
 constexpr int stage_bytes() { return kD * kD * (int)sizeof(TS); }
 
-template <typename TS, bool NORM, bool STAGED, int NB, int MINB>
+template <typename TS, int EPI, bool STAGED, int NB, int MINB>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
 decode_d128(const DecodeParams p)
 {
+    constexpr bool NORM = EPI != kEpiRaw;
     using V = Vec16<TS>;
     constexpr int EPV = V::N;                  // state elements per 16-byte vector
     constexpr int LPR = kD / EPV;              // lanes per state row: 32 fp32, 16 fp16
@@ -195,9 +198,24 @@ decode_d128(const DecodeParams p)
 #pragma unroll
         for (int i = 0; i < kWarps; ++i) tot += red[i];
         const float rstd = rsqrtf(tot * (1.0f / kD) + p.eps);
-        if (row_lane) {
-            const float y = gn_l * o_keep * rstd * silu(z_l);
-            p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
+        if constexpr (EPI == kEpiBf16) {
+            if (row_lane) {
+                const float y = gn_l * o_keep * rstd * silu(z_l);
+                p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
+            }
+        } else {
+            // int8 groups of 32: a group spans two warps' rows, so the normed
+            // values meet in shared memory and warp w < 4 quantises group w.
+            __shared__ float y_s[kD];
+            if (row_lane) {
+                const float y = gn_l * o_keep * rstd * silu(z_l);
+                y_s[row0 + lane] = y;
+                if (p.y != nullptr) p.y[seq * p.y_stride + (int64_t)h * kD + row0 + lane] = y;
+            }
+            __syncthreads();
+            if (warp < kD / 32)
+                quant_group32(y_s[32 * warp + lane], p.xq + seq * p.xq_stride + (int64_t)h * kD + 32 * warp + lane,
+                              p.xs + seq * p.xs_stride + (int64_t)h * (kD / 32) + warp, lane);
         }
     }
 }
@@ -211,10 +229,11 @@ decode_d128(const DecodeParams p)
 constexpr int kGenWarps = 4;
 constexpr int kMaxD = 256;
 
-template <typename TS, bool NORM>
+template <typename TS, int EPI>
 __global__ void __launch_bounds__(kGenWarps * 32)
 decode_generic(const DecodeParams p)
 {
+    constexpr bool NORM = EPI != kEpiRaw;
     constexpr int MAXV = kMaxD / 32;
     __shared__ float o_s[kMaxD];
     __shared__ float red[kGenWarps];
@@ -282,47 +301,95 @@ decode_generic(const DecodeParams p)
         for (int i = 0; i < kGenWarps; ++i) tot += red[i];
         const float rstd = rsqrtf(tot / (float)D + p.eps);
         const float *zp = p.z + seq * p.z_stride + (int64_t)h * D;
-        uint16_t *op = p.out + seq * p.out_stride + (int64_t)h * D;
-        for (int a = threadIdx.x; a < D; a += kGenWarps * 32)
-            op[a] = bf16_bits_rn(p.gn[a] * o_s[a] * rstd * silu(zp[a]));
+        for (int a = threadIdx.x; a < D; a += kGenWarps * 32) {
+            const float y = p.gn[a] * o_s[a] * rstd * silu(zp[a]);
+            if constexpr (EPI == kEpiBf16) {
+                p.out[seq * p.out_stride + (int64_t)h * D + a] = bf16_bits_rn(y);
+            } else {
+                o_s[a] = y;                    // this thread's own entry
+                if (p.y != nullptr) p.y[seq * p.y_stride + (int64_t)h * D + a] = y;
+            }
+        }
+        if constexpr (EPI == kEpiQ8) {        // D % 32 == 0 (checked on the host)
+            __syncthreads();
+            for (int grp = warp; grp < D / 32; grp += kGenWarps)
+                quant_group32(o_s[32 * grp + lane], p.xq + seq * p.xq_stride + (int64_t)h * D + 32 * grp + lane,
+                              p.xs + seq * p.xs_stride + (int64_t)h * (D / 32) + grp, lane);
+        }
     }
 }
 
-// Register-batched loads for fp32 calls whose whole state is at most this
-// many bytes (it can sit in L2 between calls), staged loads otherwise.
-constexpr int64_t kRegPathMaxStateBytes = REG_PATH_MAX_BYTES;
+// Which of the D == 128 variants a call takes, from per-launch times measured
+// on GB300 for batch 1..32 (NV = 48), fp32 and fp16, with the state in L2 (one
+// layer repeated) and streaming from HBM (48 distinct layers):
+//  * grid <= one CTA per SM (latency-bound, occupancy moot): every load of a
+//    lane in flight at once, in registers.  Best for fp16 in both cases; for
+//    fp32 within 8 % of the best in both (register batches are 8 % faster from
+//    L2 but 11 % slower from HBM, staging the reverse);
+//  * fp32 up to kStagedMinCtasPerSm CTAs per SM: register batches;
+//  * otherwise staged.
+enum class Path { kRegAll, kRegBatched, kStaged };
+constexpr int kStagedMinCtasPerSm = STAGED_MIN_CTAS_PER_SM;
 
-template <typename TS, bool NORM>
+template <typename TS>
+Path pick_path(unsigned grid)
+{
+#if DECODE_PATH_FORCE >= 0
+    (void)grid;
+    return static_cast<Path>(DECODE_PATH_FORCE);
+#else
+    const unsigned sms = (unsigned)sm_count();
+    if (grid <= sms) return Path::kRegAll;
+    if (sizeof(TS) == 4 && grid < (unsigned)kStagedMinCtasPerSm * sms) return Path::kRegBatched;
+    return Path::kStaged;
+#endif
+}
+
+template <typename TS, int EPI>
 cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
 {
     const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
-    const int64_t state_bytes = (int64_t)p.batch * p.nv * kD * kD * (int64_t)sizeof(TS);
-    if constexpr (sizeof(TS) == 4) {           // fp16 is faster staged at every size measured
-        if (fast && state_bytes <= kRegPathMaxStateBytes) {
-            using F = RegShape<TS>;
-            decode_d128<TS, NORM, false, F::kBatches, F::kMinBlocks><<<grid, kWarps * 32, 0, s>>>(p);
-            return cudaGetLastError();
-        }
+    if (!fast) {
+        decode_generic<TS, EPI><<<grid, kGenWarps * 32, 0, s>>>(p);
+        return cudaGetLastError();
     }
-    if (fast) {
-        constexpr auto kern = decode_d128<TS, NORM, true, 1, StagedShape<TS>::kMinBlocks>;
+    switch (pick_path<TS>(grid)) {
+    case Path::kRegAll:
+        decode_d128<TS, EPI, false, 1, 1><<<grid, kWarps * 32, 0, s>>>(p);
+        break;
+    case Path::kRegBatched:
+        if constexpr (sizeof(TS) == 4) {
+            decode_d128<TS, EPI, false, RegShape<TS>::kBatches, RegShape<TS>::kMinBlocks>
+                <<<grid, kWarps * 32, 0, s>>>(p);
+            break;
+        }
+        [[fallthrough]];
+    default: {
+        constexpr auto kern = decode_d128<TS, EPI, true, 1, StagedShape<TS>::kMinBlocks>;
         const cudaError_t e = allow_dynamic_smem<kern>(stage_bytes<TS>());
         if (e != cudaSuccess) return e;
         kern<<<grid, kWarps * 32, stage_bytes<TS>(), s>>>(p);
-    } else {
-        decode_generic<TS, NORM><<<grid, kGenWarps * 32, 0, s>>>(p);
+    }
     }
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams &p, bool f16_state, bool norm, bool fast, cudaStream_t s)
+cudaError_t launch_decode(const DecodeParams &p, bool f16_state, int epi, bool fast, cudaStream_t s)
 {
     if (f16_state) {
-        return norm ? launch_typed<__half, true>(p, fast, s) : launch_typed<__half, false>(p, fast, s);
+        switch (epi) {
+        case kEpiRaw: return launch_typed<__half, kEpiRaw>(p, fast, s);
+        case kEpiBf16: return launch_typed<__half, kEpiBf16>(p, fast, s);
+        default: return launch_typed<__half, kEpiQ8>(p, fast, s);
+        }
     }
-    return norm ? launch_typed<float, true>(p, fast, s) : launch_typed<float, false>(p, fast, s);
+    switch (epi) {
+    case kEpiRaw: return launch_typed<float, kEpiRaw>(p, fast, s);
+    case kEpiBf16: return launch_typed<float, kEpiBf16>(p, fast, s);
+    default: return launch_typed<float, kEpiQ8>(p, fast, s);
+    }
 }
 
 }  // namespace gdn

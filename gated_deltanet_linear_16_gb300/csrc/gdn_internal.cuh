@@ -30,7 +30,16 @@ struct DecodeParams {
     // Token rows are then b * 2 + t for q, k, v, alpha, beta and o.
     void *state_mid;
     int64_t mid_pitch;
+    // int8 epilogue only: codes [batch][nv*d], group scales [batch][nv*d/32],
+    // and (nullable) the fp32 normed values [batch][nv*d]; row strides in elements.
+    int8_t *xq;
+    float *xs, *y;
+    int64_t xq_stride, xs_stride, y_stride;
 };
+
+// What the single-token kernels write after the step: raw o, the normed output
+// as bf16, or the normed output as int8 groups of 32.
+constexpr int kEpiRaw = 0, kEpiBf16 = 1, kEpiQ8 = 2;
 
 struct PrefillParams {
     void *state;            // float* or __half*
@@ -67,7 +76,7 @@ struct ConvNormParams {
 // Launchers (one per translation unit family).  They pick the kernel variant
 // (fast D == 128 path when the alignment allows it, general otherwise) and
 // return the launch status.
-cudaError_t launch_decode(const DecodeParams &p, bool f16_state, bool norm, bool fast, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams &p, bool f16_state, int epi, bool fast, cudaStream_t s);
 cudaError_t launch_decode_chunk2(const DecodeParams &p, bool f16_state, bool fast, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, bool f16_state, bool fast, cudaStream_t s);
 cudaError_t launch_conv_norm(const ConvNormParams &p, bool f16_state, bool fast, cudaStream_t s);
@@ -127,6 +136,19 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z));
 __device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
     __nv_bfloat16 b = __float2bfloat16_rn(x);
     return *reinterpret_cast<uint16_t *>(&b);
+}
+
+// One group of 32 values, one per lane of a warp, to int8 codes and a scale
+// (logicaffeine_compile/codegen_cuda/gdn.rs, kernel `gdn_gate_norm_q`): scale =
+// max |y| / 127 over the group (1 if all zero), code = y / scale rounded to the
+// nearest integer, ties to even.  Both divisions are IEEE fp32 divisions.
+__device__ __forceinline__ void quant_group32(float yv, int8_t *code, float *scale, int lane) {
+    float am = fabsf(yv);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, off));
+    const float sc = am > 0.f ? am / 127.0f : 1.0f;
+    *code = (int8_t)__float2int_rn(yv / sc);
+    if (lane == 0) *scale = sc;
 }
 
 // cp.async (global -> shared, bypassing L1) and its hardware group waits.

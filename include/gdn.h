@@ -119,6 +119,36 @@ GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
                             int64_t z_stride, int64_t out_stride, void *stream);
 
 /*
+ * gdn_decode_norm_q8 -- gdn_decode_norm with the activation quantisation of
+ * the o-projection's input fused in: the normed output leaves as int8 codes
+ * in groups of 32 with one fp32 scale per group.
+ *   Defined by: gdn.rs, kernel `gdn_gate_norm_q` (the gate norm, then per
+ *   32-value group: scale = max |y| / 127, or 1 when the group is all zero;
+ *   code = y / scale rounded to the nearest integer, ties to even; computed in
+ *   fp32); the step and the norm as gdn_decode_norm.
+ *   Groups are 32 consecutive values of a token's NV*D output vector, so a
+ *   head holds D/32 of them; D must be a multiple of 32
+ *   (GDN_ERR_UNSUPPORTED otherwise).
+ *   xq           [batch] rows of NV*D int8 codes, written; row stride
+ *                xq_stride elements (bytes).
+ *   xs           [batch] rows of NV*D/32 fp32 scales, written; row stride
+ *                xs_stride elements.
+ *   y            NULL, or [batch] rows of NV*D fp32: the normed values the
+ *                codes were taken from, written; row stride y_stride.
+ *   Other arguments and errors as gdn_decode_norm (xq, xs and y overlapping
+ *   any operand: GDN_ERR_ALIAS).
+ */
+GDN_API int gdn_decode_norm_q8(void *state, int state_dtype, int64_t state_pitch,
+                               const float *q, const float *k, const float *v,
+                               const float *alpha, const float *beta,
+                               const float *z, const float *gn, float eps,
+                               int8_t *xq, float *xs, float *y,
+                               int batch, int nk, int nv, int d,
+                               int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                               int64_t z_stride, int64_t xq_stride, int64_t xs_stride,
+                               int64_t y_stride, void *stream);
+
+/*
  * gdn_decode_conv_norm -- one token from the projection outputs to the normed
  * bf16 output in one launch: the depthwise causal conv ring update with silu
  * on q, k and v, the per-head L2 normalisation of q and k, the gates from

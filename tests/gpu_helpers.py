@@ -17,6 +17,7 @@ import oracle
 GUARD = 256                      # elements of sentinel before and after every buffer
 SENT32 = np.int32(0x7FBADBAD)    # quiet-NaN bit pattern
 SENT16 = np.int16(0x7DAD)        # binary16 / bf16 NaN bit pattern
+SENT8 = 0x5A                     # int8 codes: a value the tests never expect in padding
 
 # Parity bars (stated for the method): fp32 results within 1e-4 of the largest
 # reference magnitude; fp16 state and bf16 output within 2e-2 relative L2.
@@ -49,7 +50,7 @@ def bf16_to_f64(bits):
 class Rows:
     """`rows` rows of `length` elements, `stride` apart, inside a guarded device buffer.
 
-    dtype is a torch dtype (float32, float16 or int16 for bf16 bits).  Padding
+    dtype is a torch dtype (float32, float16, int16 for bf16 bits, or int8).  Padding
     between rows and the guard bands hold the sentinel.  `misalign` shifts the
     payload by that many elements (to force the general kernels)."""
 
@@ -60,10 +61,14 @@ class Rows:
         self.nelem = (rows - 1) * self.stride + length if rows > 0 else 0
         self.off = GUARD + misalign
         total = self.off + self.nelem + GUARD
-        ibits = torch.int32 if dtype == torch.float32 else torch.int16
-        sent = int(SENT32) if dtype == torch.float32 else int(SENT16)
+        if dtype == torch.float32:
+            ibits, sent = torch.int32, int(SENT32)
+        elif dtype == torch.int8:
+            ibits, sent = torch.int8, SENT8
+        else:
+            ibits, sent = torch.int16, int(SENT16)
         self.raw = torch.full((total,), sent, dtype=ibits, device="cuda")
-        self.buf = self.raw.view(dtype) if dtype != torch.int16 else self.raw
+        self.buf = self.raw.view(dtype) if dtype not in (torch.int16, torch.int8) else self.raw
         self.sentinel = sent
         self.ibits = ibits
 

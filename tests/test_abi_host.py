@@ -41,7 +41,8 @@ def lib(built):
 def test_exports_match_header(built):
     want = declared_symbols()
     assert want == sorted(["gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm",
-                           "gdn_decode_conv_norm_noalloc", "gdn_prefill_seq", "gdn_h_f32_to_f16",
+                           "gdn_decode_conv_norm_noalloc", "gdn_decode_norm_q8", "gdn_prefill_seq",
+                           "gdn_h_f32_to_f16",
                            "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error"])
     out = subprocess.run(["nm", "-D", "--defined-only", gdn.library_path()], capture_output=True, text=True,
                          check=True).stdout
@@ -199,6 +200,36 @@ def test_decode_empty_batch_is_ok(lib):
 ])
 def test_decode_norm_rejects(lib, kw, want):
     assert decode_norm(lib, **kw) == want
+
+
+def decode_norm_q8(lib, **kw):
+    a = dict(state=A, dt=0, pitch=2 * 64 * 64, q=A + (1 << 30), k=A + (2 << 30), v=A + (3 << 30),
+             alpha=A + (4 << 30), beta=A + (5 << 30), z=A + (7 << 30), gn=A + (8 << 30), eps=1e-6,
+             xq=A + (6 << 30), xs=A + (9 << 30), y=A + (10 << 30), batch=2, nk=1, nv=2, d=64, qk=64, vs=128,
+             gb=2, zs=128, xqs=128, xss=4, ys=128)
+    a.update(kw)
+    return lib.gdn_decode_norm_q8(a["state"], a["dt"], a["pitch"], a["q"], a["k"], a["v"], a["alpha"],
+                                  a["beta"], a["z"], a["gn"], a["eps"], a["xq"], a["xs"], a["y"], a["batch"],
+                                  a["nk"], a["nv"], a["d"], a["qk"], a["vs"], a["gb"], a["zs"], a["xqs"],
+                                  a["xss"], a["ys"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(d=48, pitch=2 * 48 * 48, qk=48, vs=96, zs=96, xqs=96, xss=3, ys=96), UNSUP),   # D % 32 != 0
+    (dict(xq=None), ARG), (dict(xs=None), ARG), (dict(xss=3), ARG), (dict(xqs=127), ARG),
+    (dict(eps=-1.0), ARG), (dict(xs=A + (9 << 30) + 2), ALIGN),
+    (dict(xq=A + (9 << 30) + 8), ALIAS),                # codes over the scales
+    (dict(y=A + 64), ALIAS),                            # normed values inside the state
+    (dict(xs=A + (3 << 30)), ALIAS),                    # scales over v
+])
+def test_decode_norm_q8_rejects(lib, kw, want):
+    assert decode_norm_q8(lib, **kw) == want
+
+
+def test_decode_norm_q8_empty_and_optional_y(lib):
+    assert decode_norm_q8(lib, batch=0) == OK
+    assert decode_norm_q8(lib, batch=0, y=None) == OK
+    assert decode_norm_q8(lib, batch=0, xq=None) == ARG
 
 
 @pytest.mark.parametrize("kw,want", [
