@@ -54,9 +54,9 @@ REF_LAYERS_PER_STEP = 4      # oracle sample per step of the reference arm
 # dram__bytes_write.sum), valid only while the kernel source is the one it was taken on.
 NCU_TRAFFIC = {
     # mean of three mid-sequence launches of the full 48-layer workload, ncu --cache-control none
-    # (reads 102.8 MB, writes 96.2-99.7 MB); see profiles/decode_d128_f32_norm_batched48.md
-    "decode_norm_f32": {"bytes_per_launch": 201139200,
-                        "src_sha256": "0f48ccb0c5b56683cd3de2e92f6aaee2429e8e5ecfa6648f5ceb90f10e0dfc71"},
+    # (reads 102.8 MB, writes 96.4-99.6 MB); see profiles/decode_d128_f32_norm_batched48.md
+    "decode_norm_f32": {"bytes_per_launch": 201224618,
+                        "src_sha256": "b18e453a10e1cf9d478d29f9cfc73fd90ebe9df0111a69308e2ffd3de9879993"},
 }
 
 
