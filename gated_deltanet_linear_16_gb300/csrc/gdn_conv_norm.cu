@@ -22,8 +22,9 @@
 //    channels) from the ring as it was, without writing it, and keeps the
 //    shifted rows in shared memory;
 //  * after reading, a CTA counts itself in a per-(sequence, key head) counter
-//    (fence + atomic add); the CTA that completes the count is the last reader
-//    of those ring rows, so it writes them and resets the counter to zero.
+//    (fence + atomic add, by a thread with no global stores to drain, its
+//    result read only after the step); the CTA that completes the count is the
+//    last reader of those ring rows, so it writes them and resets the counter.
 // No barrier spans CTAs and nothing spins.  (Thread-block clusters, tried
 // first for this exchange, cost ~30 % on GB300: co-scheduling the cluster's
 // CTAs left SM slots idle.)
@@ -174,11 +175,13 @@ conv_norm_d128(const ConvNormParams p)
     }
     if (tid == 0) gates(p, seq, h, gate_s[0], gate_s[1]);
     __syncthreads();                                     // this CTA is done reading the q/k ring rows
-    if (tid == 0) {
+    // The count is taken by a q/k producer thread (it has no global stores for
+    // its fence to drain); its result is needed only after the step.
+    constexpr int kCounter = kWarps * 32 - 1;
+    int seen = 0;
+    if (tid == kCounter) {
         __threadfence();                                 // the reads above come before the count
-        const int seen = atomicAdd(p.counters + cl, 1);
-        last_reader = seen == p.repeat - 1;
-        if (last_reader) __threadfence();                // every other reader's count came first
+        seen = atomicAdd(p.counters + cl, 1);
     }
 
     float kx[EPV], qx[EPV];
@@ -252,6 +255,11 @@ conv_norm_d128(const ConvNormParams p)
     // 5. gated RMS norm over the head's outputs
     const float ss = group_sum<32>(o_keep * o_keep);
     if (lane == 0) red[warp] = ss;
+    if (tid == kCounter) {
+        const bool last = seen == p.repeat - 1;
+        if (last) __threadfence();                       // every other reader's count came first
+        last_reader = last;
+    }
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
