@@ -6,8 +6,10 @@
 // and destination must not alias.
 //
 // Pure HBM streams (6 bytes per element either way).  The vector kernels move
-// 8 elements per thread per step (two 16-byte fp32 vectors <-> one 16-byte
-// fp16 vector) and keep 4 steps in flight per thread; the grid is a whole
+// 4 elements per thread per step -- one 16-byte fp32 vector <-> one 8-byte
+// fp16 vector -- so every warp-wide load and store covers one contiguous span
+// (512 B of fp32, 256 B of fp16) and no store leaves part of a sector for a
+// later instruction; 8 steps are in flight per thread.  The grid is a whole
 // number of waves (4 CTAs of 256 threads per SM), and the few elements past
 // the last full vector are done by the first threads.  Unaligned pointers take
 // a scalar grid-stride kernel with the same results.
@@ -18,7 +20,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kCtasPerSm = 4;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 
 __device__ __forceinline__ unsigned pack_h2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
@@ -32,39 +34,27 @@ __device__ __forceinline__ float2 unpack_h2(unsigned u) {
 __global__ void __launch_bounds__(kThreads)
 f32_to_f16_vec(const float *__restrict__ src, uint16_t *__restrict__ dst, uint64_t n)
 {
-    const uint64_t nvec = n / 8;
+    const uint64_t nvec = n / 4;
     const uint64_t stride = (uint64_t)gridDim.x * kThreads;
     const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
     const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    uint2 *d2 = reinterpret_cast<uint2 *>(dst);
     uint64_t i = tid;
     for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
-        uint4 a[kUnroll], b[kUnroll];
+        uint4 a[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            a[u] = __ldcs(s4 + 2 * (i + u * stride));
-            b[u] = __ldcs(s4 + 2 * (i + u * stride) + 1);
-        }
+        for (int u = 0; u < kUnroll; ++u) a[u] = __ldcs(s4 + i + u * stride);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            uint4 r;
-            r.x = pack_h2(__uint_as_float(a[u].x), __uint_as_float(a[u].y));
-            r.y = pack_h2(__uint_as_float(a[u].z), __uint_as_float(a[u].w));
-            r.z = pack_h2(__uint_as_float(b[u].x), __uint_as_float(b[u].y));
-            r.w = pack_h2(__uint_as_float(b[u].z), __uint_as_float(b[u].w));
-            __stcs(d4 + i + u * stride, r);
-        }
+        for (int u = 0; u < kUnroll; ++u)
+            __stcs(d2 + i + u * stride, make_uint2(pack_h2(__uint_as_float(a[u].x), __uint_as_float(a[u].y)),
+                                                   pack_h2(__uint_as_float(a[u].z), __uint_as_float(a[u].w))));
     }
     for (; i < nvec; i += stride) {
-        const uint4 a = __ldcs(s4 + 2 * i), b = __ldcs(s4 + 2 * i + 1);
-        uint4 r;
-        r.x = pack_h2(__uint_as_float(a.x), __uint_as_float(a.y));
-        r.y = pack_h2(__uint_as_float(a.z), __uint_as_float(a.w));
-        r.z = pack_h2(__uint_as_float(b.x), __uint_as_float(b.y));
-        r.w = pack_h2(__uint_as_float(b.z), __uint_as_float(b.w));
-        __stcs(d4 + i, r);
+        const uint4 a = __ldcs(s4 + i);
+        __stcs(d2 + i, make_uint2(pack_h2(__uint_as_float(a.x), __uint_as_float(a.y)),
+                                  pack_h2(__uint_as_float(a.z), __uint_as_float(a.w))));
     }
-    const uint64_t tail = nvec * 8 + tid;
+    const uint64_t tail = nvec * 4 + tid;
     if (tail < n) {
         __half h = __float2half_rn(src[tail]);
         dst[tail] = *reinterpret_cast<uint16_t *>(&h);
@@ -74,35 +64,30 @@ f32_to_f16_vec(const float *__restrict__ src, uint16_t *__restrict__ dst, uint64
 __global__ void __launch_bounds__(kThreads)
 f16_to_f32_vec(const uint16_t *__restrict__ src, float *__restrict__ dst, uint64_t n)
 {
-    const uint64_t nvec = n / 8;
+    const uint64_t nvec = n / 4;
     const uint64_t stride = (uint64_t)gridDim.x * kThreads;
     const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    const uint2 *s2 = reinterpret_cast<const uint2 *>(src);
     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
     uint64_t i = tid;
     for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
-        uint4 a[kUnroll];
+        uint2 a[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) a[u] = __ldcs(s4 + i + u * stride);
+        for (int u = 0; u < kUnroll; ++u) a[u] = __ldcs(s2 + i + u * stride);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const float2 x0 = unpack_h2(a[u].x), x1 = unpack_h2(a[u].y);
-            const float2 x2 = unpack_h2(a[u].z), x3 = unpack_h2(a[u].w);
-            __stcs(d4 + 2 * (i + u * stride), make_uint4(__float_as_uint(x0.x), __float_as_uint(x0.y),
-                                                         __float_as_uint(x1.x), __float_as_uint(x1.y)));
-            __stcs(d4 + 2 * (i + u * stride) + 1, make_uint4(__float_as_uint(x2.x), __float_as_uint(x2.y),
-                                                             __float_as_uint(x3.x), __float_as_uint(x3.y)));
+            __stcs(d4 + i + u * stride, make_uint4(__float_as_uint(x0.x), __float_as_uint(x0.y),
+                                                   __float_as_uint(x1.x), __float_as_uint(x1.y)));
         }
     }
     for (; i < nvec; i += stride) {
-        const uint4 a = __ldcs(s4 + i);
-        const float2 x0 = unpack_h2(a.x), x1 = unpack_h2(a.y), x2 = unpack_h2(a.z), x3 = unpack_h2(a.w);
-        __stcs(d4 + 2 * i, make_uint4(__float_as_uint(x0.x), __float_as_uint(x0.y),
-                                      __float_as_uint(x1.x), __float_as_uint(x1.y)));
-        __stcs(d4 + 2 * i + 1, make_uint4(__float_as_uint(x2.x), __float_as_uint(x2.y),
-                                          __float_as_uint(x3.x), __float_as_uint(x3.y)));
+        const uint2 a = __ldcs(s2 + i);
+        const float2 x0 = unpack_h2(a.x), x1 = unpack_h2(a.y);
+        __stcs(d4 + i, make_uint4(__float_as_uint(x0.x), __float_as_uint(x0.y),
+                                  __float_as_uint(x1.x), __float_as_uint(x1.y)));
     }
-    const uint64_t tail = nvec * 8 + tid;
+    const uint64_t tail = nvec * 4 + tid;
     if (tail < n) {
         __half h = *reinterpret_cast<const __half *>(src + tail);
         dst[tail] = __half2float(h);
@@ -142,14 +127,14 @@ unsigned grid_for(uint64_t work_items)
 
 cudaError_t launch_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, bool vec, cudaStream_t s)
 {
-    if (vec) f32_to_f16_vec<<<grid_for(n / 8 > 0 ? n / 8 : n), kThreads, 0, s>>>(src, dst, n);
+    if (vec) f32_to_f16_vec<<<grid_for(n / 4 > 0 ? n / 4 : n), kThreads, 0, s>>>(src, dst, n);
     else f32_to_f16_scalar<<<grid_for(n), kThreads, 0, s>>>(src, dst, n);
     return cudaGetLastError();
 }
 
 cudaError_t launch_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, bool vec, cudaStream_t s)
 {
-    if (vec) f16_to_f32_vec<<<grid_for(n / 8 > 0 ? n / 8 : n), kThreads, 0, s>>>(src, dst, n);
+    if (vec) f16_to_f32_vec<<<grid_for(n / 4 > 0 ? n / 4 : n), kThreads, 0, s>>>(src, dst, n);
     else f16_to_f32_scalar<<<grid_for(n), kThreads, 0, s>>>(src, dst, n);
     return cudaGetLastError();
 }
