@@ -671,10 +671,19 @@ def cpu_baseline(sample_layers=None, budget_s=8.0):
         spent += time.perf_counter() - t0
         done_heads += B * NV
         layers += 1
+    # the same oracle on one thread, over one layer
+    S0, (x, gn) = _oracle_inputs(0)
+    S1 = S0.copy()
+    t0 = time.perf_counter()
+    o = oracle.decode(S1, x["q"], x["k"], x["v"], x["alpha"], x["beta"], NK)
+    oracle.gated_rmsnorm(o.reshape(-1, D), x["z"].reshape(-1, D), gn, EPS)
+    one = time.perf_counter() - t0
     return {"value": done_heads / spent, "unit": UNIT, "cores": len(chunks), "kind": "oracle",
             "seconds": spent,
             "sample": f"{layers} of 48 layers x 32 sequences x 48 heads ({done_heads} token-heads), "
-                      f"decode + gated norm, fp64 C oracle on {len(chunks)} host threads"}
+                      f"decode + gated norm, fp64 C oracle on {len(chunks)} host threads",
+            "single_thread": {"value": B * NV / one, "unit": UNIT, "cores": 1,
+                              "sample": "1 layer x 32 sequences x 48 heads on 1 host thread"}}
 
 
 def run_reference(args, rank, world):
