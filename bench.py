@@ -449,32 +449,42 @@ def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096, graph=
 
 
 def row_conv_norm(torch, gdn, dev, stream, pk, taps=4):
-    """Fused decode from projections on one layer at batch 32 (fp32 state): conv ring update +
-    silu, q/k L2 norm, gates from logits, the step and the gated norm in one launch."""
+    """Fused decode from projections (conv ring update + silu, q/k L2 norm, gates from logits, the
+    step and the gated norm in one launch): one layer at batch 32 with an fp32 state (also through
+    the allocation-free entry point), and the 256-slot fp16 pool."""
     import gdn_synth as gs
-    x = gs.conv_decode_inputs(SEED, B, NK, NV, D, taps)
-    t = {k: torch.from_numpy(v).to(dev) for k, v in x.items()}
     C = (2 * NK + NV) * D
-    g = torch.Generator(device=dev)
-    g.manual_seed(3)
-    S = torch.empty((B, NV, D, D), device=dev).normal_(0.0, 0.02, generator=g)
-    ring = t["ring"].reshape(B, taps * C).contiguous()
-    gn = torch.from_numpy(gs.norm_weight(SEED, D)).to(dev)
-    out = torch.empty((B, NV * D), dtype=torch.int16, device=dev)
-    ws = torch.zeros(B * NK, dtype=torch.int32, device=dev)
-    s = time_fn(torch, stream, lambda: gdn.gdn_decode_conv_norm(
-        S, ring, t["x"], t["conv_w"], t["br"], t["ar"], t["dt"], t["rate"], t["z"], gn, out, ws,
-        batch=B, nk=NK, nv=NV, d=D, taps=taps, stream=stream.cuda_stream), 50)
-    # state read + write; ring: taps-1 entries read, all taps written; x, z read; w, dt, rate, gn once;
-    # gate logits read; bf16 out written
-    by = (B * NV * D * D * 4 * 2 + B * ((taps - 1) + taps + 1) * C * 4 + taps * C * 4
-          + B * NV * D * 4 + B * NV * 2 * 4 + 2 * NV * 4 + D * 4 + B * NV * D * 2)
-    del S, ring, gn, out, t, ws
-    torch.cuda.empty_cache()
-    return {"conv_norm_from_projections": {
-        "config": "B=32 NK=16 NV=48 D=128 fp32, 4-tap conv", "us_per_launch": s * 1e6,
-        "token_heads_per_s": B * NV / s, "achieved_gbs": by / s / 1e9,
-        "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}}
+    res = {}
+    for label, batch, f16 in (("fp32_b32", B, False), ("fp16_pool_b256", 256, True)):
+        x = gs.conv_decode_inputs(SEED, batch, NK, NV, D, taps)
+        t = {k: torch.from_numpy(v).to(dev) for k, v in x.items()}
+        g = torch.Generator(device=dev)
+        g.manual_seed(3)
+        S = torch.empty((batch, NV * D * D), device=dev).normal_(0.0, 0.02, generator=g)
+        if f16:
+            S = S.half()
+        ring = t["ring"].reshape(batch, taps * C).contiguous()
+        gn = torch.from_numpy(gs.norm_weight(SEED, D)).to(dev)
+        out = torch.empty((batch, NV * D), dtype=torch.int16, device=dev)
+        ws = torch.zeros(batch * NK, dtype=torch.int32, device=dev)
+        args = (S, ring, t["x"], t["conv_w"], t["br"], t["ar"], t["dt"], t["rate"], t["z"], gn, out)
+        kw = dict(batch=batch, nk=NK, nv=NV, d=D, taps=taps, stream=stream.cuda_stream)
+        s = time_fn(torch, stream, lambda: gdn.gdn_decode_conv_norm(*args, ws, **kw), 50 if not f16 else 20)
+        es = 2 if f16 else 4
+        # state read + write; ring: taps-1 entries read, all taps written; x, z read; w, dt, rate, gn
+        # once; gate logits read; bf16 out written
+        by = (batch * NV * D * D * es * 2 + batch * ((taps - 1) + taps + 1) * C * 4 + taps * C * 4
+              + batch * NV * D * 4 + batch * NV * 2 * 4 + 2 * NV * 4 + D * 4 + batch * NV * D * 2)
+        r = {"config": f"B={batch} NK=16 NV=48 D=128 {'fp16' if f16 else 'fp32'}, 4-tap conv",
+             "us_per_launch": s * 1e6, "token_heads_per_s": batch * NV / s, "achieved_gbs": by / s / 1e9,
+             "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}
+        if not f16:
+            s2 = time_fn(torch, stream, lambda: gdn.gdn_decode_conv_norm_noalloc(*args, **kw), 50)
+            r["noalloc_us_per_launch"] = s2 * 1e6
+        res[label] = r
+        del S, ring, gn, out, t, ws, args
+        torch.cuda.empty_cache()
+    return {"conv_norm_from_projections": res}
 
 
 def row_q8(torch, gdn, dev, stream, pk):
@@ -508,30 +518,37 @@ def row_q8(torch, gdn, dev, stream, pk):
 
 
 def row_chunk2(torch, gdn, dev, stream, pk):
-    """Two-token verify step on one layer at batch 32 (fp32 state): the state is read once and
-    written twice (intermediate + final); both tokens' inputs read, both outputs written."""
-    g = torch.Generator(device=dev)
-    g.manual_seed(2)
-    S = torch.empty((B, NV, D, D), device=dev).normal_(0.0, 0.02, generator=g)
-    M = torch.empty_like(S)
-    R = 2 * B
-    q = torch.randn((R, NK * D), device=dev, generator=g)
-    k = torch.randn((R, NK * D), device=dev, generator=g)
-    q = (q.view(R, NK, D) / q.view(R, NK, D).norm(dim=-1, keepdim=True)).view(R, NK * D).contiguous()
-    k = (k.view(R, NK, D) / k.view(R, NK, D).norm(dim=-1, keepdim=True)).view(R, NK * D).contiguous()
-    v = torch.randn((R, NV * D), device=dev, generator=g)
-    a = torch.sigmoid(torch.randn((R, NV), device=dev, generator=g) + 2.0)
-    bt = torch.sigmoid(torch.randn((R, NV), device=dev, generator=g))
-    o = torch.empty((R, NV * D), device=dev)
-    s = time_fn(torch, stream, lambda: gdn.gdn_decode_chunk2(S, M, q, k, v, a, bt, o, batch=B, nk=NK, nv=NV, d=D,
-                                                             stream=stream.cuda_stream), 50)
-    by = B * NV * D * D * 4 * 3 + R * (2 * NK * D + 2 * NV * D + 2 * NV) * 4
-    del S, M, q, k, v, a, bt, o
-    torch.cuda.empty_cache()
-    return {"chunk2_verify": {"config": "B=32 NK=16 NV=48 D=128 fp32, two tokens per launch",
-                              "us_per_launch": s * 1e6, "token_heads_per_s": R * NV / s,
-                              "achieved_gbs": by / s / 1e9, "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"],
-                              "algorithmic_bytes": by}}
+    """Two-token verify step, one layer at batch 32 (fp32 state) and on the 256-slot fp16 pool: the
+    state is read once and written twice (intermediate + final); both tokens' inputs read, both
+    outputs written."""
+    res = {}
+    for label, batch, f16 in (("fp32_b32", B, False), ("fp16_pool_b256", 256, True)):
+        g = torch.Generator(device=dev)
+        g.manual_seed(2)
+        S = torch.empty((batch, NV, D, D), device=dev).normal_(0.0, 0.02, generator=g)
+        if f16:
+            S = S.half()
+        M = torch.empty_like(S)
+        R = 2 * batch
+        q = torch.randn((R, NK * D), device=dev, generator=g)
+        k = torch.randn((R, NK * D), device=dev, generator=g)
+        q = (q.view(R, NK, D) / q.view(R, NK, D).norm(dim=-1, keepdim=True)).view(R, NK * D).contiguous()
+        k = (k.view(R, NK, D) / k.view(R, NK, D).norm(dim=-1, keepdim=True)).view(R, NK * D).contiguous()
+        v = torch.randn((R, NV * D), device=dev, generator=g)
+        a = torch.sigmoid(torch.randn((R, NV), device=dev, generator=g) + 2.0)
+        bt = torch.sigmoid(torch.randn((R, NV), device=dev, generator=g))
+        o = torch.empty((R, NV * D), device=dev)
+        s = time_fn(torch, stream, lambda: gdn.gdn_decode_chunk2(S, M, q, k, v, a, bt, o, batch=batch, nk=NK, nv=NV,
+                                                                 d=D, stream=stream.cuda_stream), 50 if not f16 else 20)
+        es = 2 if f16 else 4
+        by = batch * NV * D * D * es * 3 + R * (2 * NK * D + 2 * NV * D + 2 * NV) * 4
+        res[label] = {"config": f"B={batch} NK=16 NV=48 D=128 {'fp16' if f16 else 'fp32'}, two tokens per launch",
+                      "us_per_launch": s * 1e6, "token_heads_per_s": R * NV / s,
+                      "achieved_gbs": by / s / 1e9, "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"],
+                      "algorithmic_bytes": by}
+        del S, M, q, k, v, a, bt, o
+        torch.cuda.empty_cache()
+    return {"chunk2_verify": res}
 
 
 def row_fp16_pool(torch, gdn, dev, stream, pk, want):

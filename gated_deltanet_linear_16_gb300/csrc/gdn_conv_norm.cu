@@ -388,11 +388,13 @@ conv_norm_generic(const ConvNormParams p)
 }
 
 // Shapes of the D == 128 kernel, by measurement on GB300 (one layer at batch 32
-// fp32, 256-slot fp16 pool): fp32 register batches (4 x 4 loads, 3 CTAs per
-// SM); fp16 staged in shared memory (32 KB + 10 KB a CTA, 5 CTAs per SM).
+// fp32, 256-slot fp16 pool): fp32 register batches (4 x 4 loads, 4 CTAs per
+// SM: a CTA spends part of its life in the producer phase, so more of them
+// keep the state streaming); fp16 staged in shared memory (32 KB + 10 KB a
+// CTA, 5 CTAs per SM).
 template <typename TS> struct ConvShape {
     static constexpr bool kStaged = false;
-    static constexpr int kBatches = 4, kMinBlocks = 3;
+    static constexpr int kBatches = 4, kMinBlocks = 4;
 };
 template <> struct ConvShape<__half> {
     static constexpr bool kStaged = true;
