@@ -54,6 +54,16 @@ def test_general_kernel_any_d(D, f16):
     check_decode(r, f16=f16, norm=True)
 
 
+@pytest.mark.parametrize("f16", [False, True])
+@pytest.mark.parametrize("norm", [True, False])
+@pytest.mark.parametrize("B", [2, 8, 32])
+def test_every_load_variant(B, norm, f16):
+    """NV = 48: grids of 96, 384 and 1536 CTAs take the all-in-registers, register-batched (fp32;
+    fp16 is staged there) and staged loads of the D = 128 kernel."""
+    r = run_decode_case(B, 16, 48, 128, 1, f16=f16, norm=norm, seed=200 + B)
+    check_decode(r, f16=f16, norm=norm)
+
+
 def test_many_heads_several_waves():
     """B * NV = 640 CTAs: several waves over the SMs, with NV = 40 not a multiple of NK = 16."""
     r = run_decode_case(16, 16, 40, 128, 2, f16=False, norm=True, seed=4)
