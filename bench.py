@@ -630,15 +630,20 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
         gdn.gdn_prefill_seq(S, q, k, v, a, bt, o, batch=PB, seq_len=T, nk=NK, nv=NV, d=D, stream=sp)
 
     s = time_fn(torch, stream, pf, 3, warm=1)
+    # the same call on an fp16 state (widened once on load, carried in fp32, rounded once on store)
+    S16 = torch.zeros((PB, NV, D, D), dtype=torch.float16, device=dev)
+    s16 = time_fn(torch, stream, lambda: gdn.gdn_prefill_seq(S16, q, k, v, a, bt, o, batch=PB, seq_len=T, nk=NK,
+                                                             nv=NV, d=D, stream=sp), 3, warm=1)
     th = PB * NV * T
     io = (2 * R * NK * D + R * NV * D * 2 + 2 * R * NV) * 4 + 2 * PB * NV * D * D * 4
     fma = th * D * D * 3                # per token-head: S.k, the rank-1 write, S.q (D^2 FMA each)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     clk = (pk.get("sm_max_mhz") or 2070.0) * 1e6
     fma_peak = sms * 128 * clk          # FP32 FMA lanes x max clock: FMA per second
-    del q, k, v, a, bt, o, S
+    del q, k, v, a, bt, o, S, S16
     torch.cuda.empty_cache()
     return {"prefill": {"config": f"B=8 T={T} NK=16 NV=48 D=128 fp32, state on chip",
+                        "fp16_state": {"ms": s16 * 1e3, "token_heads_per_s": th / s16},
                         "ms": s * 1e3, "token_heads_per_s": th / s,
                         "roofline": {"bound": "alu", "achieved": fma / s / 1e12, "peak": fma_peak / 1e12,
                                      "unit": "T FP32 FMA/s", "frac": fma / s / fma_peak,
