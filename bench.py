@@ -437,6 +437,7 @@ def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096, graph=
         rows.update(row_fp16_pool(torch, gdn, dev, stream, pk, want))
     if "latency" in want:
         rows.update(row_latency(torch, gdn, dev, stream, graph))
+        rows.update(row_tiny(torch, gdn, dev, stream))
     if "chunk2" in want:
         rows.update(row_chunk2(torch, gdn, dev, stream, pk))
     if "convnorm" in want:
@@ -608,6 +609,30 @@ def row_latency(torch, gdn, dev, stream, graph=True):
                                      "us_per_step": s * 1e6, "token_heads_per_s": NV / s}}
 
 
+def row_tiny(torch, gdn, dev, stream):
+    """The pages' tiny configuration (batch 1, NK 1, NV 2, D 4, fp32 state from zero): 64 sequential
+    decode steps with the fused norm, captured as one CUDA graph; latency per step."""
+    import gdn_synth as gs
+    T, nk, nv, d = 64, 1, 2, 4
+    xs = [gs.decode_inputs(SEED, 1, nk, nv, d, step=t) for t in range(T)]
+    t_in = {k: torch.from_numpy(np.stack([x[k] for x in xs])).to(dev) for k in ("q", "k", "v", "alpha", "beta", "z")}
+    gn = torch.from_numpy(gs.norm_weight(SEED, d)).to(dev)
+    S = torch.zeros((1, nv, d, d), device=dev)
+    out = torch.empty((T, nv * d), dtype=torch.int16, device=dev)
+
+    def steps():
+        for t in range(T):
+            gdn.gdn_decode_norm(S, t_in["q"][t], t_in["k"][t], t_in["v"][t], t_in["alpha"][t], t_in["beta"][t],
+                                t_in["z"][t], gn, out[t], batch=1, nk=nk, nv=nv, d=d, eps=EPS, stream=None)
+
+    run, used = graphed(torch, steps, torch.cuda.Stream(device=dev))
+    s = time_fn(torch, stream, run, 20)
+    del S, out, t_in
+    return {"tiny_config_latency": {"config": "B=1 NK=1 NV=2 D=4 fp32, 64 sequential steps, fused norm",
+                                    "submission": "CUDA graph of 64 steps" if used else "eager",
+                                    "us_per_step": s / T * 1e6}}
+
+
 def row_prefill(torch, gdn, dev, stream, pk, T=4096):
     """Prefill: B=8, T tokens in one call, fp32 state from zero (inputs drawn on the device at the
     generator's distributions; values do not change the timing)."""
@@ -634,6 +659,13 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
     S16 = torch.zeros((PB, NV, D, D), dtype=torch.float16, device=dev)
     s16 = time_fn(torch, stream, lambda: gdn.gdn_prefill_seq(S16, q, k, v, a, bt, o, batch=PB, seq_len=T, nk=NK,
                                                              nv=NV, d=D, stream=sp), 3, warm=1)
+    # the gated norm over every token's raw o (gdn_gate_norm, bf16 out): o and z read, out written
+    z = torch.randn((R, NV * D), device=dev, generator=g)
+    gn = torch.ones(D, device=dev)
+    out = torch.empty((R, NV * D), dtype=torch.int16, device=dev)
+    s_norm = time_fn(torch, stream, lambda: gdn.gdn_gate_norm(o, z, gn, out, rows=R, nv=NV, d=D, stream=sp), 5)
+    norm_bytes = R * NV * D * (4 + 4 + 2) + D * 4
+    del z, gn, out
     th = PB * NV * T
     io = (2 * R * NK * D + R * NV * D * 2 + 2 * R * NV) * 4 + 2 * PB * NV * D * D * 4
     fma = th * D * D * 3                # per token-head: S.k, the rank-1 write, S.q (D^2 FMA each)
@@ -644,6 +676,9 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
     torch.cuda.empty_cache()
     return {"prefill": {"config": f"B=8 T={T} NK=16 NV=48 D=128 fp32, state on chip",
                         "fp16_state": {"ms": s16 * 1e3, "token_heads_per_s": th / s16},
+                        "gate_norm_of_outputs": {"us": s_norm * 1e6, "achieved_gbs": norm_bytes / s_norm / 1e9,
+                                                 "frac_of_hbm_peak": norm_bytes / s_norm / 1e9 / pk["hbm_gbs"],
+                                                 "algorithmic_bytes": norm_bytes},
                         "ms": s * 1e3, "token_heads_per_s": th / s,
                         "roofline": {"bound": "alu", "achieved": fma / s / 1e12, "peak": fma_peak / 1e12,
                                      "unit": "T FP32 FMA/s", "frac": fma / s / fma_peak,

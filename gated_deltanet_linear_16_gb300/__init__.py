@@ -24,6 +24,7 @@ __all__ = [
     "GDN_STATE_F32", "GDN_STATE_F16", "STATUS",
     "gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
     "gdn_decode_conv_norm_noalloc", "GDN_NOALLOC_MAX_KEY_HEADS", "gdn_decode_norm_q8",
+    "gdn_gate_norm", "gdn_gate_norm_q8",
     "gdn_h_f32_to_f16", "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error",
 ]
 
@@ -62,6 +63,8 @@ def _declare(lib):
                                     i64, i64, i64, i64, i64, P]
     lib.gdn_decode_norm_q8.argtypes = [P, i32, i64, P, P, P, P, P, P, P, f32, P, P, P, i32, i32, i32, i32,
                                        i64, i64, i64, i64, i64, i64, i64, P]
+    lib.gdn_gate_norm.argtypes = [P, P, P, f32, P, i64, i32, i32, i64, i64, i64, P]
+    lib.gdn_gate_norm_q8.argtypes = [P, P, P, f32, P, P, P, i64, i32, i32, i64, i64, i64, i64, i64, P]
     lib.gdn_decode_conv_norm.argtypes = [P, i32, i64, P, i64, i32, P, P, P, P, P, P, P, P, f32, f32, P, P,
                                          i32, i32, i32, i32, i64, i64, i64, i64, P]
     lib.gdn_decode_conv_norm_noalloc.argtypes = [P, i32, i64, P, i64, i32, P, P, P, P, P, P, P, P, f32, f32, P,
@@ -73,7 +76,8 @@ def _declare(lib):
     lib.gdn_h_f32_to_f16.argtypes = [P, P, u64, P]
     lib.gdn_h_f16_to_f32.argtypes = [P, P, u64, P]
     for fn in ("gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
-               "gdn_decode_conv_norm_noalloc", "gdn_decode_norm_q8", "gdn_h_f32_to_f16",
+               "gdn_decode_conv_norm_noalloc", "gdn_decode_norm_q8", "gdn_gate_norm", "gdn_gate_norm_q8",
+               "gdn_h_f32_to_f16",
                "gdn_h_f16_to_f32"):
         getattr(lib, fn).restype = i32
     lib.gdn_status_str.argtypes = [i32]
@@ -195,6 +199,30 @@ def gdn_decode_norm_q8(state, q, k, v, alpha, beta, z, gn, xq, xs, y=None, *, ba
         y_stride if y_stride is not None else nv * d,
         _stream(stream))
     _check("gdn_decode_norm_q8", st)
+
+
+def gdn_gate_norm(o, z, gn, out, *, rows, nv, d, eps=1e-6, o_stride=None, z_stride=None, out_stride=None,
+                  stream=None):
+    """The gated RMS norm over `rows` rows of NV heads x D raw outputs (e.g. a prefill's o); bf16 out."""
+    lib = load()
+    hv = nv * d
+    st = lib.gdn_gate_norm(_ptr(o), _ptr(z), _ptr(gn), float(eps), _ptr(out), rows, nv, d,
+                           o_stride if o_stride is not None else hv, z_stride if z_stride is not None else hv,
+                           out_stride if out_stride is not None else hv, _stream(stream))
+    _check("gdn_gate_norm", st)
+
+
+def gdn_gate_norm_q8(o, z, gn, xq, xs, y=None, *, rows, nv, d, eps=1e-6, o_stride=None, z_stride=None,
+                     xq_stride=None, xs_stride=None, y_stride=None, stream=None):
+    """gdn_gate_norm with int8 output groups of 32 (codes xq, fp32 scales xs, optional fp32 y)."""
+    lib = load()
+    hv = nv * d
+    st = lib.gdn_gate_norm_q8(_ptr(o), _ptr(z), _ptr(gn), float(eps), _ptr(xq), _ptr(xs), _ptr(y), rows, nv, d,
+                              o_stride if o_stride is not None else hv, z_stride if z_stride is not None else hv,
+                              xq_stride if xq_stride is not None else hv,
+                              xs_stride if xs_stride is not None else hv // 32,
+                              y_stride if y_stride is not None else hv, _stream(stream))
+    _check("gdn_gate_norm_q8", st)
 
 
 def gdn_decode_conv_norm(state, conv_state, x, conv_w, br, ar, dt, rate, z, gn, out, workspace, *, batch, nk,

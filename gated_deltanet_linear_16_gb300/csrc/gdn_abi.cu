@@ -176,6 +176,54 @@ int decode_entry(void *state, int state_dtype, int64_t state_pitch,
 
 int report_cuda_error(cudaError_t e) { return cuda_status(e); }
 
+namespace {
+
+// The standalone gated norm: rows of NV heads x D raw outputs o (and gate
+// inputs z) to the bf16 or int8 epilogue.  Checks as for decode.
+int norm_entry(const float *o, const float *z, const float *gn, float eps, NormParams p, int epi,
+               int64_t rows, int nv, int d, int64_t o_stride, int64_t z_stride, void *stream)
+{
+    if (rows < 0 || nv <= 0 || d <= 0) return GDN_ERR_ARG;
+    if (d > 256) return GDN_ERR_UNSUPPORTED;
+    if (epi == kEpiQ8 && d % 32 != 0) return GDN_ERR_UNSUPPORTED;
+    if (!(eps >= 0.0f && std::isfinite(eps))) return GDN_ERR_ARG;
+    if (rows > INT64_MAX / nv || rows * nv > (int64_t)INT32_MAX * 8) return GDN_ERR_UNSUPPORTED;   // grid size
+    const int64_t hv = (int64_t)nv * d;
+    Operand ops[7];
+    int n = 0;
+    if (epi == kEpiBf16) {
+        ops[n++] = {p.out, rows, hv, p.out_stride, 2};
+    } else {
+        ops[n++] = {p.xq, rows, hv, p.xq_stride, 1};
+        ops[n++] = {p.xs, rows, hv / 32, p.xs_stride, 4};
+        if (p.y != nullptr) ops[n++] = {p.y, rows, hv, p.y_stride, 4};
+    }
+    const int n_out = n;
+    ops[n++] = {o, rows, hv, o_stride, 4};
+    ops[n++] = {z, rows, hv, z_stride, 4};
+    ops[n++] = {gn, 1, d, d, 4};
+    if (rows == 0) {
+        for (int i = 0; i < n; ++i) if (ops[i].p == nullptr) return GDN_ERR_ARG;
+        return GDN_OK;
+    }
+    const int st = check_operands(ops, n, n_out);
+    if (st != GDN_OK) return st;
+    p.o = o; p.z = z; p.gn = gn; p.eps = eps;
+    p.rows = rows; p.nv = nv; p.d = d; p.o_stride = o_stride; p.z_stride = z_stride;
+    // D == 128 vector kernel: 16-byte o, z, gn rows; 8-byte bf16 or 4-byte int8 and 16-byte y rows
+    bool fast = d == 128 && vec16(o) && vec16(z) && vec16(gn) && (o_stride * 4) % 16 == 0 &&
+                (z_stride * 4) % 16 == 0;
+    if (epi == kEpiBf16) {
+        fast = fast && aligned(p.out, 8) && (p.out_stride * 2) % 8 == 0;
+    } else {
+        fast = fast && aligned(p.xq, 4) && p.xq_stride % 4 == 0 &&
+               (p.y == nullptr || (vec16(p.y) && (p.y_stride * 4) % 16 == 0));
+    }
+    return cuda_status(launch_gate_norm(p, epi, fast, (cudaStream_t)stream));
+}
+
+}  // namespace
+
 }  // namespace gdn
 
 using namespace gdn;
@@ -370,6 +418,27 @@ GDN_API int gdn_prefill_seq(void *state, int state_dtype, int64_t state_pitch,
                       vec16(q) && vec16(k) && (qk_stride * 4) % 16 == 0 &&
                       vec16(v) && (v_stride * 4) % 16 == 0;
     return cuda_status(launch_prefill(p, state_dtype == GDN_STATE_F16, fast, (cudaStream_t)stream));
+}
+
+GDN_API int gdn_gate_norm(const float *o, const float *z, const float *gn, float eps, uint16_t *out,
+                          int64_t rows, int nv, int d, int64_t o_stride, int64_t z_stride,
+                          int64_t out_stride, void *stream)
+{
+    NormParams p{};
+    p.out = out; p.out_stride = out_stride;
+    return norm_entry(o, z, gn, eps, p, kEpiBf16, rows, nv, d, o_stride, z_stride, stream);
+}
+
+GDN_API int gdn_gate_norm_q8(const float *o, const float *z, const float *gn, float eps,
+                             int8_t *xq, float *xs, float *y, int64_t rows, int nv, int d,
+                             int64_t o_stride, int64_t z_stride, int64_t xq_stride, int64_t xs_stride,
+                             int64_t y_stride, void *stream)
+{
+    NormParams p{};
+    p.xq = xq; p.xq_stride = xq_stride;
+    p.xs = xs; p.xs_stride = xs_stride;
+    p.y = y; p.y_stride = y_stride;
+    return norm_entry(o, z, gn, eps, p, kEpiQ8, rows, nv, d, o_stride, z_stride, stream);
 }
 
 GDN_API int gdn_h_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, void *stream)

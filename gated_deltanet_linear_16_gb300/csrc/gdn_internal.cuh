@@ -41,6 +41,17 @@ struct DecodeParams {
 // as bf16, or the normed output as int8 groups of 32.
 constexpr int kEpiRaw = 0, kEpiBf16 = 1, kEpiQ8 = 2;
 
+// The gated RMS norm over rows of raw outputs (rows of NV heads x D values).
+struct NormParams {
+    const float *o, *z, *gn;
+    uint16_t *out;                     // bf16 epilogue
+    int8_t *xq;                        // int8 epilogue: codes, group scales, optional fp32 y
+    float *xs, *y;
+    int64_t rows, o_stride, z_stride, out_stride, xq_stride, xs_stride, y_stride;
+    int nv, d;
+    float eps;
+};
+
 struct PrefillParams {
     void *state;            // float* or __half*
     int64_t pitch;
@@ -80,6 +91,7 @@ cudaError_t launch_decode(const DecodeParams &p, bool f16_state, int epi, bool f
 cudaError_t launch_decode_chunk2(const DecodeParams &p, bool f16_state, bool fast, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, bool f16_state, bool fast, cudaStream_t s);
 cudaError_t launch_conv_norm(const ConvNormParams &p, bool f16_state, bool fast, cudaStream_t s);
+cudaError_t launch_gate_norm(const NormParams &p, int epi, bool fast, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, bool vec, cudaStream_t s);
 cudaError_t launch_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, bool vec, cudaStream_t s);
 

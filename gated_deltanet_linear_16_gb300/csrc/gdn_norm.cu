@@ -1,0 +1,158 @@
+// gdn_norm.cu -- the gated RMS norm as its own launch, over rows of raw
+// outputs o (e.g. every token of a prefill call), with a bf16 output or the
+// int8 activation groups.
+//
+// Follows logicaffeine_compile/codegen_cuda/gdn.rs, kernels `gdn_gate_norm`
+// (out = gn o / sqrt(mean_head o^2 + eps) * silu(z): the norm first, then the
+// gate; gn shared by all heads) and `gdn_gate_norm_q` (the same with the
+// int8 quantisation of the o-projection's input fused in: groups of 32 values,
+// scale = max |y| / 127, codes rounded to nearest even).
+//
+// An HBM stream (o and z read once, the output written once).  General D: one
+// warp per (row, head), lanes strided over the head's D values (coalesced
+// 128-byte warp accesses), every load of a lane in flight before the
+// reduction; 8 warps per CTA.  D == 128 takes the vector kernel below.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+constexpr int kMaxPer = 8;                 // D <= 256: values per lane
+
+template <int EPI>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+gate_norm_rows(const NormParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t unit = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);   // (row, head)
+    if (unit >= p.rows * p.nv) return;                  // whole warps leave together
+    const int64_t row = unit / p.nv;
+    const int h = (int)(unit - row * p.nv);
+    const int D = p.d;
+    const float *op = p.o + row * p.o_stride + (int64_t)h * D;
+    const float *zp = p.z + row * p.z_stride + (int64_t)h * D;
+
+    float ov[kMaxPer], zv[kMaxPer];
+#pragma unroll
+    for (int j = 0; j < kMaxPer; ++j) {
+        const int a = lane + 32 * j;
+        ov[j] = a < D ? __ldcs(op + a) : 0.f;
+        zv[j] = a < D ? __ldcs(zp + a) : 0.f;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxPer; ++j) ss = fmaf(ov[j], ov[j], ss);
+    ss = group_sum<32>(ss);
+    const float rstd = rsqrtf(ss / (float)D + p.eps);
+
+#pragma unroll
+    for (int j = 0; j < kMaxPer; ++j) {
+        if (32 * j >= D) break;                         // warp-uniform
+        const int a = lane + 32 * j;
+        const bool in = a < D;
+        const float y = in ? __ldg(p.gn + a) * ov[j] * rstd * silu(zv[j]) : 0.f;
+        if constexpr (EPI == kEpiBf16) {
+            if (in) p.out[row * p.out_stride + (int64_t)h * D + a] = bf16_bits_rn(y);
+        } else {                                        // D % 32 == 0: a whole group per j
+            if (p.y != nullptr) p.y[row * p.y_stride + (int64_t)h * D + a] = y;
+            quant_group32(y, p.xq + row * p.xq_stride + (int64_t)h * D + a,
+                          p.xs + row * p.xs_stride + (int64_t)h * (D / 32) + j, lane);
+        }
+    }
+}
+
+// D == 128 with 16-byte aligned rows: a lane holds 4 consecutive values of a
+// head (one 16-byte load each of o and z), warps loop over (row, head) units
+// with several units in flight, and the grid is a few CTAs per SM.  An int8 group
+// of 32 values is then 8 lanes.
+constexpr int kD = 128;
+constexpr int kCtasPerSm = 8;
+#ifndef NORM_IN_FLIGHT
+#define NORM_IN_FLIGHT 2
+#endif
+constexpr int kInFlight = NORM_IN_FLIGHT;   // (row, head) units per warp in flight
+
+template <int EPI>
+__device__ __forceinline__ void norm_unit_d128(const NormParams &p, int64_t unit, float4 ov, float4 zv,
+                                               int lane)
+{
+    const int64_t row = unit / p.nv;
+    const int h = (int)(unit - row * p.nv);
+    float ss = ov.x * ov.x;
+    ss = fmaf(ov.y, ov.y, ss);
+    ss = fmaf(ov.z, ov.z, ss);
+    ss = fmaf(ov.w, ov.w, ss);
+    ss = group_sum<32>(ss);
+    const float rstd = rsqrtf(ss * (1.0f / kD) + p.eps);
+    const float4 g = __ldg(reinterpret_cast<const float4 *>(p.gn) + lane);
+    float y[4] = {g.x * ov.x * rstd * silu(zv.x), g.y * ov.y * rstd * silu(zv.y),
+                  g.z * ov.z * rstd * silu(zv.z), g.w * ov.w * rstd * silu(zv.w)};
+    const int64_t e0 = (int64_t)h * kD + 4 * lane;
+    if constexpr (EPI == kEpiBf16) {
+        const uint2 b = make_uint2((unsigned)bf16_bits_rn(y[0]) | ((unsigned)bf16_bits_rn(y[1]) << 16),
+                                   (unsigned)bf16_bits_rn(y[2]) | ((unsigned)bf16_bits_rn(y[3]) << 16));
+        __stcs(reinterpret_cast<uint2 *>(p.out + row * p.out_stride + e0), b);
+    } else {
+        if (p.y != nullptr)
+            __stcs(reinterpret_cast<float4 *>(p.y + row * p.y_stride + e0), make_float4(y[0], y[1], y[2], y[3]));
+        float am = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, off));
+        const float sc = am > 0.f ? am / 127.0f : 1.0f;    // the group's 8 lanes agree
+        unsigned packed = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) packed |= ((unsigned)(__float2int_rn(y[i] / sc) & 0xff)) << (8 * i);
+        *reinterpret_cast<unsigned *>(p.xq + row * p.xq_stride + e0) = packed;
+        if ((lane & 7) == 0) p.xs[row * p.xs_stride + (int64_t)h * (kD / 32) + (lane >> 3)] = sc;
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+gate_norm_d128(const NormParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t units = p.rows * p.nv;
+    const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+    int64_t u = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    auto ld = [&](int64_t unit, float4 &ov, float4 &zv) {
+        const int64_t row = unit / p.nv;
+        const int64_t e0 = (unit - row * p.nv) * kD + 4 * lane;
+        ov = __ldcs(reinterpret_cast<const float4 *>(p.o + row * p.o_stride + e0));
+        zv = __ldcs(reinterpret_cast<const float4 *>(p.z + row * p.z_stride + e0));
+    };
+    for (; u + (kInFlight - 1) * nwarps < units; u += kInFlight * nwarps) {   // kInFlight units at once
+        float4 ov[kInFlight], zv[kInFlight];
+#pragma unroll
+        for (int i = 0; i < kInFlight; ++i) ld(u + i * nwarps, ov[i], zv[i]);
+#pragma unroll
+        for (int i = 0; i < kInFlight; ++i) norm_unit_d128<EPI>(p, u + i * nwarps, ov[i], zv[i], lane);
+    }
+    for (; u < units; u += nwarps) {
+        float4 o0, z0;
+        ld(u, o0, z0);
+        norm_unit_d128<EPI>(p, u, o0, z0, lane);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gate_norm(const NormParams &p, int epi, bool fast, cudaStream_t s)
+{
+    const int64_t units = p.rows * p.nv;
+    if (fast) {
+        const int64_t full = (int64_t)sm_count() * kCtasPerSm;
+        const int64_t need = (units + kWarpsPerCta - 1) / kWarpsPerCta;
+        const unsigned grid = (unsigned)(need < full ? need : full);
+        if (epi == kEpiQ8) gate_norm_d128<kEpiQ8><<<grid, kWarpsPerCta * 32, 0, s>>>(p);
+        else gate_norm_d128<kEpiBf16><<<grid, kWarpsPerCta * 32, 0, s>>>(p);
+        return cudaGetLastError();
+    }
+    const unsigned grid = (unsigned)((units + kWarpsPerCta - 1) / kWarpsPerCta);
+    if (epi == kEpiQ8) gate_norm_rows<kEpiQ8><<<grid, kWarpsPerCta * 32, 0, s>>>(p);
+    else gate_norm_rows<kEpiBf16><<<grid, kWarpsPerCta * 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

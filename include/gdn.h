@@ -149,6 +149,39 @@ GDN_API int gdn_decode_norm_q8(void *state, int state_dtype, int64_t state_pitch
                                int64_t y_stride, void *stream);
 
 /*
+ * gdn_gate_norm -- the gated RMS norm as its own call, over rows of raw
+ * outputs o (for instance every token of gdn_prefill_seq), bf16 out.
+ *   Defined by: gdn.rs, kernel `gdn_gate_norm` (per head of D values:
+ *   out = gn * o / sqrt(mean o^2 + eps) * silu(z); the norm first, then the
+ *   gate; gn shared by all heads).
+ *   o, z         [rows] rows of NV*D fp32, row strides o_stride, z_stride.
+ *   gn           [D] fp32.  eps >= 0, finite.  1 <= D <= 256.
+ *   out          [rows] rows of NV*D bf16 (raw uint16 bits, round to nearest
+ *                even), written; row stride out_stride.
+ *   rows = 0 is a valid empty call.  Errors: GDN_ERR_ARG, GDN_ERR_UNSUPPORTED
+ *   (D > 256), GDN_ERR_ALIGN, GDN_ERR_ALIAS (out overlapping any operand),
+ *   GDN_ERR_CUDA.
+ */
+GDN_API int gdn_gate_norm(const float *o, const float *z, const float *gn, float eps, uint16_t *out,
+                          int64_t rows, int nv, int d, int64_t o_stride, int64_t z_stride,
+                          int64_t out_stride, void *stream);
+
+/*
+ * gdn_gate_norm_q8 -- gdn_gate_norm with the int8 epilogue of
+ * gdn_decode_norm_q8 (gdn.rs `gdn_gate_norm_q`): groups of 32 consecutive
+ * values of a row, scale = max |y| / 127 (1 for an all-zero group), code =
+ * y / scale rounded to nearest even, in fp32.  D must be a multiple of 32.
+ *   xq           [rows] rows of NV*D int8 codes, row stride xq_stride.
+ *   xs           [rows] rows of NV*D/32 fp32 scales, row stride xs_stride.
+ *   y            NULL, or [rows] rows of NV*D fp32 normed values, y_stride.
+ *   Other arguments and errors as gdn_gate_norm.
+ */
+GDN_API int gdn_gate_norm_q8(const float *o, const float *z, const float *gn, float eps,
+                             int8_t *xq, float *xs, float *y, int64_t rows, int nv, int d,
+                             int64_t o_stride, int64_t z_stride, int64_t xq_stride, int64_t xs_stride,
+                             int64_t y_stride, void *stream);
+
+/*
  * gdn_decode_conv_norm -- one token from the projection outputs to the normed
  * bf16 output in one launch: the depthwise causal conv ring update with silu
  * on q, k and v, the per-head L2 normalisation of q and k, the gates from

@@ -41,7 +41,8 @@ def lib(built):
 def test_exports_match_header(built):
     want = declared_symbols()
     assert want == sorted(["gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm",
-                           "gdn_decode_conv_norm_noalloc", "gdn_decode_norm_q8", "gdn_prefill_seq",
+                           "gdn_decode_conv_norm_noalloc", "gdn_decode_norm_q8", "gdn_gate_norm",
+                           "gdn_gate_norm_q8", "gdn_prefill_seq",
                            "gdn_h_f32_to_f16",
                            "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error"])
     out = subprocess.run(["nm", "-D", "--defined-only", gdn.library_path()], capture_output=True, text=True,
@@ -230,6 +231,34 @@ def test_decode_norm_q8_empty_and_optional_y(lib):
     assert decode_norm_q8(lib, batch=0) == OK
     assert decode_norm_q8(lib, batch=0, y=None) == OK
     assert decode_norm_q8(lib, batch=0, xq=None) == ARG
+
+
+def gate_norm(lib, q8=False, **kw):
+    a = dict(o=A, z=A + (1 << 30), gn=A + (2 << 30), eps=1e-6, out=A + (3 << 30), xq=A + (3 << 30),
+             xs=A + (4 << 30), y=A + (5 << 30), rows=7, nv=3, d=64, os=192, zs=192, outs=192, xqs=192, xss=6,
+             ys=192)
+    a.update(kw)
+    if q8:
+        return lib.gdn_gate_norm_q8(a["o"], a["z"], a["gn"], a["eps"], a["xq"], a["xs"], a["y"], a["rows"], a["nv"],
+                                    a["d"], a["os"], a["zs"], a["xqs"], a["xss"], a["ys"], None)
+    return lib.gdn_gate_norm(a["o"], a["z"], a["gn"], a["eps"], a["out"], a["rows"], a["nv"], a["d"], a["os"],
+                             a["zs"], a["outs"], None)
+
+
+@pytest.mark.parametrize("q8,kw,want", [
+    (False, dict(d=257, os=771, zs=771, outs=771), UNSUP), (False, dict(nv=0), ARG), (False, dict(rows=-1), ARG),
+    (False, dict(o=None), ARG), (False, dict(eps=float("inf")), ARG), (False, dict(os=100), ARG),
+    (False, dict(out=A + 2), ALIAS), (False, dict(out=A + (3 << 30) + 1), ALIGN),
+    (True, dict(d=48, os=144, zs=144, xqs=144, xss=4, ys=144), UNSUP), (True, dict(xs=None), ARG),
+    (True, dict(xq=A + (4 << 30) + 4), ALIAS), (True, dict(y=A + (1 << 30) + 64), ALIAS),
+])
+def test_gate_norm_rejects(lib, q8, kw, want):
+    assert gate_norm(lib, q8=q8, **kw) == want
+
+
+def test_gate_norm_empty_is_ok(lib):
+    assert gate_norm(lib, rows=0) == OK
+    assert gate_norm(lib, q8=True, rows=0, y=None) == OK
 
 
 @pytest.mark.parametrize("kw,want", [

@@ -1,0 +1,111 @@
+"""GPU parity: gdn_gate_norm / gdn_gate_norm_q8 (the gated RMS norm as its own call, gdn.rs
+`gdn_gate_norm` and `gdn_gate_norm_q`) against the fp64 oracle, alone and after a prefill call.
+
+bf16 output: relative L2 against the oracle's fp64 norm (the bf16 bar).  int8: the fp32 values y
+the kernel writes are held to the fp32 bar, and the oracle's fp32 quantiser applied to them must
+give the kernel's codes and scales bit for bit.  Strided rows, guard bands, D = 5 ... 256 and an
+all-zero head (gate input 0) are covered."""
+import numpy as np
+import pytest
+import torch
+
+import gdn_synth as gs
+import gated_deltanet_linear_16_gb300 as gdn
+import oracle
+from tests.gpu_helpers import TOL_F32, TOL_REL_L2, Rows, bf16_to_f64, max_rel_err, rel_l2
+
+pytestmark = pytest.mark.gpu
+EPS = 1e-6
+
+
+@pytest.fixture(autouse=True)
+def _lib(cuda_lib):
+    return cuda_lib
+
+
+def _inputs(rows, nv, d, seed):
+    rng = np.random.default_rng(seed)
+    o = (rng.standard_normal((rows, nv * d)) * rng.choice([1e-3, 0.1, 3.0], size=(rows, 1))).astype(np.float32)
+    z = rng.standard_normal((rows, nv * d)).astype(np.float32)
+    z[0, (nv - 1) * d:] = 0.0                         # one all-zero head: silu(0) = 0
+    gn = gs.norm_weight(seed, d)
+    return o, z, gn
+
+
+def _ref(o, z, gn, nv, d):
+    rows = o.shape[0]
+    return oracle.gated_rmsnorm(o.astype(np.float64).reshape(rows * nv, d), z.reshape(rows * nv, d), gn,
+                                EPS).reshape(rows, nv * d)
+
+
+@pytest.mark.parametrize("rows,nv,d,pad", [(5, 3, 128, 3), (5, 3, 128, 4), (1000, 48, 128, 0), (33, 2, 64, 4),
+                                            (4, 3, 5, 0), (3, 2, 256, 8), (1, 48, 128, 4)])
+def test_bf16(rows, nv, d, pad):
+    """pad = 0 or a multiple of 4 keeps D = 128 rows 16-byte aligned (the vector kernel); 3 does not."""
+    o, z, gn = _inputs(rows, nv, d, seed=300 + d + pad)
+    hv = nv * d
+    ob, zb, gb = Rows(rows, hv, hv + pad), Rows(rows, hv, hv + 2 * pad), Rows(1, d)
+    out = Rows(rows, hv, hv + 4 * pad, torch.int16)
+    ob.write(o); zb.write(z); gb.write(gn)
+    gdn.gdn_gate_norm(ob.ptr, zb.ptr, gb.ptr, out.ptr, rows=rows, nv=nv, d=d, eps=EPS, o_stride=ob.stride,
+                      z_stride=zb.stride, out_stride=out.stride)
+    torch.cuda.synchronize()
+    got = bf16_to_f64(out.read())
+    assert rel_l2(got, _ref(o, z, gn, nv, d)) <= TOL_REL_L2
+    assert not got[0, (nv - 1) * d:].any()
+    assert all(b.intact() for b in (ob, zb, gb, out)), "guard band or padding overwritten"
+
+
+@pytest.mark.parametrize("rows,nv,d,with_y,pad", [(6, 3, 128, True, 4), (6, 3, 128, True, 1), (777, 48, 128, True, 0),
+                                                  (9, 2, 64, True, 4), (2, 4, 32, True, 4), (3, 2, 256, True, 4),
+                                                  (6, 3, 128, False, 4)])
+def test_q8(rows, nv, d, with_y, pad):
+    """pad 4 / 0: the D = 128 vector kernel (int8 groups over 8 lanes); pad 1: the general kernel."""
+    o, z, gn = _inputs(rows, nv, d, seed=400 + d + pad)
+    hv = nv * d
+    ob, zb, gb = Rows(rows, hv, hv + pad), Rows(rows, hv, hv + pad), Rows(1, d)
+    xq, xs = Rows(rows, hv, hv + 16, torch.int8), Rows(rows, hv // 32, hv // 32 + 2)
+    yb = Rows(rows, hv, hv + 4) if with_y else None
+    ob.write(o); zb.write(z); gb.write(gn)
+    gdn.gdn_gate_norm_q8(ob.ptr, zb.ptr, gb.ptr, xq.ptr, xs.ptr, yb.ptr if yb else None, rows=rows, nv=nv, d=d,
+                         eps=EPS, o_stride=ob.stride, z_stride=zb.stride, xq_stride=xq.stride,
+                         xs_stride=xs.stride, y_stride=yb.stride if yb else 0)
+    torch.cuda.synchronize()
+    ref = _ref(o, z, gn, nv, d).reshape(-1)
+    codes = xq.read().reshape(-1).astype(np.int64)
+    scales = xs.read().reshape(-1)
+    step = np.repeat(scales.astype(np.float64), 32)
+    assert np.all(np.abs(codes * step - ref) <= 0.5 * step * (1 + 1e-6) + TOL_F32 * np.max(np.abs(ref)))
+    g0 = ((nv - 1) * d) // 32
+    assert np.all(scales[g0:g0 + d // 32] == 1.0) and not codes[(nv - 1) * d:nv * d].any()
+    if yb is not None:
+        y = yb.read().reshape(-1)
+        assert max_rel_err(y, ref) <= TOL_F32, max_rel_err(y, ref)
+        c_ref, s_ref = oracle.quant_q8(y)
+        assert np.array_equal(codes, c_ref.astype(np.int64)), "codes differ from the fp32 quantiser's"
+        assert np.array_equal(scales.view(np.uint32), s_ref.view(np.uint32)), "scales differ"
+    bufs = [ob, zb, gb, xq, xs] + ([yb] if yb else [])
+    assert all(b.intact() for b in bufs), "guard band or padding overwritten"
+
+
+def test_prefill_then_norm():
+    """gdn_prefill_seq's raw o for every token, normed by gdn_gate_norm: against the oracle's prefill
+    followed by its norm."""
+    B, NK, NV, D, T = 2, 2, 6, 128, 20
+    rows = B * T
+    x = gs.prefill_inputs(7, B, T, NK, NV, D)
+    z = np.stack([gs.decode_inputs(7, B, NK, NV, D, step=t)["z"] for t in range(T)], axis=1).reshape(rows, NV * D)
+    gn = gs.norm_weight(7, D)
+    S0 = gs.state_heads(7, range(B), range(NV), D)
+    dev = torch.device("cuda")
+    t = {k: torch.from_numpy(np.ascontiguousarray(v.reshape(rows, -1))).to(dev) for k, v in x.items()}
+    S = torch.from_numpy(S0).to(dev)
+    o = torch.empty((rows, NV * D), device=dev)
+    gdn.gdn_prefill_seq(S, t["q"], t["k"], t["v"], t["alpha"], t["beta"], o, batch=B, seq_len=T, nk=NK, nv=NV, d=D)
+    out = torch.empty((rows, NV * D), dtype=torch.int16, device=dev)
+    gdn.gdn_gate_norm(o, torch.from_numpy(z).to(dev), torch.from_numpy(gn).to(dev), out, rows=rows, nv=NV, d=D,
+                      eps=EPS)
+    torch.cuda.synchronize()
+    o_ref = oracle.prefill(S0.astype(np.float64), x["q"], x["k"], x["v"], x["alpha"], x["beta"], NK)
+    ref = oracle.gated_rmsnorm(o_ref.reshape(rows * NV, D), z.reshape(rows * NV, D), gn, EPS)
+    assert rel_l2(bf16_to_f64(out.cpu().numpy()).reshape(rows * NV, D), ref) <= TOL_REL_L2
