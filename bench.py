@@ -324,6 +324,9 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- e2e: host inputs in pinned memory -> device, 48 launches, bf16 outputs -> host
     e2e = None if args.no_e2e else run_e2e(args, torch, gdn, state, x, outb, dev, stream, not args.no_graph)
+    if e2e is not None and world > 1:          # whole job: the slowest rank's step, every rank's units
+        e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], world, dev)
+        e2e["value"] = job_throughput(B * NV * L, world, e2e["ms_per_step"])
     del state, x, outb
     torch.cuda.empty_cache()
 

@@ -20,9 +20,7 @@
 //    costs three multiply-adds per element (u, the rank-1 write into R, o)
 //    instead of four; gam is folded back into R before it could underflow
 //    (below 2^-32, or alpha = 0);
-//  * the multiply-adds are Blackwell's paired fp32 FMA (fma.rn.f32x2), two
-//    lanes of work per issued instruction, which leaves issue slots for the
-//    shared loads;
+//  * the multiply-adds work on element pairs (float2) held in registers;
 //  * a CTA is one warp (32 rows of one head).  With ~168 registers a thread
 //    an SM holds 11-12 such warps, and one-warp CTAs let the block scheduler
 //    spread the B*NV*D/32 warps evenly over the SMs (a 4-warp CTA per head
@@ -98,18 +96,15 @@ __device__ __forceinline__ void stage_chunk(Stage &st, const PrefillParams &p, i
     }
 }
 
+// Element pairs through scalar fp32 FMA / multiply.  (The paired form,
+// fma.rn.f32x2, gives the same bits; at this kernel's occupancy -- about ten
+// warps per SM -- scalar FMA issues faster on GB300: 95 vs ~80 FMA per clock
+// per SM in a pure FMA loop, 4.43 vs 4.50 ms here.)
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    unsigned long long ra = *reinterpret_cast<unsigned long long *>(&a);
-    unsigned long long rb = *reinterpret_cast<unsigned long long *>(&b);
-    unsigned long long rc = *reinterpret_cast<unsigned long long *>(&c), rd;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-    return *reinterpret_cast<float2 *>(&rd);
+    return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
 }
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-    unsigned long long ra = *reinterpret_cast<unsigned long long *>(&a);
-    unsigned long long rb = *reinterpret_cast<unsigned long long *>(&b), rd;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
-    return *reinterpret_cast<float2 *>(&rd);
+    return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
 }
 
 // Four consecutive state elements <-> fp32 (fp16: one 8-byte access, rounded to
