@@ -19,7 +19,10 @@
 //    scalar gam (the product of the alphas since the last fold), so a token
 //    costs three multiply-adds per element (u, the rank-1 write into R, o)
 //    instead of four; gam is folded back into R before it could underflow
-//    (below 2^-32, or alpha = 0);
+//    (below 2^-32, or alpha = 0).  The write into R needs coef / gam: it is
+//    taken as coef * (1/gam), with 1/alpha computed once per staged token and
+//    1/gam re-derived exactly at every chunk, so no division sits in the
+//    token loop and the running reciprocal drifts over at most 8 tokens;
 //  * the multiply-adds work on element pairs (float2) held in registers;
 //  * a CTA is one warp (32 rows of one head).  With ~168 registers a thread
 //    an SM holds 11-12 such warps, and one-warp CTAs let the block scheduler
@@ -46,6 +49,7 @@ struct __align__(16) Stage {
     float v[kTC][kRows];
     float alpha[kTC];
     float beta[kTC];
+    float inv_alpha[kTC];         // 1 / alpha, computed once per chunk after it lands
 };
 
 __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
@@ -159,7 +163,7 @@ prefill_d128(const PrefillParams p)
             R[rr][2 * jj + 1] = make_float2(t.z, t.w);
         }
     }
-    float gam = 1.0f;
+    float gam = 1.0f, inv_gam = 1.0f;
 
     float *orow = p.o + (int64_t)seq * T * p.o_stride + (int64_t)h * kD + a0 + half;
     const unsigned lane_off = 16u * half;
@@ -173,8 +177,11 @@ prefill_d128(const PrefillParams p)
             cp_async_wait<0>();
         }
         __syncwarp();
-        const Stage &st = ring[c & 1];
+        Stage &st = ring[c & 1];
         const int n = min(kTC, T - c * kTC);
+        if (lane < n) st.inv_alpha[lane] = 1.0f / st.alpha[lane];
+        inv_gam = 1.0f / gam;          // exact once a chunk: the running product drifts at most 8 steps
+        __syncwarp();
         const unsigned k_s = (unsigned)__cvta_generic_to_shared(st.k[0]) + lane_off;
         const unsigned q_s = (unsigned)__cvta_generic_to_shared(st.q[0]) + lane_off;
         for (int tt = 0; tt < n; ++tt) {
@@ -200,7 +207,8 @@ prefill_d128(const PrefillParams p)
             const unsigned k2 = after(kt, coef_a, p.zero), q2 = after(qt, coef_b, p.zero);
             float2 oa0 = make_float2(0.f, 0.f), oa1 = oa0, ob0 = oa0, ob1 = oa0;
             if (gnew >= kMinScale) {            // warp-uniform: one head per warp
-                const float ca = coef_a / gnew, cb = coef_b / gnew;
+                const float inv_gnew = inv_gam * st.inv_alpha[tt];
+                const float ca = coef_a * inv_gnew, cb = coef_b * inv_gnew;
                 const float2 ca2 = make_float2(ca, ca), cb2 = make_float2(cb, cb);
 #pragma unroll
                 for (int jj = 0; jj < kD / 8; ++jj) {
@@ -217,6 +225,7 @@ prefill_d128(const PrefillParams p)
                     ob1 = ffma2(R[1][2 * jj + 1], q23, ob1);
                 }
                 gam = gnew;
+                inv_gam = inv_gnew;
             } else {
                 const float2 g2 = make_float2(gnew, gnew);
                 const float2 ca2 = make_float2(coef_a, coef_a), cb2 = make_float2(coef_b, coef_b);
@@ -235,6 +244,7 @@ prefill_d128(const PrefillParams p)
                     ob1 = ffma2(R[1][2 * jj + 1], q23, ob1);
                 }
                 gam = 1.0f;
+                inv_gam = 1.0f;
             }
             float sa = (oa0.x + oa0.y) + (oa1.x + oa1.y);
             float sb = (ob0.x + ob0.y) + (ob1.x + ob1.y);
