@@ -13,9 +13,10 @@
 // `gdn_step` and `gdn_gate_norm`.
 //
 // GB300 design.  The page's launcher gives one block to a key head and its
-// NV/NK value heads.  Here every value head keeps one CTA -- the decode
-// kernel's shape (8 warps x 16 rows), so the 64 KB-per-head state stream is
-// unchanged and no CTA waits for another:
+// NV/NK value heads.  For fp32 states every value head keeps one CTA here --
+// the decode kernel's shape (8 warps x 16 rows), so the 64 KB-per-head state
+// stream is unchanged and no CTA waits for another (fp16 states take the
+// page's per-key-head shape, conv_norm_kh below, which measured faster there):
 //  * every CTA issues its state loads first, then updates the ring rows of its
 //    own value head's v channels and computes v (one writer per ring row);
 //  * every CTA also computes the key head's q and k (conv, silu, L2: 256
@@ -283,6 +284,176 @@ conv_norm_d128(const ConvNormParams p)
     }
 }
 
+// One CTA per (sequence, key head) and its R = NV/NK value heads (the page's
+// block shape; taken for fp16 states): q and k are computed once, every ring
+// row of the key head is written in place by its only owner (no counter), and
+// the value heads are stepped one after another from NBUF shared-memory
+// buffers, head r + NBUF loading while head r is stepped.  With an fp16 head
+// only 32 KB, the per-value-head kernel spent more on recomputing the key
+// head's q and k three times than on the state stream.
+constexpr int kMaxRepeat = 8;
+
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+    switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
+    }
+}
+
+template <typename TS, int NBUF, int MINB>
+__global__ void __launch_bounds__(kWarps * 32, MINB)
+conv_norm_kh(const ConvNormParams p)
+{
+    using V = Vec16<TS>;
+    constexpr int EPV = V::N;
+    constexpr int LPR = kD / EPV;
+    constexpr int RPL = 32 / LPR;
+    constexpr int NLD = kRowsPerWarp / RPL;
+    constexpr int VPR = kD * (int)sizeof(TS) / 16;
+    constexpr int PER = NLD / kGroups;
+    constexpr int HEAD_BYTES = kD * kD * (int)sizeof(TS);
+    static_assert(NLD % kGroups == 0 && NBUF * kGroups - 1 <= 7, "shape");
+
+    extern __shared__ __align__(16) unsigned char smem_raw[];   // NBUF heads, [kD rows][VPR] each
+    __shared__ __align__(16) float q_s[kD];
+    __shared__ __align__(16) float k_s[kD];
+    __shared__ float v_s[kMaxRepeat][kD];
+    __shared__ float red_qk[kWarps], red[2][kWarps];
+    __shared__ float gate_s[kMaxRepeat][2];
+
+    const int cl = blockIdx.x;                          // (sequence, key head)
+    const int seq = cl / p.nk;
+    const int kh = cl - seq * p.nk;
+    const int R = p.repeat;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int sub = lane / LPR;
+    const int col = (lane % LPR) * EPV;
+    const int row0 = warp * kRowsPerWarp;
+    const int64_t C = (int64_t)(2 * p.nk + p.nv) * kD;
+    TS *state_seq = reinterpret_cast<TS *>(p.state) + seq * p.pitch;
+
+    auto rowp_of = [&](int r) {
+        return state_seq + (int64_t)(kh + r * p.nk) * kD * kD + (int64_t)(row0 + sub) * kD + col;
+    };
+    auto mine_of = [&](int buf) {
+        return reinterpret_cast<uint4 *>(smem_raw + buf * HEAD_BYTES) + (row0 + sub) * VPR + (lane % LPR);
+    };
+    auto issue = [&](int r) {                           // head r into buffer r % NBUF, kGroups groups
+        TS *rp = rowp_of(r);
+        uint4 *m = mine_of(r % NBUF);
+#pragma unroll
+        for (int gi = 0; gi < kGroups; ++gi) {
+#pragma unroll
+            for (int ii = 0; ii < PER; ++ii) {
+                const int i = gi * PER + ii;
+                cp_async16(m + i * RPL * VPR, rp + (int64_t)i * RPL * kD);
+            }
+            cp_async_commit();
+        }
+    };
+
+    // 1. the first heads' state in flight before the producers run
+    for (int r = 0; r < NBUF && r < R; ++r) issue(r);
+
+    // 2. producers: q (threads 0..127) and k (128..255) of the key head, then the v channels of its
+    //    value heads; this CTA owns every one of these ring rows, so each is shifted in place
+    float *ring = p.ring + seq * p.ring_pitch;
+    const float *x = p.x + seq * p.x_stride;
+    {
+        const int i = tid & (kD - 1);
+        const int64_t c = tid < kD ? (int64_t)kh * kD + i : (int64_t)(p.nk + kh) * kD + i;
+        const float val = conv_silu_channel(ring, x, p.w, c, C, p.taps);
+        const float sq = group_sum<32>(val * val);
+        if (lane == 0) red_qk[warp] = sq;
+        __syncthreads();
+        const int w0 = tid < kD ? 0 : 4;
+        const float t = (red_qk[w0] + red_qk[w0 + 1]) + (red_qk[w0 + 2] + red_qk[w0 + 3]);
+        (tid < kD ? q_s : k_s)[i] = val / sqrtf(t + p.l2_eps);
+    }
+    for (int j = tid; j < R * kD; j += kWarps * 32) {
+        const int r = j / kD, i = j - r * kD;
+        v_s[r][i] = conv_silu_channel(ring, x, p.w, 2 * (int64_t)p.nk * kD + (int64_t)(kh + r * p.nk) * kD + i,
+                                      C, p.taps);
+    }
+    if (tid < R) gates(p, seq, kh + tid * p.nk, gate_s[tid][0], gate_s[tid][1]);
+    __syncthreads();
+
+    float kx[EPV], qx[EPV];
+#pragma unroll
+    for (int j = 0; j < EPV; j += 4) {
+        const float4 a = *reinterpret_cast<const float4 *>(k_s + col + j);
+        const float4 b = *reinterpret_cast<const float4 *>(q_s + col + j);
+        kx[j] = a.x; kx[j + 1] = a.y; kx[j + 2] = a.z; kx[j + 3] = a.w;
+        qx[j] = b.x; qx[j + 1] = b.y; qx[j + 2] = b.z; qx[j + 3] = b.w;
+    }
+    float kq = 0.f;
+#pragma unroll
+    for (int j = 0; j < EPV; ++j) kq = fmaf(kx[j], qx[j], kq);
+    kq = group_sum<LPR>(kq);
+    const bool row_lane = lane < kRowsPerWarp;
+    const float gn_l = row_lane ? __ldg(p.gn + row0 + lane) : 0.f;
+
+    // 3. the value heads in turn
+    for (int r = 0; r < R; ++r) {
+        const int h = kh + r * p.nk;
+        TS *rowp = rowp_of(r);
+        const uint4 *mine = mine_of(r % NBUF);
+        const int later = min(NBUF - 1, R - 1 - r);     // heads issued after this one
+        const float v_l = row_lane ? v_s[r][row0 + lane] : 0.f;
+        const float z_l = row_lane ? __ldg(p.z + seq * p.z_stride + (int64_t)h * kD + row0 + lane) : 0.f;
+        const float alpha = gate_s[r][0], beta = gate_s[r][1];
+        float o_keep = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < kGroups; ++gi) {
+            cp_async_wait_n(kGroups - 1 - gi + kGroups * later);
+#pragma unroll
+            for (int ii = 0; ii < PER; ++ii) {
+                const int i = gi * PER + ii;
+                float s[EPV];
+                V::unpack(mine[i * RPL * VPR], s);
+                float u = 0.f, w = 0.f;
+#pragma unroll
+                for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
+                u = group_sum<LPR>(u);
+                w = group_sum<LPR>(w);
+                const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
+                const float coef = beta * (va - alpha * u);
+                const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
+#pragma unroll
+                for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
+                st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
+                if constexpr (RPL == 1) {
+                    if (lane == i) o_keep = oa;
+                } else {
+#pragma unroll
+                    for (int rr = 0; rr < RPL; ++rr) {
+                        const float orr = __shfl_sync(kFull, oa, rr * LPR);
+                        if (lane == i * RPL + rr) o_keep = orr;
+                    }
+                }
+            }
+        }
+        const float ss = group_sum<32>(o_keep * o_keep);
+        if (lane == 0) red[r & 1][warp] = ss;
+        __syncthreads();                                // also: every warp is done with this buffer
+        float tot = 0.f;
+#pragma unroll
+        for (int i = 0; i < kWarps; ++i) tot += red[r & 1][i];
+        const float rstd = rsqrtf(tot * (1.0f / kD) + p.eps);
+        if (row_lane) {
+            const float y = gn_l * o_keep * rstd * silu(z_l);
+            p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
+        }
+        if (r + NBUF < R) issue(r + NBUF);
+    }
+}
+
 // Any 1 <= D <= 256, any alignment, any NV/NK: one CTA per (sequence, key
 // head); the producers for the key head and all of its value heads go to
 // shared memory, then the value heads are stepped one after the other (warp
@@ -387,11 +558,11 @@ conv_norm_generic(const ConvNormParams p)
     }
 }
 
-// Shapes of the D == 128 kernel, by measurement on GB300 (one layer at batch 32
-// fp32, 256-slot fp16 pool): fp32 register batches (4 x 4 loads, 4 CTAs per
-// SM: a CTA spends part of its life in the producer phase, so more of them
-// keep the state streaming); fp16 staged in shared memory (32 KB + 10 KB a
-// CTA, 5 CTAs per SM).
+// Shapes of the per-value-head D == 128 kernel, by measurement on GB300 (one
+// layer at batch 32 fp32, 256-slot fp16 pool): fp32 register batches (4 x 4
+// loads, 4 CTAs per SM: a CTA spends part of its life in the producer phase,
+// so more of them keep the state streaming); fp16 staged in shared memory
+// (32 KB + 10 KB a CTA, 5 CTAs per SM) -- used for fp16 only when NV/NK > 8.
 template <typename TS> struct ConvShape {
     static constexpr bool kStaged = false;
     static constexpr int kBatches = 4, kMinBlocks = 4;
@@ -404,6 +575,15 @@ template <> struct ConvShape<__half> {
 template <typename TS>
 cudaError_t launch_typed(const ConvNormParams &p, bool fast, cudaStream_t s)
 {
+    if constexpr (sizeof(TS) == 2) {
+        if (fast && p.repeat <= kMaxRepeat) {            // one CTA per key head, one staging buffer
+            constexpr auto kern = conv_norm_kh<TS, 1, 5>;
+            const cudaError_t e = allow_dynamic_smem<kern>(stage_bytes<TS>());
+            if (e != cudaSuccess) return e;
+            kern<<<(unsigned)((int64_t)p.batch * p.nk), kWarps * 32, stage_bytes<TS>(), s>>>(p);
+            return cudaGetLastError();
+        }
+    }
     if (fast) {
         using F = ConvShape<TS>;
         constexpr auto kern = conv_norm_d128<TS, F::kStaged, F::kBatches, F::kMinBlocks>;

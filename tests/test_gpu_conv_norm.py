@@ -3,9 +3,10 @@ the gated norm, in one launch) against the fp64 oracle composed from its parts.
 
 The conv state update is a pure data move (shift by one, append the token), so it is compared bit
 for bit; the h-state and the bf16 output use the fp32 / fp16-state / bf16 bars of the other tests.
-NV/NK = 1, 3, 8 and 9 run on the D = 128 kernel (one CTA per value head, the last reader of a key
-head's q/k ring rows writes them); D != 128 and a misaligned state run on the general kernel.  The
-workspace counters must be zero again after every call."""
+NV/NK = 1, 3, 8 and 9 run on the D = 128 kernels: fp32 (and fp16 with NV/NK = 9) on the one with a
+CTA per value head, where the last reader of a key head's q/k ring rows writes them; fp16 with
+NV/NK <= 8 on the one with a CTA per key head.  D != 128 and a misaligned state run on the general
+kernel.  The workspace counters must be zero again after every call."""
 import numpy as np
 import pytest
 import torch
