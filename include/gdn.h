@@ -205,10 +205,13 @@ GDN_API int gdn_gate_norm_q8(const float *o, const float *z, const float *gn, fl
  *   z, gn, eps, out as gdn_decode_norm; l2_eps >= 0 for the q/k norm.
  *   workspace    [batch*NK] int32 counters owned by the caller: zero before
  *                the first call (e.g. cudaMemsetAsync); every call leaves
- *                them zero.  The value heads of a key head each read its
- *                q/k ring rows, and the counters let the last reader write
- *                them.  Calls that can overlap on the GPU need separate
- *                workspaces (and separate conv states).
+ *                them zero.  Where the kernel gives each value head its own
+ *                block (fp32 states, or NV/NK > 8), the value heads of a key
+ *                head each read its q/k ring rows and the counters let the
+ *                last reader write them; the fp16 kernel (one block per key
+ *                head) does not touch them.  Always required.  Calls that can
+ *                overlap on the GPU need separate workspaces (and separate
+ *                conv states).
  *   NV must be a multiple of NK (the value heads of a key head are h = kh +
  *   r*NK, r < NV/NK).  State and output as gdn_decode_norm.
  *   Errors as gdn_decode_norm; GDN_ERR_UNSUPPORTED if NV % NK != 0.
