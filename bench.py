@@ -89,10 +89,13 @@ def peaks():
     return {"hbm_gbs": 6800.0, "source": "fallback", "sm_max_mhz": 2070.0}
 
 
-def src_sha(name):
-    p = os.path.join(ROOT, "gated_deltanet_linear_16_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def src_sha(*names):
+    """sha256 over the named kernel sources, in order (the kernel and the header it includes)."""
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "gated_deltanet_linear_16_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 # ------------------------------------------------------------------ clocks
@@ -320,7 +323,7 @@ def run_ours(args, rank, world, local_rank):
     pk = peaks()
     achieved = bytes_launch / launch_s / 1e9
     tr = NCU_TRAFFIC["decode_norm_f32"]
-    traffic = tr["bytes_per_launch"] if tr["src_sha256"] == src_sha("gdn_decode.cu") else None
+    traffic = tr["bytes_per_launch"] if tr["src_sha256"] == src_sha("gdn_decode.cu", "gdn_internal.cuh") else None
 
     # ---- e2e: host inputs in pinned memory -> device, 48 launches, bf16 outputs -> host
     e2e = None if args.no_e2e else run_e2e(args, torch, gdn, state, x, outb, dev, stream, not args.no_graph)
@@ -432,6 +435,21 @@ def time_fn(torch, stream, fn, reps, warm=2):
     return e0.elapsed_time(e1) / reps / 1e3     # seconds per call
 
 
+# Rows on one layer at batch 32 (100 MB of fp32 state, under the 129 MB L2) cycle through this many
+# layers' states, so every launch streams its state from HBM as a model's layers do.
+ROW_LAYERS = 8
+
+
+def cycling(fns):
+    """One callable that runs fns[0], fns[1], ... in turn, one per call."""
+    it = [0]
+
+    def call():
+        fns[it[0] % len(fns)]()
+        it[0] += 1
+    return call
+
+
 def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096, graph=True):
     want = set(only.split(",")) if only else {"fp16", "conv", "latency", "prefill", "chunk2", "convnorm", "q8"}
     rows = {}
@@ -454,8 +472,8 @@ def run_rows(torch, gdn, dev, stream, pk, only=None, prefill_tokens=4096, graph=
 
 def row_conv_norm(torch, gdn, dev, stream, pk, taps=4):
     """Fused decode from projections (conv ring update + silu, q/k L2 norm, gates from logits, the
-    step and the gated norm in one launch): one layer at batch 32 with an fp32 state (also through
-    the allocation-free entry point), and the 256-slot fp16 pool."""
+    step and the gated norm in one launch): batch 32 with fp32 states, ROW_LAYERS layers' states and
+    conv rings in turn (also through the allocation-free entry point), and the 256-slot fp16 pool."""
     import gdn_synth as gs
     C = (2 * NK + NV) * D
     res = {}
@@ -464,26 +482,31 @@ def row_conv_norm(torch, gdn, dev, stream, pk, taps=4):
         t = {k: torch.from_numpy(v).to(dev) for k, v in x.items()}
         g = torch.Generator(device=dev)
         g.manual_seed(3)
-        S = torch.empty((batch, NV * D * D), device=dev).normal_(0.0, 0.02, generator=g)
+        nl = 1 if f16 else ROW_LAYERS                  # the fp16 pool (403 MB) is larger than L2 alone
+        S = torch.empty((nl, batch, NV * D * D), device=dev).normal_(0.0, 0.02, generator=g)
         if f16:
             S = S.half()
-        ring = t["ring"].reshape(batch, taps * C).contiguous()
+        ring = t["ring"].reshape(1, batch, taps * C).repeat(nl, 1, 1).contiguous()
         gn = torch.from_numpy(gs.norm_weight(SEED, D)).to(dev)
         out = torch.empty((batch, NV * D), dtype=torch.int16, device=dev)
         ws = torch.zeros(batch * NK, dtype=torch.int32, device=dev)
-        args = (S, ring, t["x"], t["conv_w"], t["br"], t["ar"], t["dt"], t["rate"], t["z"], gn, out)
+        args = [(S[l], ring[l], t["x"], t["conv_w"], t["br"], t["ar"], t["dt"], t["rate"], t["z"], gn, out)
+                for l in range(nl)]
         kw = dict(batch=batch, nk=NK, nv=NV, d=D, taps=taps, stream=stream.cuda_stream)
-        s = time_fn(torch, stream, lambda: gdn.gdn_decode_conv_norm(*args, ws, **kw), 50 if not f16 else 20)
+        s = time_fn(torch, stream, cycling([lambda a=a: gdn.gdn_decode_conv_norm(*a, ws, **kw) for a in args]),
+                    48 if not f16 else 20)
         es = 2 if f16 else 4
         # state read + write; ring: taps-1 entries read, all taps written; x, z read; w, dt, rate, gn
         # once; gate logits read; bf16 out written
         by = (batch * NV * D * D * es * 2 + batch * ((taps - 1) + taps + 1) * C * 4 + taps * C * 4
               + batch * NV * D * 4 + batch * NV * 2 * 4 + 2 * NV * 4 + D * 4 + batch * NV * D * 2)
-        r = {"config": f"B={batch} NK=16 NV=48 D=128 {'fp16' if f16 else 'fp32'}, 4-tap conv",
+        r = {"config": f"B={batch} NK=16 NV=48 D=128 {'fp16' if f16 else 'fp32'}, 4-tap conv"
+                       + ("" if f16 else f", {nl} layers' states in turn"),
              "us_per_launch": s * 1e6, "token_heads_per_s": batch * NV / s, "achieved_gbs": by / s / 1e9,
              "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}
         if not f16:
-            s2 = time_fn(torch, stream, lambda: gdn.gdn_decode_conv_norm_noalloc(*args, **kw), 50)
+            s2 = time_fn(torch, stream, cycling([lambda a=a: gdn.gdn_decode_conv_norm_noalloc(*a, **kw)
+                                                 for a in args]), 48)
             r["noalloc_us_per_launch"] = s2 * 1e6
         res[label] = r
         del S, ring, gn, out, t, ws, args
@@ -492,11 +515,11 @@ def row_conv_norm(torch, gdn, dev, stream, pk, taps=4):
 
 
 def row_q8(torch, gdn, dev, stream, pk):
-    """Decode + gated norm with the int8 epilogue (groups of 32, one fp32 scale each) on one
-    layer at batch 32 (fp32 state), next to the bf16 epilogue on the same inputs."""
+    """Decode + gated norm with the int8 epilogue (groups of 32, one fp32 scale each) at batch 32
+    (fp32 states, ROW_LAYERS layers' states in turn), next to the bf16 epilogue on the same inputs."""
     g = torch.Generator(device=dev)
     g.manual_seed(4)
-    S = torch.empty((B, NV, D, D), device=dev).normal_(0.0, 0.02, generator=g)
+    S = torch.empty((ROW_LAYERS, B, NV, D, D), device=dev).normal_(0.0, 0.02, generator=g)
     q = torch.randn((B, NK, D), device=dev, generator=g)
     q = (q / q.norm(dim=-1, keepdim=True)).view(B, NK * D).contiguous()
     k = torch.randn((B, NK, D), device=dev, generator=g)
@@ -510,26 +533,30 @@ def row_q8(torch, gdn, dev, stream, pk):
     xs = torch.empty((B, NV * D // 32), device=dev)
     out = torch.empty((B, NV * D), dtype=torch.int16, device=dev)
     kw = dict(batch=B, nk=NK, nv=NV, d=D, stream=stream.cuda_stream)
-    s_q8 = time_fn(torch, stream, lambda: gdn.gdn_decode_norm_q8(S, q, k, v, a, bt, z, gn, xq, xs, None, **kw), 50)
-    s_bf = time_fn(torch, stream, lambda: gdn.gdn_decode_norm(S, q, k, v, a, bt, z, gn, out, **kw), 50)
+    s_q8 = time_fn(torch, stream, cycling([lambda l=l: gdn.gdn_decode_norm_q8(S[l], q, k, v, a, bt, z, gn, xq, xs,
+                                                                            None, **kw) for l in range(ROW_LAYERS)]), 48)
+    s_bf = time_fn(torch, stream, cycling([lambda l=l: gdn.gdn_decode_norm(S[l], q, k, v, a, bt, z, gn, out, **kw)
+                                           for l in range(ROW_LAYERS)]), 48)
     by = B * NV * D * D * 4 * 2 + B * (2 * NK * D + 2 * NV * D + 2 * NV) * 4 + D * 4 + B * NV * D * (1 + 4 / 32)
     del S, q, k, v, z, a, bt, gn, xq, xs, out
     torch.cuda.empty_cache()
     return {"decode_norm_int8_epilogue": {
-        "config": "B=32 NK=16 NV=48 D=128 fp32, int8 codes + fp32 scale per 32 outputs", "us_per_launch": s_q8 * 1e6,
+        "config": f"B=32 NK=16 NV=48 D=128 fp32, int8 codes + fp32 scale per 32 outputs, {ROW_LAYERS} layers' "
+                  "states in turn", "us_per_launch": s_q8 * 1e6,
         "bf16_epilogue_us_per_launch": s_bf * 1e6, "achieved_gbs": by / s_q8 / 1e9,
         "frac_of_hbm_peak": by / s_q8 / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}}
 
 
 def row_chunk2(torch, gdn, dev, stream, pk):
-    """Two-token verify step, one layer at batch 32 (fp32 state) and on the 256-slot fp16 pool: the
-    state is read once and written twice (intermediate + final); both tokens' inputs read, both
-    outputs written."""
+    """Two-token verify step at batch 32 (fp32 states, ROW_LAYERS layers' states in turn) and on the
+    256-slot fp16 pool: the state is read once and written twice (intermediate + final); both
+    tokens' inputs read, both outputs written."""
     res = {}
     for label, batch, f16 in (("fp32_b32", B, False), ("fp16_pool_b256", 256, True)):
         g = torch.Generator(device=dev)
         g.manual_seed(2)
-        S = torch.empty((batch, NV, D, D), device=dev).normal_(0.0, 0.02, generator=g)
+        nl = 1 if f16 else ROW_LAYERS
+        S = torch.empty((nl, batch, NV, D, D), device=dev).normal_(0.0, 0.02, generator=g)
         if f16:
             S = S.half()
         M = torch.empty_like(S)
@@ -542,11 +569,14 @@ def row_chunk2(torch, gdn, dev, stream, pk):
         a = torch.sigmoid(torch.randn((R, NV), device=dev, generator=g) + 2.0)
         bt = torch.sigmoid(torch.randn((R, NV), device=dev, generator=g))
         o = torch.empty((R, NV * D), device=dev)
-        s = time_fn(torch, stream, lambda: gdn.gdn_decode_chunk2(S, M, q, k, v, a, bt, o, batch=batch, nk=NK, nv=NV,
-                                                                 d=D, stream=stream.cuda_stream), 50 if not f16 else 20)
+        s = time_fn(torch, stream, cycling([lambda l=l: gdn.gdn_decode_chunk2(S[l], M[l], q, k, v, a, bt, o, batch=batch,
+                                                                             nk=NK, nv=NV, d=D,
+                                                                             stream=stream.cuda_stream)
+                                            for l in range(nl)]), 48 if not f16 else 20)
         es = 2 if f16 else 4
         by = batch * NV * D * D * es * 3 + R * (2 * NK * D + 2 * NV * D + 2 * NV) * 4
-        res[label] = {"config": f"B={batch} NK=16 NV=48 D=128 {'fp16' if f16 else 'fp32'}, two tokens per launch",
+        res[label] = {"config": f"B={batch} NK=16 NV=48 D=128 {'fp16' if f16 else 'fp32'}, two tokens per launch"
+                                + ("" if f16 else f", {nl} layers' states in turn"),
                       "us_per_launch": s * 1e6, "token_heads_per_s": R * NV / s,
                       "achieved_gbs": by / s / 1e9, "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"],
                       "algorithmic_bytes": by}
@@ -668,7 +698,12 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
     out = torch.empty((R, NV * D), dtype=torch.int16, device=dev)
     s_norm = time_fn(torch, stream, lambda: gdn.gdn_gate_norm(o, z, gn, out, rows=R, nv=NV, d=D, stream=sp), 5)
     norm_bytes = R * NV * D * (4 + 4 + 2) + D * 4
-    del z, gn, out
+    # the same into int8 groups of 32 with an fp32 scale each (gdn_gate_norm_q8, no fp32 copy)
+    xq = torch.empty((R, NV * D), dtype=torch.int8, device=dev)
+    xs = torch.empty((R, NV * D // 32), device=dev)
+    s_q8 = time_fn(torch, stream, lambda: gdn.gdn_gate_norm_q8(o, z, gn, xq, xs, rows=R, nv=NV, d=D, stream=sp), 5)
+    q8_bytes = R * NV * D * (4 + 4 + 1) + R * NV * D // 32 * 4 + D * 4
+    del z, gn, out, xq, xs
     th = PB * NV * T
     io = (2 * R * NK * D + R * NV * D * 2 + 2 * R * NV) * 4 + 2 * PB * NV * D * D * 4
     fma = th * D * D * 3                # per token-head: S.k, the rank-1 write, S.q (D^2 FMA each)
@@ -682,6 +717,9 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
                         "gate_norm_of_outputs": {"us": s_norm * 1e6, "achieved_gbs": norm_bytes / s_norm / 1e9,
                                                  "frac_of_hbm_peak": norm_bytes / s_norm / 1e9 / pk["hbm_gbs"],
                                                  "algorithmic_bytes": norm_bytes},
+                        "gate_norm_q8_of_outputs": {"us": s_q8 * 1e6, "achieved_gbs": q8_bytes / s_q8 / 1e9,
+                                                    "frac_of_hbm_peak": q8_bytes / s_q8 / 1e9 / pk["hbm_gbs"],
+                                                    "algorithmic_bytes": q8_bytes},
                         "ms": s * 1e3, "token_heads_per_s": th / s,
                         "roofline": {"bound": "alu", "achieved": fma / s / 1e12, "peak": fma_peak / 1e12,
                                      "unit": "T FP32 FMA/s", "frac": fma / s / fma_peak,

@@ -28,7 +28,7 @@ template <> struct Chunk2Shape<__half> {
     static constexpr int kWarps = 8, kBatches = 2, kMinBlocks = 3;
 };
 
-template <typename TS, int WARPS, int NB, int MINB>
+template <typename TS, int WARPS, int NB, int MINB, bool EARLY>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 chunk2_d128(const DecodeParams p)
 {
@@ -54,6 +54,7 @@ chunk2_d128(const DecodeParams p)
 
     TS *rowp = reinterpret_cast<TS *>(p.state) + seq * p.pitch + slice;
     TS *midp = reinterpret_cast<TS *>(p.state_mid) + seq * p.mid_pitch + slice;
+    early_start<EARLY>(reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD, p.pf_bytes);
 
     uint4 raw[NB > 1 ? 2 : 1][LPB];
 #pragma unroll
@@ -216,10 +217,17 @@ cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
 {
     const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
     using F = Chunk2Shape<TS>;
-    if (fast)
-        chunk2_d128<TS, F::kWarps, F::kBatches, F::kMinBlocks><<<grid, F::kWarps * 32, 0, s>>>(p);
-    else
-        chunk2_generic<TS><<<grid, kGenWarps * 32, 0, s>>>(p);
+    if (fast) {   // early launch (grids of a few waves) with a quarter of the head asked of the L2
+        if (early_grid(grid, F::kMinBlocks)) {
+            DecodeParams q = p;
+            q.pf_bytes = (unsigned)(kD * kD * sizeof(TS) / 4);
+            return launch_early(chunk2_d128<TS, F::kWarps, F::kBatches, F::kMinBlocks, true>, grid,
+                                F::kWarps * 32, 0, s, true, q);
+        }
+        return launch_early(chunk2_d128<TS, F::kWarps, F::kBatches, F::kMinBlocks, false>, grid, F::kWarps * 32,
+                            0, s, false, p);
+    }
+    chunk2_generic<TS><<<grid, kGenWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 namespace gdn {
 
@@ -35,6 +36,9 @@ struct DecodeParams {
     int8_t *xq;
     float *xs, *y;
     int64_t xq_stride, xs_stride, y_stride;
+    // set by the launcher: bytes of the CTA's state head an early-launched
+    // kernel asks the L2 for while it waits (see early_start)
+    unsigned pf_bytes;
 };
 
 // What the single-token kernels write after the step: raw o, the normed output
@@ -82,6 +86,7 @@ struct ConvNormParams {
     int64_t z_stride, out_stride;
     int batch, nk, nv, d, taps, repeat;   // repeat = NV / NK value heads per key head
     float l2_eps, eps, inv_sqrt_d;
+    unsigned pf_bytes;      // as DecodeParams::pf_bytes
 };
 
 // Launchers (one per translation unit family).  They pick the kernel variant
@@ -119,7 +124,65 @@ cudaError_t allow_dynamic_smem(int bytes)
     return e;
 }
 
+// Early launch.  A kernel launched with programmatic stream serialisation may
+// become resident while the kernel before it in the stream drains its last
+// CTAs, so its own start (and, with an L2 prefetch, its first state bytes)
+// overlaps that drain.  Measured on GB300: a gain for grids of a few waves
+// (one layer at batch 32: 3.4 waves, -4 to -6 % per launch with a quarter or
+// half of the head prefetched), a loss for grids of many waves (the 256-slot
+// fp16 pool: 20-27 waves, up to +3 % without a prefetch and +7 % with one),
+// so it is taken for grids of at most kEarlyMaxWaves waves of `ctas_per_sm`
+// CTAs per SM.
+constexpr int kEarlyMaxWaves = 4;
+inline bool early_grid(unsigned grid, int ctas_per_sm)
+{
+    return (int64_t)grid <= (int64_t)kEarlyMaxWaves * sm_count() * ctas_per_sm;
+}
+
+// Launch kern with programmatic stream serialisation when `early`, else as a
+// plain launch.  `early` only for a kernel instantiated with early_start<true>.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_early(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                         bool early, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // ---------------------------------------------------------------- device helpers
+
+// First statement of a kernel that launch_early may launch early (EARLY: the
+// kernel is compiled for, and only ever given, an early launch; the plain
+// variant carries none of this code, which measured 1-4 % slower on plain
+// launches even with nothing to do).  In order: let the next kernel in the
+// stream launch early too; ask the L2 for the first `pf_bytes` of this CTA's
+// state head (threads 0..3 a quarter each; `head` 16-byte aligned, pf_bytes a
+// multiple of 64, 0 for none); wait until the previous kernel has completed
+// and its writes are visible.  Nothing is read or written before that wait:
+// an L2 prefetch is a hint and changes no value a load returns, so the results
+// are those of plain stream order whatever the previous kernel did.
+template <bool EARLY>
+__device__ __forceinline__ void early_start(const void *head, unsigned pf_bytes)
+{
+    if constexpr (EARLY) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (pf_bytes != 0 && threadIdx.x < 4) {
+            const char *b = static_cast<const char *>(head) + threadIdx.x * (pf_bytes / 4);
+            asm volatile("{ .reg .u64 ga; cvta.to.global.u64 ga, %0; cp.async.bulk.prefetch.L2.global [ga], %1; }"
+                         :: "l"(b), "r"(pf_bytes / 4) : "memory");
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+}
 
 // Streaming 16-byte global load / store: the state is touched once per call,
 // so keep it from displacing reusable lines (cache-streaming hint).

@@ -43,6 +43,17 @@
  *   that keep every row 16-byte aligned) are taken automatically; any other
  *   1 <= D <= 256 runs a general kernel with the same results up to fp32
  *   summation order.
+ * - Ordering: results are those of plain stream order.  When their grid is
+ *   a few waves at most (e.g. one layer at batch 32), the D == 128 kernels of
+ *   gdn_decode*, gdn_decode_chunk2 and (fp32 states) gdn_decode_conv_norm*
+ *   are launched with CUDA's programmatic stream serialisation: such a kernel
+ *   may become resident while the kernel before it in the stream is still
+ *   running, but reads and writes no memory until that kernel has completed
+ *   (meanwhile it only asks the L2 for part of its state, a hint), and it lets
+ *   the kernel after it start the same way.  A caller's kernel that follows
+ *   in the stream sees the outputs as usual; if it is itself launched with
+ *   that attribute it must wait for its grid dependency (griddepcontrol.wait)
+ *   before reading them, as that attribute always requires.
  */
 #ifndef GDN_H
 #define GDN_H
