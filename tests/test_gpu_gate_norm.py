@@ -109,3 +109,38 @@ def test_prefill_then_norm():
     o_ref = oracle.prefill(S0.astype(np.float64), x["q"], x["k"], x["v"], x["alpha"], x["beta"], NK)
     ref = oracle.gated_rmsnorm(o_ref.reshape(rows * NV, D), z.reshape(rows * NV, D), gn, EPS)
     assert rel_l2(bf16_to_f64(out.cpu().numpy()).reshape(rows * NV, D), ref) <= TOL_REL_L2
+
+
+@pytest.mark.parametrize("pad", [0, 1])
+def test_q8_near_ties(pad):
+    """Quotients y / scale planted within a few ulp of half-integers (the ties and near-ties of
+    round-half-even), on the vector kernel (pad 0) and the general one (pad 1): with z = 20
+    (silu(20) = 20 in fp32) and gn = 1, y is o times one per-head factor up to rounding, so o =
+    +-(k + 1/2) / 127 next to a group maximum of 1 puts 127 y / max|y| next to k + 1/2.  Codes
+    and scales must equal the oracle's fp32 quantiser on the kernel's own y bit for bit."""
+    rows, nv, d = 4, 3, 128
+    hv = nv * d
+    rng = np.random.default_rng(77)
+    k = rng.integers(0, 127, size=(rows, hv // 32, 32)).astype(np.float64)
+    o = rng.choice([-1.0, 1.0], size=k.shape) * (k + 0.5) / 127.0
+    o[:, :, 0] = rng.choice([-1.0, 1.0], size=(rows, hv // 32))       # the group maximum, |o| = 1
+    o = o.reshape(rows, hv).astype(np.float32)
+    z = np.full((rows, hv), 20.0, np.float32)
+    gn = np.ones(d, np.float32)
+    ob, zb, gb = Rows(rows, hv, hv + pad), Rows(rows, hv, hv + pad), Rows(1, d)
+    xq, xs, yb = Rows(rows, hv, hv + 16, torch.int8), Rows(rows, hv // 32, hv // 32 + 2), Rows(rows, hv, hv + 4)
+    ob.write(o); zb.write(z); gb.write(gn)
+    gdn.gdn_gate_norm_q8(ob.ptr, zb.ptr, gb.ptr, xq.ptr, xs.ptr, yb.ptr, rows=rows, nv=nv, d=d, eps=EPS,
+                         o_stride=ob.stride, z_stride=zb.stride, xq_stride=xq.stride, xs_stride=xs.stride,
+                         y_stride=yb.stride)
+    torch.cuda.synchronize()
+    y = yb.read().reshape(-1)
+    codes = xq.read().reshape(-1).astype(np.int64)
+    scales = xs.read().reshape(-1)
+    q = y.reshape(-1, 32).astype(np.float64) / scales[:, None].astype(np.float64)
+    near = np.abs(np.abs(q) - np.floor(np.abs(q)) - 0.5) < 1e-3
+    assert near[:, 1:].mean() > 0.9, "the planted quotients did not land next to half-integers"
+    c_ref, s_ref = oracle.quant_q8(y)
+    assert np.array_equal(scales.view(np.uint32), s_ref.view(np.uint32)), "scales differ"
+    assert np.array_equal(codes, c_ref.astype(np.int64)), "codes differ from the fp32 quantiser's"
+    assert all(b.intact() for b in (ob, zb, gb, xq, xs, yb)), "guard band or padding overwritten"
