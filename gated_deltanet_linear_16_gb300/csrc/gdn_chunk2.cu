@@ -20,15 +20,27 @@ namespace {
 
 constexpr int kD = 128;
 
-// Shapes by measurement on GB300 (one layer at batch 32 fp32, 256-slot fp16 pool).
+// STAGED: the head goes to shared memory by cp.async with every load in flight
+// (kGroups commit groups, each consumed as it lands); otherwise NB register
+// batches, the next in flight while one is stepped.  Shapes by measurement on
+// GB300 (batch 32 fp32 over 8 layers' states, the 256-slot fp16 pool; all
+// bitwise-identical): fp16 staged at 4 CTAs/SM 192.9 us against register
+// batches (8 warps x 2 x 3 CTAs/SM) 207.5 and staged at 3 CTAs/SM 209.9; fp32
+// staged at 3 CTAs/SM 47.7 us against register batches (8 x 4 x 4) 47.9.
+constexpr int kGroups = 4;
 template <typename TS> struct Chunk2Shape {
-    static constexpr int kWarps = 8, kBatches = 4, kMinBlocks = 4;
+    static constexpr bool kStaged = true;
+    static constexpr int kWarps = 8, kBatches = 1, kMinBlocks = 3;
 };
 template <> struct Chunk2Shape<__half> {
-    static constexpr int kWarps = 8, kBatches = 2, kMinBlocks = 3;
+    static constexpr bool kStaged = true;
+    static constexpr int kWarps = 8, kBatches = 1, kMinBlocks = 4;
 };
 
-template <typename TS, int WARPS, int NB, int MINB, bool EARLY>
+template <typename TS>
+constexpr int stage_bytes() { return kD * kD * (int)sizeof(TS); }
+
+template <typename TS, int WARPS, bool STAGED, int NB, int MINB, bool EARLY>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 chunk2_d128(const DecodeParams p)
 {
@@ -38,8 +50,10 @@ chunk2_d128(const DecodeParams p)
     constexpr int RPL = 32 / LPR;              // rows per warp-wide load
     constexpr int RPW = kD / WARPS;            // rows per warp
     constexpr int NLD = RPW / RPL;             // 16-byte state loads per lane
-    constexpr int LPB = NLD / NB;              // loads per batch
-    static_assert(RPW <= 32 && NLD % NB == 0, "shape");
+    constexpr int VPR = kD * (int)sizeof(TS) / 16;   // 16-byte vectors per state row
+    constexpr int NBAT = STAGED ? kGroups : NB;      // groups / batches of loads
+    constexpr int LPB = NLD / NBAT;                  // loads per group / batch
+    static_assert(RPW <= 32 && NLD % NBAT == 0, "shape");
 
     const int unit = blockIdx.x;               // (sequence, value head)
     const int seq = unit / p.nv;
@@ -56,9 +70,23 @@ chunk2_d128(const DecodeParams p)
     TS *midp = reinterpret_cast<TS *>(p.state_mid) + seq * p.mid_pitch + slice;
     early_start<EARLY>(reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD, p.pf_bytes);
 
-    uint4 raw[NB > 1 ? 2 : 1][LPB];
+    extern __shared__ __align__(16) unsigned char smem_raw[];   // staged: [kD rows][VPR], the head as stored
+    uint4 *mine = reinterpret_cast<uint4 *>(smem_raw) + (row0 + sub) * VPR + (lane % LPR);
+    uint4 raw[STAGED ? 1 : (NB > 1 ? 2 : 1)][STAGED ? 1 : LPB];
+    if constexpr (STAGED) {                    // a lane reads back only what it copied: no barrier
 #pragma unroll
-    for (int i = 0; i < LPB; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
+        for (int gi = 0; gi < kGroups; ++gi) {
+#pragma unroll
+            for (int ii = 0; ii < LPB; ++ii) {
+                const int i = gi * LPB + ii;
+                cp_async16(mine + i * RPL * VPR, rowp + (int64_t)i * RPL * kD);
+            }
+            cp_async_commit();
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < LPB; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
+    }
 
     // token t of sequence b reads input row 2 b + t
     const bool row_lane = lane < RPW;
@@ -84,18 +112,9 @@ chunk2_d128(const DecodeParams p)
     }
 
     float o_keep[2] = {0.f, 0.f};
-#pragma unroll
-    for (int bt = 0; bt < NB; ++bt) {
-        if (bt + 1 < NB) {
-#pragma unroll
-            for (int i = 0; i < LPB; ++i)
-                raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * LPB + i) * RPL * kD);
-        }
-#pragma unroll
-        for (int ii = 0; ii < LPB; ++ii) {
-            const int i = bt * LPB + ii;
+    auto row_steps = [&](const uint4 packed_in, const int i) {   // both tokens on state row slice i
             float s[EPV];
-            V::unpack(raw[bt & 1][ii], s);
+            V::unpack(packed_in, s);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 float u = 0.f, w = 0.f;
@@ -125,6 +144,24 @@ chunk2_d128(const DecodeParams p)
                     }
                 }
             }
+    };
+#pragma unroll
+    for (int bt = 0; bt < NBAT; ++bt) {
+        if constexpr (STAGED) {
+            if (bt == 0) cp_async_wait<kGroups - 1>();
+            else if (bt == 1) cp_async_wait<kGroups - 2>();
+            else if (bt == 2) cp_async_wait<kGroups - 3>();
+            else cp_async_wait<0>();
+#pragma unroll
+            for (int ii = 0; ii < LPB; ++ii) row_steps(mine[(bt * LPB + ii) * RPL * VPR], bt * LPB + ii);
+        } else {
+            if (bt + 1 < NBAT) {
+#pragma unroll
+                for (int i = 0; i < LPB; ++i)
+                    raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * LPB + i) * RPL * kD);
+            }
+#pragma unroll
+            for (int ii = 0; ii < LPB; ++ii) row_steps(raw[bt & 1][ii], bt * LPB + ii);
         }
     }
     if (row_lane) {
@@ -218,14 +255,23 @@ cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
     const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
     using F = Chunk2Shape<TS>;
     if (fast) {   // early launch (grids of a few waves) with a quarter of the head asked of the L2
+        const int smem = F::kStaged ? stage_bytes<TS>() : 0;
         if (early_grid(grid, F::kMinBlocks)) {
+            constexpr auto kern = chunk2_d128<TS, F::kWarps, F::kStaged, F::kBatches, F::kMinBlocks, true>;
+            if (F::kStaged) {
+                const cudaError_t e = allow_dynamic_smem<kern>(smem);
+                if (e != cudaSuccess) return e;
+            }
             DecodeParams q = p;
             q.pf_bytes = (unsigned)(kD * kD * sizeof(TS) / 4);
-            return launch_early(chunk2_d128<TS, F::kWarps, F::kBatches, F::kMinBlocks, true>, grid,
-                                F::kWarps * 32, 0, s, true, q);
+            return launch_early(kern, grid, F::kWarps * 32, smem, s, true, q);
         }
-        return launch_early(chunk2_d128<TS, F::kWarps, F::kBatches, F::kMinBlocks, false>, grid, F::kWarps * 32,
-                            0, s, false, p);
+        constexpr auto kern = chunk2_d128<TS, F::kWarps, F::kStaged, F::kBatches, F::kMinBlocks, false>;
+        if (F::kStaged) {
+            const cudaError_t e = allow_dynamic_smem<kern>(smem);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_early(kern, grid, F::kWarps * 32, smem, s, false, p);
     }
     chunk2_generic<TS><<<grid, kGenWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
