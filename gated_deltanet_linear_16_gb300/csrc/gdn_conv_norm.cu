@@ -288,10 +288,14 @@ conv_norm_d128(const ConvNormParams p)
 // One CTA per (sequence, key head) and its R = NV/NK value heads (the page's
 // block shape; taken for fp16 states): q and k are computed once, every ring
 // row of the key head is written in place by its only owner (no counter), and
-// the value heads are stepped one after another from NBUF shared-memory
-// buffers, head r + NBUF loading while head r is stepped.  With an fp16 head
-// only 32 KB, the per-value-head kernel spent more on recomputing the key
-// head's q and k three times than on the state stream.
+// the value heads are stepped one after another from one 32 KB shared-memory
+// buffer: as soon as a lane has stepped a commit group of rows of head r, it
+// copies the same rows of head r + 1 into the slots it has just read (a lane
+// reads back only its own copies, so no barrier), and the next head streams in
+// while this one finishes (150.4 -> 146.3 us at 256 slots; a second 32 KB
+// buffer measured slower, with fewer CTAs per SM).  With an fp16 head only 32
+// KB, the per-value-head kernel spent more on recomputing the key head's q and
+// k three times than on the state stream.
 constexpr int kMaxRepeat = 8;
 
 __device__ __forceinline__ void cp_async_wait_n(int n) {
@@ -307,7 +311,7 @@ __device__ __forceinline__ void cp_async_wait_n(int n) {
     }
 }
 
-template <typename TS, int NBUF, int MINB>
+template <typename TS, int MINB>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
 conv_norm_kh(const ConvNormParams p)
 {
@@ -318,10 +322,9 @@ conv_norm_kh(const ConvNormParams p)
     constexpr int NLD = kRowsPerWarp / RPL;
     constexpr int VPR = kD * (int)sizeof(TS) / 16;
     constexpr int PER = NLD / kGroups;
-    constexpr int HEAD_BYTES = kD * kD * (int)sizeof(TS);
-    static_assert(NLD % kGroups == 0 && NBUF * kGroups - 1 <= 7, "shape");
+    static_assert(NLD % kGroups == 0, "shape");
 
-    extern __shared__ __align__(16) unsigned char smem_raw[];   // NBUF heads, [kD rows][VPR] each
+    extern __shared__ __align__(16) unsigned char smem_raw[];   // one head, [kD rows][VPR]
     __shared__ __align__(16) float q_s[kD];
     __shared__ __align__(16) float k_s[kD];
     __shared__ float v_s[kMaxRepeat][kD];
@@ -342,25 +345,20 @@ conv_norm_kh(const ConvNormParams p)
     auto rowp_of = [&](int r) {
         return state_seq + (int64_t)(kh + r * p.nk) * kD * kD + (int64_t)(row0 + sub) * kD + col;
     };
-    auto mine_of = [&](int buf) {
-        return reinterpret_cast<uint4 *>(smem_raw + buf * HEAD_BYTES) + (row0 + sub) * VPR + (lane % LPR);
-    };
-    auto issue = [&](int r) {                           // head r into buffer r % NBUF, kGroups groups
+    uint4 *const mine = reinterpret_cast<uint4 *>(smem_raw) + (row0 + sub) * VPR + (lane % LPR);
+    auto issue_group = [&](int r, int gi) {             // commit group gi of head r's rows
         TS *rp = rowp_of(r);
-        uint4 *m = mine_of(r % NBUF);
 #pragma unroll
-        for (int gi = 0; gi < kGroups; ++gi) {
-#pragma unroll
-            for (int ii = 0; ii < PER; ++ii) {
-                const int i = gi * PER + ii;
-                cp_async16(m + i * RPL * VPR, rp + (int64_t)i * RPL * kD);
-            }
-            cp_async_commit();
+        for (int ii = 0; ii < PER; ++ii) {
+            const int i = gi * PER + ii;
+            cp_async16(mine + i * RPL * VPR, rp + (int64_t)i * RPL * kD);
         }
+        cp_async_commit();
     };
 
-    // 1. the first heads' state in flight before the producers run
-    for (int r = 0; r < NBUF && r < R; ++r) issue(r);
+    // 1. the first head's state in flight before the producers run
+#pragma unroll
+    for (int gi = 0; gi < kGroups; ++gi) issue_group(0, gi);
 
     // 2. producers: q (threads 0..127) and k (128..255) of the key head, then the v channels of its
     //    value heads; this CTA owns every one of these ring rows, so each is shifted in place
@@ -404,15 +402,14 @@ conv_norm_kh(const ConvNormParams p)
     for (int r = 0; r < R; ++r) {
         const int h = kh + r * p.nk;
         TS *rowp = rowp_of(r);
-        const uint4 *mine = mine_of(r % NBUF);
-        const int later = min(NBUF - 1, R - 1 - r);     // heads issued after this one
         const float v_l = row_lane ? v_s[r][row0 + lane] : 0.f;
         const float z_l = row_lane ? __ldg(p.z + seq * p.z_stride + (int64_t)h * kD + row0 + lane) : 0.f;
         const float alpha = gate_s[r][0], beta = gate_s[r][1];
         float o_keep = 0.f;
 #pragma unroll
         for (int gi = 0; gi < kGroups; ++gi) {
-            cp_async_wait_n(kGroups - 1 - gi + kGroups * later);
+            if (r + 1 < R) cp_async_wait<kGroups - 1>();   // this group; the next head's earlier ones may pend
+            else cp_async_wait_n(kGroups - 1 - gi);
 #pragma unroll
             for (int ii = 0; ii < PER; ++ii) {
                 const int i = gi * PER + ii;
@@ -439,6 +436,7 @@ conv_norm_kh(const ConvNormParams p)
                     }
                 }
             }
+            if (r + 1 < R) issue_group(r + 1, gi);      // refill the slots just stepped with head r + 1
         }
         const float ss = group_sum<32>(o_keep * o_keep);
         if (lane == 0) red[r & 1][warp] = ss;
@@ -451,7 +449,6 @@ conv_norm_kh(const ConvNormParams p)
             const float y = gn_l * o_keep * rstd * silu(z_l);
             p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
         }
-        if (r + NBUF < R) issue(r + NBUF);
     }
 }
 
@@ -578,7 +575,7 @@ cudaError_t launch_typed(const ConvNormParams &p, bool fast, cudaStream_t s)
 {
     if constexpr (sizeof(TS) == 2) {
         if (fast && p.repeat <= kMaxRepeat) {            // one CTA per key head, one staging buffer
-            constexpr auto kern = conv_norm_kh<TS, 1, 5>;
+            constexpr auto kern = conv_norm_kh<TS, 5>;
             const cudaError_t e = allow_dynamic_smem<kern>(stage_bytes<TS>());
             if (e != cudaSuccess) return e;
             // a plain launch: launched early (with or without an L2 prefetch of its heads) it
