@@ -230,7 +230,7 @@ decode_d128(const DecodeParams p)
 constexpr int kGenWarps = 4;
 constexpr int kMaxD = 256;
 
-template <typename TS, int EPI>
+template <typename TS, int EPI, bool EARLY>
 __global__ void __launch_bounds__(kGenWarps * 32)
 decode_generic(const DecodeParams p)
 {
@@ -238,6 +238,7 @@ decode_generic(const DecodeParams p)
     constexpr int MAXV = kMaxD / 32;
     __shared__ float o_s[kMaxD];
     __shared__ float red[kGenWarps];
+    early_start<EARLY>(nullptr, 0);            // no prefetch: rows need not be aligned here
 
     const int D = p.d;
     const int unit = blockIdx.x;
@@ -351,7 +352,9 @@ cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
 {
     const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
     if (!fast) {
-        decode_generic<TS, EPI><<<grid, kGenWarps * 32, 0, s>>>(p);
+        if (grid <= (unsigned)sm_count())      // one wave: launched early (the tiny-config chain)
+            return launch_early(decode_generic<TS, EPI, true>, grid, kGenWarps * 32, 0, s, true, p);
+        decode_generic<TS, EPI, false><<<grid, kGenWarps * 32, 0, s>>>(p);
         return cudaGetLastError();
     }
     // Early launch (grids of a few waves, see early_grid) with the first quarter of the head

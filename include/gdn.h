@@ -45,8 +45,9 @@
  *   summation order.
  * - Ordering: results are those of plain stream order.  When their grid is
  *   a few waves at most (e.g. one layer at batch 32), the D == 128 kernels of
- *   gdn_decode*, gdn_decode_chunk2 and (fp32 states) gdn_decode_conv_norm*
- *   are launched with CUDA's programmatic stream serialisation: such a kernel
+ *   gdn_decode*, gdn_decode_chunk2 and (fp32 states) gdn_decode_conv_norm*,
+ *   and the general gdn_decode* kernel on grids of one wave, are launched
+ *   with CUDA's programmatic stream serialisation: such a kernel
  *   may become resident while the kernel before it in the stream is still
  *   running, but reads and writes no memory until that kernel has completed
  *   (meanwhile it only asks the L2 for part of its state, a hint), and it lets

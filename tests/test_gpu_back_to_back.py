@@ -1,7 +1,7 @@
 """GPU: calls enqueued back to back on one state, with no host synchronisation between them.
 
-The D = 128 decode, two-token and decode-from-projections kernels are launched with programmatic
-stream serialisation: a kernel may become resident while the one before it in the stream is still
+The D = 128 decode, two-token and decode-from-projections kernels on grids of a few waves, and the
+general decode kernel on one-wave grids, are launched with programmatic stream serialisation: a kernel may become resident while the one before it in the stream is still
 draining, asks the L2 for its state block, and waits for its predecessor's completion before it
 reads or writes anything.  Every call here reads the state (and conv ring) that the call before it
 wrote, and the first call reads a state that a torch copy has just written, so a wait in the wrong
@@ -60,11 +60,12 @@ def _assert_bitwise(res):
 
 
 @pytest.mark.parametrize("f16", [False, True])
-@pytest.mark.parametrize("B", [2, 8, 32])
-def test_decode_chain(B, f16):
-    """Six steps alternating the bf16-normed and raw decode; B = 2, 8, 32 takes the all-in-registers,
-    register-batched (fp32) or staged, and staged kernels."""
-    T, seed = 6, 900 + B
+@pytest.mark.parametrize("B,NK,NV,D", [(2, NK, NV, D), (8, NK, NV, D), (32, NK, NV, D), (1, 1, 2, 4), (3, 2, 3, 40)])
+def test_decode_chain(B, NK, NV, D, f16):
+    """Six steps alternating the bf16-normed and raw decode; at D = 128, B = 2, 8, 32 takes the
+    all-in-registers, register-batched (fp32) or staged, and staged kernels; D = 4 (the tiny
+    configuration) and D = 40 take the general kernel, also launched early for one-wave grids."""
+    T, seed = 6, 900 + B + D
     S0 = gs.state_heads(seed, range(B), range(NV), D, dtype=np.float16 if f16 else np.float32)
     xs = [gs.decode_inputs(seed, B, NK, NV, D, step=t) for t in range(T)]
     gn = _t(gs.norm_weight(seed, D))
