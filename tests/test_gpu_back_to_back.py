@@ -60,11 +60,13 @@ def _assert_bitwise(res):
 
 
 @pytest.mark.parametrize("f16", [False, True])
-@pytest.mark.parametrize("B,NK,NV,D", [(2, NK, NV, D), (8, NK, NV, D), (32, NK, NV, D), (1, 1, 2, 4), (3, 2, 3, 40)])
+@pytest.mark.parametrize("B,NK,NV,D", [(1, NK, NV, D), (2, NK, NV, D), (8, NK, NV, D), (32, NK, NV, D), (1, 1, 2, 4),
+                                        (3, 2, 3, 40)])
 def test_decode_chain(B, NK, NV, D, f16):
-    """Six steps alternating the bf16-normed and raw decode; at D = 128, B = 2, 8, 32 takes the
-    all-in-registers, register-batched (fp32) or staged, and staged kernels; D = 4 (the tiny
-    configuration) and D = 40 take the general kernel, also launched early for one-wave grids."""
+    """Six steps alternating the bf16-normed and raw decode; at D = 128, B = 1 and 2 take the
+    all-in-registers loads and B = 8, 32 the register-batched (fp32) or staged, and staged kernels;
+    D = 4 (the tiny configuration) and D = 40 take the general kernel, also launched early for
+    one-wave grids."""
     T, seed = 6, 900 + B + D
     S0 = gs.state_heads(seed, range(B), range(NV), D, dtype=np.float16 if f16 else np.float32)
     xs = [gs.decode_inputs(seed, B, NK, NV, D, step=t) for t in range(T)]

@@ -56,10 +56,10 @@ def test_general_kernel_any_d(D, f16):
 
 @pytest.mark.parametrize("f16", [False, True])
 @pytest.mark.parametrize("norm", [True, False])
-@pytest.mark.parametrize("B", [2, 8, 32])
+@pytest.mark.parametrize("B", [1, 2, 8, 32])
 def test_every_load_variant(B, norm, f16):
-    """NV = 48: grids of 96, 384 and 1536 CTAs take the all-in-registers, register-batched (fp32;
-    fp16 is staged there) and staged loads of the D = 128 kernel."""
+    """NV = 48: grids of 48, 96, 384 and 1536 CTAs take the all-in-registers (48, 96),
+    register-batched (fp32; fp16 is staged there) and staged loads of the D = 128 kernel."""
     r = run_decode_case(B, 16, 48, 128, 1, f16=f16, norm=norm, seed=200 + B)
     check_decode(r, f16=f16, norm=norm)
 

@@ -95,9 +95,10 @@ def run_q8(B, NK, NV, D, f16, seed, T=2, misalign=0, with_y=True, zero_head=True
 
 
 @pytest.mark.parametrize("f16", [False, True])
-@pytest.mark.parametrize("B,NK,NV", [(3, 2, 6), (8, 16, 48), (32, 16, 48)])
+@pytest.mark.parametrize("B,NK,NV", [(3, 2, 6), (2, 16, 48), (8, 16, 48), (32, 16, 48)])
 def test_d128_variants(f16, B, NK, NV):
-    """Grids of 18, 384 and 1536 CTAs: the all-in-registers, register-batched and staged loads."""
+    """Grids of 18, 96, 384 and 1536 CTAs: the all-in-registers (18, 96), register-batched and
+    staged loads."""
     run_q8(B, NK, NV, 128, f16, seed=100 + B, T=2 if B < 32 else 1)
 
 
