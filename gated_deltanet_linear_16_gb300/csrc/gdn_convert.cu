@@ -10,7 +10,7 @@
 // fp16 vector -- so every warp-wide load and store covers one contiguous span
 // (512 B of fp32, 256 B of fp16) and no store leaves part of a sector for a
 // later instruction; 8 steps are in flight per thread.  The grid is a whole
-// number of waves (4 CTAs of 256 threads per SM), and the few elements past
+// number of waves (8 CTAs of 256 threads per SM), and the few elements past
 // the last full vector are done by the first threads.  Unaligned pointers take
 // a scalar grid-stride kernel with the same results.
 #include "gdn_internal.cuh"
@@ -19,7 +19,7 @@ namespace gdn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 4;
+constexpr int kCtasPerSm = 8;   // 8: f32 -> f16 183-187 us over the 202 M-element pool, 4: 189; f16 -> f32 alike
 constexpr int kUnroll = 8;
 
 __device__ __forceinline__ unsigned pack_h2(float a, float b) {
