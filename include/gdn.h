@@ -47,9 +47,9 @@
  *   a few waves at most (e.g. one layer at batch 32), the D == 128 kernels of
  *   gdn_decode*, gdn_decode_chunk2 and (fp32 states) gdn_decode_conv_norm*,
  *   and the general gdn_decode* kernel on grids of one wave, are launched
- *   with CUDA's programmatic stream serialisation: such a kernel
- *   may become resident while the kernel before it in the stream is still
- *   running, but reads and writes no memory until that kernel has completed
+ *   with CUDA's programmatic stream serialisation: such a kernel may become
+ *   resident while the kernel before it in the stream is still running, but
+ *   reads and writes no memory until that kernel has completed
  *   (meanwhile it only asks the L2 for part of its state, a hint), and it lets
  *   the kernel after it start the same way.  A caller's kernel that follows
  *   in the stream sees the outputs as usual; if it is itself launched with
