@@ -38,7 +38,8 @@ def test_single_layer_256_steps():
 
 
 def test_batched_48_layers_one_token():
-    """Batch 32, 48 layers, fp32 state [32][48][48][128][128] (4.83 GB), one fused launch per layer."""
+    """Batch 32, 48 layers, fp32 state [32][48][48][128][128] (4.83 GB), one fused launch per layer;
+    the same launches replayed from a CUDA graph (as the bench submits them) give the same bits."""
     B, L = 32, 48
     dev = torch.device("cuda")
     state = torch.empty((B, L, NV, D, D), dtype=torch.float32, device=dev)
@@ -56,13 +57,28 @@ def test_batched_48_layers_one_token():
     dx = {n: torch.from_numpy(np.stack([x[n] for x in xs])).to(dev) for n in xs[0]}
     dgn = torch.from_numpy(np.stack(gns)).to(dev)
     out = torch.empty((L, B, NV * D), dtype=torch.int16, device=dev)
-    for l in range(L):
-        gdn.gdn_decode_norm(state.data_ptr() + l * NV * D * D * 4, dx["q"][l], dx["k"][l], dx["v"][l],
-                            dx["alpha"][l], dx["beta"][l], dx["z"][l], dgn[l], out[l],
-                            batch=B, nk=NK, nv=NV, d=D, eps=EPS, state_pitch=L * NV * D * D,
-                            state_dtype=gdn.GDN_STATE_F32)
+    state0 = state.clone()
+
+    def step(st, ob):
+        for l in range(L):
+            gdn.gdn_decode_norm(st.data_ptr() + l * NV * D * D * 4, dx["q"][l], dx["k"][l], dx["v"][l],
+                                dx["alpha"][l], dx["beta"][l], dx["z"][l], dgn[l], ob[l],
+                                batch=B, nk=NK, nv=NV, d=D, eps=EPS, state_pitch=L * NV * D * D,
+                                state_dtype=gdn.GDN_STATE_F32)
+
+    step(state, out)                           # eager launches, back to back
     torch.cuda.synchronize()
     assert torch.isfinite(state).all().item()
+    # the bench's submission: the 48 launches captured once in a CUDA graph and replayed
+    state_g, out_g = state0, torch.empty_like(out)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(state_g, out_g)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(state_g.view(torch.int32), state.view(torch.int32)), "graph replay state differs"
+    assert torch.equal(out_g, out), "graph replay output differs"
+    del state_g, state0
     worst_s, worst_o = 0.0, 0.0
     for (b, l, h) in sample:
         x, g = xs[l], h % NK
