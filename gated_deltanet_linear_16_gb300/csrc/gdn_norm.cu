@@ -67,21 +67,21 @@ gate_norm_rows(const NormParams p)
     }
 }
 
-// D == 128 with 16-byte aligned rows: a lane holds 4 consecutive values of a
-// head (one 16-byte load each of o and z), warps loop over (row, head) units
-// with several units in flight, and the grid is a few CTAs per SM.  An int8 group
-// of 32 values is then 8 lanes.
+// D == 128 with 16-byte aligned rows, bf16 output: a lane holds 4 consecutive
+// values of a head (one 16-byte load each of o and z), warps loop over (row,
+// head) units with several units in flight, and the grid is a few CTAs per SM.
+// (The int8 output takes gate_norm_q8_hw below.)
 constexpr int kD = 128;
 constexpr int kCtasPerSm = 8;
-// (row, head) units a warp has in flight: 4 for the bf16 output (measured 312 us
-// against 324 with 2 and 371 with 1 over 32768 rows x 48 heads); 2 for int8,
-// where the quantisation's divisions, not the loads, set the pace (4: no gain).
-template <int EPI> constexpr int kInFlight = EPI == kEpiBf16 ? 4 : 2;
+// (row, head) units a warp has in flight: 4 (measured 312 us against 324 with 2
+// and 371 with 1 over 32768 rows x 48 heads).
+template <int EPI> constexpr int kInFlight = 4;   // (bf16 only)
 
 template <int EPI>
 __device__ __forceinline__ void norm_unit_d128(const NormParams &p, int64_t row, int h, float4 ov, float4 zv,
                                                int lane)
 {
+    static_assert(EPI == kEpiBf16, "the vector kernel's int8 output is gate_norm_q8_hw");
     float ss = ov.x * ov.x;
     ss = fmaf(ov.y, ov.y, ss);
     ss = fmaf(ov.z, ov.z, ss);
@@ -92,23 +92,9 @@ __device__ __forceinline__ void norm_unit_d128(const NormParams &p, int64_t row,
     float y[4] = {g.x * ov.x * rstd * silu_fast(zv.x), g.y * ov.y * rstd * silu_fast(zv.y),
                   g.z * ov.z * rstd * silu_fast(zv.z), g.w * ov.w * rstd * silu_fast(zv.w)};
     const int64_t e0 = (int64_t)h * kD + 4 * lane;
-    if constexpr (EPI == kEpiBf16) {
-        const uint2 b = make_uint2((unsigned)bf16_bits_rn(y[0]) | ((unsigned)bf16_bits_rn(y[1]) << 16),
-                                   (unsigned)bf16_bits_rn(y[2]) | ((unsigned)bf16_bits_rn(y[3]) << 16));
-        __stcs(reinterpret_cast<uint2 *>(p.out + row * p.out_stride + e0), b);
-    } else {
-        if (p.y != nullptr)
-            __stcs(reinterpret_cast<float4 *>(p.y + row * p.y_stride + e0), make_float4(y[0], y[1], y[2], y[3]));
-        float am = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, off));
-        const float sc = am > 0.f ? am / 127.0f : 1.0f;    // the group's 8 lanes agree
-        unsigned packed = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) packed |= ((unsigned)(__float2int_rn(y[i] / sc) & 0xff)) << (8 * i);
-        *reinterpret_cast<unsigned *>(p.xq + row * p.xq_stride + e0) = packed;
-        if ((lane & 7) == 0) p.xs[row * p.xs_stride + (int64_t)h * (kD / 32) + (lane >> 3)] = sc;
-    }
+    const uint2 b = make_uint2((unsigned)bf16_bits_rn(y[0]) | ((unsigned)bf16_bits_rn(y[1]) << 16),
+                               (unsigned)bf16_bits_rn(y[2]) | ((unsigned)bf16_bits_rn(y[3]) << 16));
+    __stcs(reinterpret_cast<uint2 *>(p.out + row * p.out_stride + e0), b);
 }
 
 // Each warp takes chunks of NF consecutive (row, head) units, chunks nwarps
@@ -156,18 +142,92 @@ gate_norm_d128(const NormParams p)
     }
 }
 
+// int8 output: a half-warp per (row, head) unit, 8 consecutive values a lane
+// (two 16-byte loads each of o and z), so a warp works on two units at once
+// and an int8 group of 32 values is 4 lanes.  A warp takes pairs of
+// consecutive units, pairs a grid apart.  Against the bf16 kernel's layout (a
+// warp per unit, 4 values a lane) this halves the per-unit reductions, the
+// address and loop work per value: 315 against 365 us over 32768 rows x 48
+// heads, where the quantisation's divisions (IEEE, as the page's codes are
+// decided) keep the kernel bound by instruction issue rather than by HBM.
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+gate_norm_q8_hw(const NormParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int hw = lane >> 4, l = lane & 15;
+    const int64_t units = p.rows * p.nv;
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta * 2;
+    int64_t u = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * 2;
+    if (u >= units) return;                             // whole warps leave together
+    const int64_t step_rows = stride / p.nv;
+    const int step_h = (int)(stride - step_rows * p.nv);
+    int64_t row = u / p.nv;
+    int h = (int)(u - row * p.nv);
+    const float4 g0 = __ldg(reinterpret_cast<const float4 *>(p.gn) + 2 * l);
+    const float4 g1 = __ldg(reinterpret_cast<const float4 *>(p.gn) + 2 * l + 1);
+    for (; u < units; u += stride) {
+        int64_t r = row;
+        int hh = h + hw;
+        if (hh == p.nv) { hh = 0; ++r; }
+        const bool active = u + hw < units;
+        const int64_t e0 = (int64_t)hh * kD + 8 * l;
+        float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0, z0 = o0, z1 = o0;
+        if (active) {
+            o0 = __ldcs(reinterpret_cast<const float4 *>(p.o + r * p.o_stride + e0));
+            o1 = __ldcs(reinterpret_cast<const float4 *>(p.o + r * p.o_stride + e0) + 1);
+            z0 = __ldcs(reinterpret_cast<const float4 *>(p.z + r * p.z_stride + e0));
+            z1 = __ldcs(reinterpret_cast<const float4 *>(p.z + r * p.z_stride + e0) + 1);
+        }
+        const float ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+        const float zv[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+        const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        float ss = ov[0] * ov[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) ss = fmaf(ov[i], ov[i], ss);
+        ss = group_sum<16>(ss);                          // within this half-warp
+        const float rstd = rsqrtf(ss * (1.0f / kD) + p.eps);
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = gv[i] * ov[i] * rstd * silu_fast(zv[i]);
+        if (active && p.y != nullptr) {
+            __stcs(reinterpret_cast<float4 *>(p.y + r * p.y_stride + e0), make_float4(y[0], y[1], y[2], y[3]));
+            __stcs(reinterpret_cast<float4 *>(p.y + r * p.y_stride + e0) + 1, make_float4(y[4], y[5], y[6], y[7]));
+        }
+        float am = fabsf(y[0]);
+#pragma unroll
+        for (int i = 1; i < 8; ++i) am = fmaxf(am, fabsf(y[i]));
+        am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(kFull, am, 2));
+        const float sc = am > 0.f ? am / 127.0f : 1.0f;    // the group's 4 lanes agree
+        unsigned lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo |= ((unsigned)(__float2int_rn(y[i] / sc) & 0xff)) << (8 * i);
+            hi |= ((unsigned)(__float2int_rn(y[4 + i] / sc) & 0xff)) << (8 * i);
+        }
+        if (active) {
+            unsigned *q = reinterpret_cast<unsigned *>(p.xq + r * p.xq_stride + e0);
+            q[0] = lo;
+            q[1] = hi;
+            if ((l & 3) == 0) p.xs[r * p.xs_stride + (int64_t)hh * (kD / 32) + (l >> 2)] = sc;
+        }
+        row += step_rows;
+        h += step_h;
+        if (h >= p.nv) { h -= p.nv; ++row; }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gate_norm(const NormParams &p, int epi, bool fast, cudaStream_t s)
 {
     const int64_t units = p.rows * p.nv;
-    if (fast) {
+    if (fast) {                                         // a warp takes 2 (int8) or 4 (bf16) units at a time
         const int64_t full = (int64_t)sm_count() * kCtasPerSm;
-        const int nf = epi == kEpiQ8 ? kInFlight<kEpiQ8> : kInFlight<kEpiBf16>;
-        const int64_t chunks = (units + nf - 1) / nf;
-        const int64_t need = (chunks + kWarpsPerCta - 1) / kWarpsPerCta;
+        const int per_warp = epi == kEpiQ8 ? 2 : kInFlight<kEpiBf16>;
+        const int64_t need = ((units + per_warp - 1) / per_warp + kWarpsPerCta - 1) / kWarpsPerCta;
         const unsigned grid = (unsigned)(need < full ? need : full);
-        if (epi == kEpiQ8) gate_norm_d128<kEpiQ8><<<grid, kWarpsPerCta * 32, 0, s>>>(p);
+        if (epi == kEpiQ8) gate_norm_q8_hw<<<grid, kWarpsPerCta * 32, 0, s>>>(p);
         else gate_norm_d128<kEpiBf16><<<grid, kWarpsPerCta * 32, 0, s>>>(p);
         return cudaGetLastError();
     }
