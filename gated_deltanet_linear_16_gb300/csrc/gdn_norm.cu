@@ -142,74 +142,78 @@ gate_norm_d128(const NormParams p)
     }
 }
 
-// int8 output: a half-warp per (row, head) unit, 8 consecutive values a lane
-// (two 16-byte loads each of o and z), so a warp works on two units at once
-// and an int8 group of 32 values is 4 lanes.  A warp takes pairs of
-// consecutive units, pairs a grid apart.  Against the bf16 kernel's layout (a
-// warp per unit, 4 values a lane) this halves the per-unit reductions, the
-// address and loop work per value: 315 against 365 us over 32768 rows x 48
-// heads, where the quantisation's divisions (IEEE, as the page's codes are
-// decided) keep the kernel bound by instruction issue rather than by HBM.
+// int8 output: a quarter-warp (8 lanes) per (row, head) unit, 16 consecutive
+// values a lane (four 16-byte loads each of o and z), so a warp works on four
+// units at once and an int8 group of 32 values is 2 lanes.  A warp takes runs
+// of 4 consecutive units, runs a grid apart.  Against the bf16 kernel's layout
+// (a warp per unit, 4 values a lane) this cuts the per-unit reductions, the
+// address and loop work per value: 304 us over 32768 rows x 48 heads, against
+// 315 with a half-warp per unit and 365 with a warp, the quantisation's
+// divisions (IEEE, as the page decides codes) keeping the kernel bound by
+// instruction issue more than by HBM.
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 gate_norm_q8_hw(const NormParams p)
 {
     const int lane = threadIdx.x & 31;
-    const int hw = lane >> 4, l = lane & 15;
+    const int qw = lane >> 3, l = lane & 7;
     const int64_t units = p.rows * p.nv;
-    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta * 2;
-    int64_t u = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * 2;
-    if (u >= units) return;                             // whole warps leave together
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta * 4;
+    int64_t u = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * 4;
+    if (u >= units) return;
     const int64_t step_rows = stride / p.nv;
     const int step_h = (int)(stride - step_rows * p.nv);
     int64_t row = u / p.nv;
     int h = (int)(u - row * p.nv);
-    const float4 g0 = __ldg(reinterpret_cast<const float4 *>(p.gn) + 2 * l);
-    const float4 g1 = __ldg(reinterpret_cast<const float4 *>(p.gn) + 2 * l + 1);
+    float gv[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 g = __ldg(reinterpret_cast<const float4 *>(p.gn) + 4 * l + k);
+        gv[4 * k] = g.x; gv[4 * k + 1] = g.y; gv[4 * k + 2] = g.z; gv[4 * k + 3] = g.w;
+    }
     for (; u < units; u += stride) {
         int64_t r = row;
-        int hh = h + hw;
-        if (hh == p.nv) { hh = 0; ++r; }
-        const bool active = u + hw < units;
-        const int64_t e0 = (int64_t)hh * kD + 8 * l;
-        float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0, z0 = o0, z1 = o0;
-        if (active) {
-            o0 = __ldcs(reinterpret_cast<const float4 *>(p.o + r * p.o_stride + e0));
-            o1 = __ldcs(reinterpret_cast<const float4 *>(p.o + r * p.o_stride + e0) + 1);
-            z0 = __ldcs(reinterpret_cast<const float4 *>(p.z + r * p.z_stride + e0));
-            z1 = __ldcs(reinterpret_cast<const float4 *>(p.z + r * p.z_stride + e0) + 1);
+        int hh = h + qw;
+        while (hh >= p.nv) { hh -= p.nv; ++r; }     // at most 3 steps (NV may be below 4)
+        const bool active = u + qw < units;
+        const int64_t e0 = (int64_t)hh * kD + 16 * l;
+        float ov[16], zv[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (active) {
+                a = __ldcs(reinterpret_cast<const float4 *>(p.o + r * p.o_stride + e0) + k);
+                b = __ldcs(reinterpret_cast<const float4 *>(p.z + r * p.z_stride + e0) + k);
+            }
+            ov[4 * k] = a.x; ov[4 * k + 1] = a.y; ov[4 * k + 2] = a.z; ov[4 * k + 3] = a.w;
+            zv[4 * k] = b.x; zv[4 * k + 1] = b.y; zv[4 * k + 2] = b.z; zv[4 * k + 3] = b.w;
         }
-        const float ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-        const float zv[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
-        const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         float ss = ov[0] * ov[0];
 #pragma unroll
-        for (int i = 1; i < 8; ++i) ss = fmaf(ov[i], ov[i], ss);
-        ss = group_sum<16>(ss);                          // within this half-warp
+        for (int i = 1; i < 16; ++i) ss = fmaf(ov[i], ov[i], ss);
+        ss = group_sum<8>(ss);
         const float rstd = rsqrtf(ss * (1.0f / kD) + p.eps);
-        float y[8];
+        float y[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = gv[i] * ov[i] * rstd * silu_fast(zv[i]);
+        for (int i = 0; i < 16; ++i) y[i] = gv[i] * ov[i] * rstd * silu_fast(zv[i]);
         if (active && p.y != nullptr) {
-            __stcs(reinterpret_cast<float4 *>(p.y + r * p.y_stride + e0), make_float4(y[0], y[1], y[2], y[3]));
-            __stcs(reinterpret_cast<float4 *>(p.y + r * p.y_stride + e0) + 1, make_float4(y[4], y[5], y[6], y[7]));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                __stcs(reinterpret_cast<float4 *>(p.y + r * p.y_stride + e0) + k,
+                       make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]));
         }
         float am = fabsf(y[0]);
 #pragma unroll
-        for (int i = 1; i < 8; ++i) am = fmaxf(am, fabsf(y[i]));
-        am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));
-        am = fmaxf(am, __shfl_xor_sync(kFull, am, 2));
-        const float sc = am > 0.f ? am / 127.0f : 1.0f;    // the group's 4 lanes agree
-        unsigned lo = 0, hi = 0;
+        for (int i = 1; i < 16; ++i) am = fmaxf(am, fabsf(y[i]));
+        am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));    // a group of 32 is 2 lanes
+        const float sc = am > 0.f ? am / 127.0f : 1.0f;
+        unsigned w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            lo |= ((unsigned)(__float2int_rn(y[i] / sc) & 0xff)) << (8 * i);
-            hi |= ((unsigned)(__float2int_rn(y[4 + i] / sc) & 0xff)) << (8 * i);
-        }
+        for (int i = 0; i < 16; ++i) w[i >> 2] |= ((unsigned)(__float2int_rn(y[i] / sc) & 0xff)) << (8 * (i & 3));
         if (active) {
             unsigned *q = reinterpret_cast<unsigned *>(p.xq + r * p.xq_stride + e0);
-            q[0] = lo;
-            q[1] = hi;
-            if ((l & 3) == 0) p.xs[r * p.xs_stride + (int64_t)hh * (kD / 32) + (l >> 2)] = sc;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) q[k] = w[k];
+            if ((l & 1) == 0) p.xs[r * p.xs_stride + (int64_t)hh * (kD / 32) + (l >> 1)] = sc;
         }
         row += step_rows;
         h += step_h;
@@ -222,9 +226,9 @@ gate_norm_q8_hw(const NormParams p)
 cudaError_t launch_gate_norm(const NormParams &p, int epi, bool fast, cudaStream_t s)
 {
     const int64_t units = p.rows * p.nv;
-    if (fast) {                                         // a warp takes 2 (int8) or 4 (bf16) units at a time
+    if (fast) {                                         // a warp takes 4 units at a time
         const int64_t full = (int64_t)sm_count() * kCtasPerSm;
-        const int per_warp = epi == kEpiQ8 ? 2 : kInFlight<kEpiBf16>;
+        const int per_warp = epi == kEpiQ8 ? 4 : kInFlight<kEpiBf16>;
         const int64_t need = ((units + per_warp - 1) / per_warp + kWarpsPerCta - 1) / kWarpsPerCta;
         const unsigned grid = (unsigned)(need < full ? need : full);
         if (epi == kEpiQ8) gate_norm_q8_hw<<<grid, kWarpsPerCta * 32, 0, s>>>(p);
