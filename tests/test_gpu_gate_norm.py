@@ -38,7 +38,7 @@ def _ref(o, z, gn, nv, d):
                                 EPS).reshape(rows, nv * d)
 
 
-@pytest.mark.parametrize("rows,nv,d,pad", [(5, 3, 128, 3), (5, 3, 128, 4), (1000, 48, 128, 0), (33, 2, 64, 4),
+@pytest.mark.parametrize("rows,nv,d,pad", [(5, 3, 128, 3), (5, 3, 128, 4), (1000, 48, 128, 0), (9, 1, 128, 0), (33, 2, 64, 4),
                                             (4, 3, 5, 0), (3, 2, 256, 8), (1, 48, 128, 4)])
 def test_bf16(rows, nv, d, pad):
     """pad = 0 or a multiple of 4 keeps D = 128 rows 16-byte aligned (the vector kernel); 3 does not."""
@@ -57,10 +57,12 @@ def test_bf16(rows, nv, d, pad):
 
 
 @pytest.mark.parametrize("rows,nv,d,with_y,pad", [(6, 3, 128, True, 4), (6, 3, 128, True, 1), (777, 48, 128, True, 0),
+                                                  (5, 1, 128, True, 4), (7, 2, 128, False, 0),
                                                   (9, 2, 64, True, 4), (2, 4, 32, True, 4), (3, 2, 256, True, 4),
                                                   (6, 3, 128, False, 4)])
 def test_q8(rows, nv, d, with_y, pad):
-    """pad 4 / 0: the D = 128 vector kernel (int8 groups over 8 lanes); pad 1: the general kernel."""
+    """pad 4 / 0: the D = 128 vector kernel (a quarter-warp per (row, head), so NV = 1 or 2 puts
+    several rows' heads in one warp; an int8 group over 2 lanes); pad 1: the general kernel."""
     o, z, gn = _inputs(rows, nv, d, seed=400 + d + pad)
     hv = nv * d
     ob, zb, gb = Rows(rows, hv, hv + pad), Rows(rows, hv, hv + pad), Rows(1, d)
