@@ -11,7 +11,8 @@
 // An HBM stream (o and z read once, the output written once).  General D: one
 // warp per (row, head), lanes strided over the head's D values (coalesced
 // 128-byte warp accesses), every load of a lane in flight before the
-// reduction; 8 warps per CTA.  D == 128 takes the vector kernel below.
+// reduction; 8 warps per CTA.  D == 128 with aligned rows takes the vector
+// kernels below: gate_norm_d128 (bf16) and gate_norm_q8_hw (int8).
 #include "gdn_internal.cuh"
 
 namespace gdn {
