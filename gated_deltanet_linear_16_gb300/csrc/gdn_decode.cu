@@ -67,8 +67,8 @@ template <typename TS> struct RegShape { static constexpr int kBatches = 4, kMin
 template <typename TS>
 constexpr int stage_bytes() { return kD * kD * (int)sizeof(TS); }
 
-template <typename TS, int EPI, bool STAGED, int NB, int MINB, bool EARLY>
-__global__ void __launch_bounds__(kWarps * 32, MINB)
+template <typename TS, int EPI, bool STAGED, int NB, int MINB, bool EARLY, int W = kWarps>
+__global__ void __launch_bounds__(W * 32, MINB)
 decode_d128(const DecodeParams p)
 {
     constexpr bool NORM = EPI != kEpiRaw;
@@ -76,7 +76,7 @@ decode_d128(const DecodeParams p)
     constexpr int EPV = V::N;                  // state elements per 16-byte vector
     constexpr int LPR = kD / EPV;              // lanes per state row: 32 fp32, 16 fp16
     constexpr int RPL = 32 / LPR;              // rows per warp-wide access: 1 fp32, 2 fp16
-    constexpr int RPW = kD / kWarps;           // rows per warp
+    constexpr int RPW = kD / W;                // rows per warp
     constexpr int NLD = RPW / RPL;             // 16-byte state vectors per lane
     constexpr int VPR = kD * (int)sizeof(TS) / 16;   // vectors per state row
     constexpr int NBAT = STAGED ? kGroups : NB;      // groups / batches of loads
@@ -191,13 +191,13 @@ decode_d128(const DecodeParams p)
         if (row_lane) p.o[seq * p.o_stride + (int64_t)h * kD + row0 + lane] = o_keep;
     } else {
         // 4. gated RMS norm over the head's 128 outputs, in this CTA
-        __shared__ float red[kWarps];
+        __shared__ float red[W];
         const float ss = group_sum<32>(o_keep * o_keep);   // lanes >= RPW hold 0
         if (lane == 0) red[warp] = ss;
         __syncthreads();
         float tot = 0.f;
 #pragma unroll
-        for (int i = 0; i < kWarps; ++i) tot += red[i];
+        for (int i = 0; i < W; ++i) tot += red[i];
         const float rstd = rsqrtf(tot * (1.0f / kD) + p.eps);
         if constexpr (EPI == kEpiBf16) {
             if (row_lane) {
@@ -365,8 +365,9 @@ cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
     static_assert(kStagedMinCtasPerSm <= kEarlyMaxWaves * RegShape<float>::kMinBlocks,
                   "register-batched grids must stay within the early-launch waves");
     switch (pick_path<TS>(grid)) {
-    case Path::kRegAll:                          // one wave at most
-        return launch_early(decode_d128<TS, EPI, false, 1, 1, true>, grid, kWarps * 32, 0, s, true, q);
+    case Path::kRegAll:                          // one wave at most: 16 warps x 8 rows a CTA
+        return launch_early(decode_d128<TS, EPI, false, 1, 1, true, 2 * kWarps>, grid, 2 * kWarps * 32, 0, s,
+                            true, q);
     case Path::kRegBatched:                      // under kStagedMinCtasPerSm / 3 waves
         if constexpr (sizeof(TS) == 4)
             return launch_early(decode_d128<TS, EPI, false, RegShape<TS>::kBatches, RegShape<TS>::kMinBlocks, true>,
