@@ -54,9 +54,9 @@ REF_LAYERS_PER_STEP = 4      # oracle sample per step of the reference arm
 # dram__bytes_write.sum), valid only while the kernel source is the one it was taken on.
 NCU_TRAFFIC = {
     # mean of three mid-sequence launches of the full 48-layer workload, ncu --cache-control none
-    # (reads 102.9-103.1 MB, writes 96.7-99.5 MB); see profiles/decode_d128_f32_norm_batched48.md
-    "decode_norm_f32": {"bytes_per_launch": 201472171,
-                        "src_sha256": "aa210d0d0fa9317d8d942925221403ba8fe18c217bb9e001eb2af8a8b0d09c60"},
+    # (reads 102.9-103.0 MB, writes 96.2-99.4 MB); see profiles/decode_d128_f32_norm_batched48.md
+    "decode_norm_f32": {"bytes_per_launch": 201291947,
+                        "src_sha256": "a705afedce866b7ece345c0b2288507a9add0baf3a7a6825291108a3cbc60d6c"},
 }
 
 
