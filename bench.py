@@ -54,7 +54,7 @@ REF_LAYERS_PER_STEP = 4      # oracle sample per step of the reference arm
 # dram__bytes_write.sum), valid only while the kernel source is the one it was taken on.
 NCU_TRAFFIC = {
     # mean of three mid-sequence launches of the full 48-layer workload, ncu --cache-control none
-    # (reads 102.9-103.0 MB, writes 96.2-99.4 MB); see profiles/decode_d128_f32_norm_batched48.md
+    # (reads 102.9-103.0 MB, writes 96.2-99.4 MB), from the ncu capture of the batch-32 48-layer decode
     "decode_norm_f32": {"bytes_per_launch": 201291947,
                         "src_sha256": "a705afedce866b7ece345c0b2288507a9add0baf3a7a6825291108a3cbc60d6c"},
 }

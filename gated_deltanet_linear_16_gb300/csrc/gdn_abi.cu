@@ -176,6 +176,74 @@ int decode_entry(void *state, int state_dtype, int64_t state_pitch,
 
 int report_cuda_error(cudaError_t e) { return cuda_status(e); }
 
+// gdn_decode_conv_norm's checks and launch.  With `counters_of` set (the
+// allocation-free entry) the workspace argument is ignored and the counters'
+// device address comes from counters_of, called only after every argument has
+// passed its checks, so a rejected or empty call makes no CUDA call at all.
+int decode_conv_norm_entry(void *state, int state_dtype, int64_t state_pitch,
+                           float *conv_state, int64_t conv_pitch, int taps,
+                           const float *x, const float *conv_w,
+                           const float *br, const float *ar, const float *dt, const float *rate,
+                           const float *z, const float *gn, float l2_eps, float eps,
+                           uint16_t *out, int32_t *workspace, CountersFn counters_of,
+                           int batch, int nk, int nv, int d,
+                           int64_t x_stride, int64_t gate_stride, int64_t z_stride,
+                           int64_t out_stride, void *stream)
+{
+    int st = check_common(batch, nk, nv, d, state_pitch, state_dtype);
+    if (st != GDN_OK) return st;
+    if (nv % nk != 0) return GDN_ERR_UNSUPPORTED;
+    if (taps < 1 || taps > 8) return GDN_ERR_ARG;
+    if (!(eps >= 0.0f && std::isfinite(eps)) || !(l2_eps >= 0.0f && std::isfinite(l2_eps))) return GDN_ERR_ARG;
+    const int repeat = nv / nk;
+    // the general kernel keeps q, k, every value head's v, o and the gates in shared memory
+    if ((size_t)(3 + repeat) * d * 4 + 8 * (size_t)repeat > 48 * 1024) return GDN_ERR_UNSUPPORTED;
+    const int64_t selem = state_dtype == GDN_STATE_F16 ? 2 : 4;
+    const int64_t B = batch, hv = (int64_t)nv * d, C = (int64_t)(2 * nk + nv) * d;
+    if (conv_pitch < taps * C) return GDN_ERR_ARG;
+    Operand ops[12] = {
+        {state, B, (int64_t)nv * d * d, state_pitch, selem},
+        {conv_state, B, taps * C, conv_pitch, 4},
+        {out, B, hv, out_stride, 2},
+        {workspace, 1, B * nk, B * nk, 4},
+        {x, B, C, x_stride, 4},
+        {conv_w, 1, taps * C, taps * C, 4},
+        {br, B, nv, gate_stride, 4},
+        {ar, B, nv, gate_stride, 4},
+        {dt, 1, nv, nv, 4},
+        {rate, 1, nv, nv, 4},
+        {z, B, hv, z_stride, 4},
+        {gn, 1, d, d, 4},
+    };
+    // with counters_of set, the counters are the library's own, not an operand of the call
+    const int n_ops = counters_of ? 11 : 12;
+    if (counters_of) ops[3] = ops[11];
+    if (batch == 0) {
+        for (int i = 0; i < n_ops; ++i) if (ops[i].p == nullptr) return GDN_ERR_ARG;
+        return GDN_OK;
+    }
+    st = check_operands(ops, n_ops, counters_of ? 3 : 4);
+    if (st != GDN_OK) return st;
+    if (counters_of) {                       // every check has passed: now the CUDA call
+        const cudaError_t e = counters_of(&workspace);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+
+    ConvNormParams p{};
+    p.state = state; p.pitch = state_pitch;
+    p.ring = conv_state; p.ring_pitch = conv_pitch;
+    p.x = x; p.x_stride = x_stride; p.w = conv_w;
+    p.br = br; p.ar = ar; p.gate_stride = gate_stride; p.dt = dt; p.rate = rate;
+    p.z = z; p.gn = gn; p.out = out; p.z_stride = z_stride; p.out_stride = out_stride;
+    p.counters = workspace;
+    p.batch = batch; p.nk = nk; p.nv = nv; p.d = d; p.taps = taps; p.repeat = repeat;
+    p.l2_eps = l2_eps; p.eps = eps; p.inv_sqrt_d = inv_sqrt(d);
+    // D == 128 kernel: 16-byte state rows
+    const bool fast = d == 128 && vec16(state) && (state_pitch * selem) % 16 == 0;
+    return cuda_status(launch_conv_norm(p, state_dtype == GDN_STATE_F16, fast, (cudaStream_t)stream));
+}
+
+
 namespace {
 
 // The standalone gated norm: rows of NV heads x D raw outputs o (and gate
@@ -230,7 +298,7 @@ using namespace gdn;
 
 extern "C" {
 
-GDN_API int gdn_decode(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                        const float *q, const float *k, const float *v,
                        const float *alpha, const float *beta, float *o,
                        int batch, int nk, int nv, int d,
@@ -243,7 +311,7 @@ GDN_API int gdn_decode(void *state, int state_dtype, int64_t state_pitch,
                         ep, batch, nk, nv, d, qk_stride, v_stride, gb_stride, 0, stream);
 }
 
-GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode_norm(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                             const float *q, const float *k, const float *v,
                             const float *alpha, const float *beta,
                             const float *z, const float *gn, float eps,
@@ -258,7 +326,7 @@ GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
                         ep, batch, nk, nv, d, qk_stride, v_stride, gb_stride, z_stride, stream);
 }
 
-GDN_API int gdn_decode_norm_q8(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode_norm_q8(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                                const float *q, const float *k, const float *v,
                                const float *alpha, const float *beta,
                                const float *z, const float *gn, float eps,
@@ -276,7 +344,7 @@ GDN_API int gdn_decode_norm_q8(void *state, int state_dtype, int64_t state_pitch
                         ep, batch, nk, nv, d, qk_stride, v_stride, gb_stride, z_stride, stream);
 }
 
-GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode_conv_norm(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                                  float *conv_state, int64_t conv_pitch, int taps,
                                  const float *x, const float *conv_w,
                                  const float *br, const float *ar, const float *dt, const float *rate,
@@ -286,54 +354,12 @@ GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pit
                                  int64_t x_stride, int64_t gate_stride, int64_t z_stride,
                                  int64_t out_stride, void *stream)
 {
-    int st = check_common(batch, nk, nv, d, state_pitch, state_dtype);
-    if (st != GDN_OK) return st;
-    if (nv % nk != 0) return GDN_ERR_UNSUPPORTED;
-    if (taps < 1 || taps > 8) return GDN_ERR_ARG;
-    if (!(eps >= 0.0f && std::isfinite(eps)) || !(l2_eps >= 0.0f && std::isfinite(l2_eps))) return GDN_ERR_ARG;
-    const int repeat = nv / nk;
-    // the general kernel keeps q, k, every value head's v, o and the gates in shared memory
-    if ((size_t)(3 + repeat) * d * 4 + 8 * (size_t)repeat > 48 * 1024) return GDN_ERR_UNSUPPORTED;
-    const int64_t selem = state_dtype == GDN_STATE_F16 ? 2 : 4;
-    const int64_t B = batch, hv = (int64_t)nv * d, C = (int64_t)(2 * nk + nv) * d;
-    if (conv_pitch < taps * C) return GDN_ERR_ARG;
-    Operand ops[12] = {
-        {state, B, (int64_t)nv * d * d, state_pitch, selem},
-        {conv_state, B, taps * C, conv_pitch, 4},
-        {out, B, hv, out_stride, 2},
-        {workspace, 1, B * nk, B * nk, 4},
-        {x, B, C, x_stride, 4},
-        {conv_w, 1, taps * C, taps * C, 4},
-        {br, B, nv, gate_stride, 4},
-        {ar, B, nv, gate_stride, 4},
-        {dt, 1, nv, nv, 4},
-        {rate, 1, nv, nv, 4},
-        {z, B, hv, z_stride, 4},
-        {gn, 1, d, d, 4},
-    };
-    const int n_ops = 12;
-    if (batch == 0) {
-        for (int i = 0; i < n_ops; ++i) if (ops[i].p == nullptr) return GDN_ERR_ARG;
-        return GDN_OK;
-    }
-    st = check_operands(ops, n_ops, 4);
-    if (st != GDN_OK) return st;
-
-    ConvNormParams p{};
-    p.state = state; p.pitch = state_pitch;
-    p.ring = conv_state; p.ring_pitch = conv_pitch;
-    p.x = x; p.x_stride = x_stride; p.w = conv_w;
-    p.br = br; p.ar = ar; p.gate_stride = gate_stride; p.dt = dt; p.rate = rate;
-    p.z = z; p.gn = gn; p.out = out; p.z_stride = z_stride; p.out_stride = out_stride;
-    p.counters = workspace;
-    p.batch = batch; p.nk = nk; p.nv = nv; p.d = d; p.taps = taps; p.repeat = repeat;
-    p.l2_eps = l2_eps; p.eps = eps; p.inv_sqrt_d = inv_sqrt(d);
-    // D == 128 kernel: 16-byte state rows
-    const bool fast = d == 128 && vec16(state) && (state_pitch * selem) % 16 == 0;
-    return cuda_status(launch_conv_norm(p, state_dtype == GDN_STATE_F16, fast, (cudaStream_t)stream));
+    return gdn::decode_conv_norm_entry(state, state_dtype, state_pitch, conv_state, conv_pitch, taps, x, conv_w,
+                                       br, ar, dt, rate, z, gn, l2_eps, eps, out, workspace, nullptr,
+                                       batch, nk, nv, d, x_stride, gate_stride, z_stride, out_stride, stream);
 }
 
-GDN_API int gdn_decode_chunk2(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode_chunk2(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                               void *state_mid, int64_t mid_pitch,
                               const float *q, const float *k, const float *v,
                               const float *alpha, const float *beta, float *o,
@@ -377,7 +403,7 @@ GDN_API int gdn_decode_chunk2(void *state, int state_dtype, int64_t state_pitch,
     return cuda_status(launch_decode_chunk2(p, state_dtype == GDN_STATE_F16, fast, (cudaStream_t)stream));
 }
 
-GDN_API int gdn_prefill_seq(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_prefill_seq(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                             const float *q, const float *k, const float *v,
                             const float *alpha, const float *beta, float *o,
                             int batch, int seq_len, int nk, int nv, int d,

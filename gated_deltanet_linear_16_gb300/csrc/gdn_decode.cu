@@ -13,8 +13,9 @@
 //
 // GB300 design.  The state is ~99% of the bytes and is touched exactly once
 // (one read, one write per element), so the kernel is an HBM stream:
-//  * one CTA owns one (sequence, head) -- 8 warps x 16 rows -- so the norm's
-//    reduction over the head's D outputs needs a single __syncthreads;
+//  * one CTA owns one (sequence, head) -- 8 warps x 16 rows, or 16 warps x 8
+//    rows on grids of one wave -- so the norm's reduction over the head's D
+//    outputs needs a single __syncthreads;
 //  * every state access is a 16-byte vector: an fp32 row (512 B) is one
 //    warp-wide load, an fp16 row (256 B) half of one, so a warp touches whole
 //    128-byte lines and stores never leave partial sectors;
@@ -46,9 +47,11 @@ constexpr int kD = 128;
 
 // ------------------------------------------------------------------ D == 128
 
-// Three ways to bring a lane's 16 (fp32) or 8 (fp16) state vectors in, all
-// with 8 warps x 16 rows per head and the same arithmetic (bitwise-identical
-// results):
+// Three ways to bring a lane's 16-byte state vectors in, all with the same
+// arithmetic (bitwise-identical results).  The staged and register-batched
+// paths run 8 warps x 16 rows per head (16 fp32 or 8 fp16 vectors a lane);
+// the all-in-registers path runs 16 warps x 8 rows (W = 2 * kWarps: 8 fp32 or
+// 4 fp16 vectors a lane, and lanes r < 8 carry the rows' o):
 //  * staged: every load in flight at once through cp.async into shared memory
 //    (64 KB fp32 / 32 KB fp16 per CTA), four commit groups each consumed as it
 //    lands.  The loads hold no registers while in flight, so 3 (fp32) or 4

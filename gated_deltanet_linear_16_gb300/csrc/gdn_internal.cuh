@@ -100,6 +100,22 @@ cudaError_t launch_gate_norm(const NormParams &p, int epi, bool fast, cudaStream
 cudaError_t launch_f32_to_f16(const float *src, uint16_t *dst, uint64_t n, bool vec, cudaStream_t s);
 cudaError_t launch_f16_to_f32(const uint16_t *src, float *dst, uint64_t n, bool vec, cudaStream_t s);
 
+// gdn_decode_conv_norm's argument checks and launch, shared by its two entry
+// points.  `counters_of` null: `workspace` is the caller's counter buffer (an
+// operand, checked like the others).  Otherwise `workspace` is ignored and the
+// counters' address comes from counters_of, which runs only after every check
+// has passed (a rejected or empty call makes no CUDA call).
+using CountersFn = cudaError_t (*)(int32_t **);
+int decode_conv_norm_entry(void *state, int state_dtype, int64_t state_pitch,
+                           float *conv_state, int64_t conv_pitch, int taps,
+                           const float *x, const float *conv_w,
+                           const float *br, const float *ar, const float *dt, const float *rate,
+                           const float *z, const float *gn, float l2_eps, float eps,
+                           uint16_t *out, int32_t *workspace, CountersFn counters_of,
+                           int batch, int nk, int nv, int d,
+                           int64_t x_stride, int64_t gate_stride, int64_t z_stride,
+                           int64_t out_stride, void *stream);
+
 // Number of SMs of the current device (cached per device id).
 int sm_count();
 

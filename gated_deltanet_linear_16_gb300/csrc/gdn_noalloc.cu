@@ -17,10 +17,11 @@
 // when the module is loaded on a device; every completed call leaves the ones
 // it used at zero again, so they start at zero for the next call).  Its
 // device address is looked up with cudaGetSymbolAddress once per device, the
-// first time a call runs with that device current, and cached; the call then
-// goes through gdn_decode_conv_norm with that address as the workspace, so
-// the arithmetic, checks and kernels are exactly those of the workspace
-// entry point.
+// first time a call runs with that device current, and cached.  The call
+// runs the argument checks of gdn_decode_conv_norm first (a rejected or empty
+// call makes no CUDA call), then looks the address up and launches with it as
+// the workspace, so the arithmetic and kernels are exactly those of the
+// workspace entry point.
 //
 // Limits.  batch * NK <= GDN_NOALLOC_MAX_KEY_HEADS (16384 counters, 64 KB
 // per device); larger calls return GDN_ERR_UNSUPPORTED before anything runs.
@@ -29,7 +30,8 @@
 // racing on different streams) race on the counters and their results are
 // undefined.  Calls ordered on one stream are fine.  Make the first call on
 // each device before any stream capture begins, since that call does the
-// symbol lookup.
+// symbol lookup.  Calls after cudaDeviceReset of a device are not supported
+// (the cached address belongs to the old context).
 #include <atomic>
 #include <mutex>
 
@@ -46,7 +48,10 @@ std::atomic<int32_t *> g_counters_of[kMaxDevices];   // per device id, set once
 std::mutex g_setup_mutex;
 
 // The device address of g_noalloc_counters for the current device, looked up
-// on the first call per device.
+// on the first call per device (with that device current) and cached for the
+// life of the process.  The cache is not told about a device reset: after
+// cudaDeviceReset the module is loaded again in a new context and the cached
+// address is stale, so calls after a reset of that device are not supported.
 cudaError_t noalloc_counters(int32_t **out)
 {
     int dev = 0;
@@ -73,7 +78,7 @@ cudaError_t noalloc_counters(int32_t **out)
 
 extern "C" {
 
-GDN_API int gdn_decode_conv_norm_noalloc(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode_conv_norm_noalloc(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                                          float *conv_state, int64_t conv_pitch, int taps,
                                          const float *x, const float *conv_w,
                                          const float *br, const float *ar, const float *dt, const float *rate,
@@ -84,12 +89,10 @@ GDN_API int gdn_decode_conv_norm_noalloc(void *state, int state_dtype, int64_t s
                                          int64_t out_stride, void *stream)
 {
     if (batch > 0 && nk > 0 && (int64_t)batch * nk > GDN_NOALLOC_MAX_KEY_HEADS) return GDN_ERR_UNSUPPORTED;
-    int32_t *counters = nullptr;
-    const cudaError_t e = gdn::noalloc_counters(&counters);
-    if (e != cudaSuccess) return gdn::report_cuda_error(e);
-    return gdn_decode_conv_norm(state, state_dtype, state_pitch, conv_state, conv_pitch, taps, x, conv_w,
-                                br, ar, dt, rate, z, gn, l2_eps, eps, out, counters, batch, nk, nv, d,
-                                x_stride, gate_stride, z_stride, out_stride, stream);
+    // the checks of gdn_decode_conv_norm run first; the address lookup only once they pass
+    return gdn::decode_conv_norm_entry(state, state_dtype, state_pitch, conv_state, conv_pitch, taps, x, conv_w,
+                                       br, ar, dt, rate, z, gn, l2_eps, eps, out, nullptr, gdn::noalloc_counters,
+                                       batch, nk, nv, d, x_stride, gate_stride, z_stride, out_stride, stream);
 }
 
 }  // extern "C"

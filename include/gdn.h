@@ -78,9 +78,18 @@ extern "C" {
 #define GDN_ERR_ALIGN 3        /* a pointer not aligned to its element size */
 #define GDN_ERR_ALIAS 4        /* an output overlaps another operand */
 #define GDN_ERR_CUDA 5         /* the CUDA launch failed (see gdn_last_cuda_error) */
+/* There is no timeout status: no kernel of the library waits on a flag, a
+ * counter or another block (only on its own barriers and copy groups).  A
+ * base, stride or pitch that rules out the 16-byte vector kernels is not an
+ * error either: the general kernel runs instead (GDN_ERR_ALIGN is only for a
+ * pointer not aligned to its own element size). */
 
 /* Storage type of the h-state. */
-typedef enum { GDN_STATE_F32 = 0, GDN_STATE_F16 = 1 } gdn_state_dtype;
+typedef enum {
+    GDN_STATE_F32 = 0,
+    GDN_STATE_F16 = 1,
+    GDN_STATE_DTYPE_MAX_ENUM = 0x7fffffff   /* not a dtype: keeps the type int-sized on every ABI */
+} gdn_state_dtype;
 
 /*
  * gdn_decode -- one token through the recurrence for `batch` sequences,
@@ -99,7 +108,7 @@ typedef enum { GDN_STATE_F32 = 0, GDN_STATE_F16 = 1 } gdn_state_dtype;
  *   Errors: GDN_ERR_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIGN, GDN_ERR_ALIAS
  *   (state or o overlapping any operand), GDN_ERR_CUDA.
  */
-GDN_API int gdn_decode(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                        const float *q, const float *k, const float *v,
                        const float *alpha, const float *beta, float *o,
                        int batch, int nk, int nv, int d,
@@ -121,7 +130,7 @@ GDN_API int gdn_decode(void *state, int state_dtype, int64_t state_pitch,
  *                rounded to nearest even.
  *   Other arguments and errors as gdn_decode.
  */
-GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode_norm(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                             const float *q, const float *k, const float *v,
                             const float *alpha, const float *beta,
                             const float *z, const float *gn, float eps,
@@ -150,7 +159,7 @@ GDN_API int gdn_decode_norm(void *state, int state_dtype, int64_t state_pitch,
  *   Other arguments and errors as gdn_decode_norm (xq, xs and y overlapping
  *   any operand: GDN_ERR_ALIAS).
  */
-GDN_API int gdn_decode_norm_q8(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode_norm_q8(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                                const float *q, const float *k, const float *v,
                                const float *alpha, const float *beta,
                                const float *z, const float *gn, float eps,
@@ -228,7 +237,7 @@ GDN_API int gdn_gate_norm_q8(const float *o, const float *z, const float *gn, fl
  *   r*NK, r < NV/NK).  State and output as gdn_decode_norm.
  *   Errors as gdn_decode_norm; GDN_ERR_UNSUPPORTED if NV % NK != 0.
  */
-GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode_conv_norm(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                                  float *conv_state, int64_t conv_pitch, int taps,
                                  const float *x, const float *conv_w,
                                  const float *br, const float *ar, const float *dt, const float *rate,
@@ -255,12 +264,15 @@ GDN_API int gdn_decode_conv_norm(void *state, int state_dtype, int64_t state_pit
  *   then undefined.  Calls ordered on one stream are fine.
  *   Arguments, layouts and results as gdn_decode_conv_norm (without
  *   workspace).
+ *   Calls after cudaDeviceReset of a device are not supported: the address
+ *   looked up before the reset belongs to the old context.
  *   Errors as gdn_decode_conv_norm; GDN_ERR_UNSUPPORTED if batch * NK >
- *   GDN_NOALLOC_MAX_KEY_HEADS (checked first); GDN_ERR_CUDA if the address
- *   lookup fails.
+ *   GDN_NOALLOC_MAX_KEY_HEADS (checked first); then every argument check of
+ *   gdn_decode_conv_norm, before any CUDA call (batch 0 returns GDN_OK with
+ *   no CUDA call); GDN_ERR_CUDA if the address lookup fails.
  */
 #define GDN_NOALLOC_MAX_KEY_HEADS 16384
-GDN_API int gdn_decode_conv_norm_noalloc(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode_conv_norm_noalloc(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                                          float *conv_state, int64_t conv_pitch, int taps,
                                          const float *x, const float *conv_w,
                                          const float *br, const float *ar, const float *dt, const float *rate,
@@ -290,7 +302,7 @@ GDN_API int gdn_decode_conv_norm_noalloc(void *state, int state_dtype, int64_t s
  *   bit, while the state is read once instead of twice.
  *   Errors as gdn_decode (state_mid overlapping any operand: GDN_ERR_ALIAS).
  */
-GDN_API int gdn_decode_chunk2(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_decode_chunk2(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                               void *state_mid, int64_t mid_pitch,
                               const float *q, const float *k, const float *v,
                               const float *alpha, const float *beta, float *o,
@@ -316,7 +328,7 @@ GDN_API int gdn_decode_chunk2(void *state, int state_dtype, int64_t state_pitch,
  *   call, up to fp32 rounding order.
  *   Errors as gdn_decode.
  */
-GDN_API int gdn_prefill_seq(void *state, int state_dtype, int64_t state_pitch,
+GDN_API int gdn_prefill_seq(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                             const float *q, const float *k, const float *v,
                             const float *alpha, const float *beta, float *o,
                             int batch, int seq_len, int nk, int nv, int d,

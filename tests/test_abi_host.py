@@ -155,9 +155,24 @@ def test_conv_norm_noalloc_rejects_beyond_static_counters(lib):
 
 
 def test_conv_norm_noalloc_without_device_reports_cuda_error(lib):
-    """On a host without a GPU the per-device set-up fails and says so (GDN_ERR_CUDA)."""
+    """On a host without a GPU a valid call passes every check, then the per-device set-up fails and
+    says so (GDN_ERR_CUDA)."""
     assert conv_norm_noalloc(lib) == CUDA
     assert lib.gdn_last_cuda_error() != 0
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(batch=0), OK),                                 # empty call: no CUDA call at all
+    (dict(state=None), ARG), (dict(ring=None), ARG), (dict(out=None), ARG), (dict(gn=None), ARG),
+    (dict(nk=0), ARG), (dict(d=0), ARG), (dict(taps=0), ARG), (dict(taps=9), ARG), (dict(eps=-1.0), ARG),
+    (dict(nv=5), UNSUP),                                 # NV not a multiple of NK
+    (dict(dt=2), UNSUP),
+    (dict(out=A + 4096), ALIAS),                         # output inside the state
+])
+def test_conv_norm_noalloc_checks_arguments_before_any_cuda_call(lib, kw, want):
+    """The argument checks of gdn_decode_conv_norm come before the address lookup: without a GPU
+    these calls still get their own status, not GDN_ERR_CUDA."""
+    assert conv_norm_noalloc(lib, **kw) == want
 
 
 def prefill(lib, **kw):
