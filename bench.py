@@ -54,9 +54,12 @@ REF_LAYERS_PER_STEP = 4      # oracle sample per step of the reference arm
 # dram__bytes_write.sum), valid only while the kernel source is the one it was taken on.
 NCU_TRAFFIC = {
     # mean of three mid-sequence launches of the full 48-layer workload, ncu --cache-control none
-    # (reads 102.9-103.0 MB, writes 96.2-99.4 MB), from the ncu capture of the batch-32 48-layer decode
-    "decode_norm_f32": {"bytes_per_launch": 201291947,
-                        "src_sha256": "a705afedce866b7ece345c0b2288507a9add0baf3a7a6825291108a3cbc60d6c"},
+    # (reads 102.9-103.1 MB, writes 96.4-99.6 MB), from the ncu capture of the batch-32 48-layer decode
+    "decode_norm_f32": {"bytes_per_launch": 201425664,
+                        "src_sha256": "cf5cb0f8aa290eb7f1bbcc53616eba2ec58c3e148f0e1b9c4ffb9d38dc623d74"},
+    # mean of two launches of the 256-slot fp16 pool decode (reads 413.3 MB, writes 388.7-388.8 MB)
+    "decode_norm_f16_pool": {"bytes_per_launch": 802121216,
+                             "src_sha256": "cf5cb0f8aa290eb7f1bbcc53616eba2ec58c3e148f0e1b9c4ffb9d38dc623d74"},
 }
 
 
@@ -87,6 +90,12 @@ def peaks():
             j = json.load(f)
         return {"hbm_gbs": float(j["hbm_gbs"]), "source": "measured", "sm_max_mhz": j.get("sm_max_mhz")}
     return {"hbm_gbs": 6800.0, "source": "fallback", "sm_max_mhz": 2070.0}
+
+
+def pinned_traffic(key):
+    """ncu DRAM bytes per launch for NCU_TRAFFIC[key], or None once the kernel source has changed."""
+    tr = NCU_TRAFFIC[key]
+    return tr["bytes_per_launch"] if tr["src_sha256"] == src_sha("gdn_decode.cu", "gdn_internal.cuh") else None
 
 
 def src_sha(*names):
@@ -322,8 +331,7 @@ def run_ours(args, rank, world, local_rank):
     launch_s = ms_step / 1e3 / L
     pk = peaks()
     achieved = bytes_launch / launch_s / 1e9
-    tr = NCU_TRAFFIC["decode_norm_f32"]
-    traffic = tr["bytes_per_launch"] if tr["src_sha256"] == src_sha("gdn_decode.cu", "gdn_internal.cuh") else None
+    traffic = pinned_traffic("decode_norm_f32")
 
     # ---- e2e: host inputs in pinned memory -> device, 48 launches, bf16 outputs -> host
     e2e = None if args.no_e2e else run_e2e(args, torch, gdn, state, x, outb, dev, stream, not args.no_graph)
@@ -615,7 +623,8 @@ def row_fp16_pool(torch, gdn, dev, stream, pk, want):
         rows["fp16_pool_decode_norm"] = {
             "config": "B=256 NK=16 NV=48 D=128, fp16 pool pitch 790528 halves, fused norm -> bf16",
             "us_per_step": s * 1e6, "token_heads_per_s": PB * NV / s, "achieved_gbs": by / s / 1e9,
-            "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}
+            "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by,
+            "traffic": pinned_traffic("decode_norm_f16_pool")}
         del x, ob
     del pool
     torch.cuda.empty_cache()
