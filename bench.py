@@ -92,6 +92,19 @@ def peaks():
     return {"hbm_gbs": 6800.0, "source": "fallback", "sm_max_mhz": 2070.0}
 
 
+def tf32_peak_flops(pk):
+    """Dense TF32 tensor peak: the measured bf16 burst peak times the nominal TF32 / bf16 ratio
+    (1.1 / 2.25 PFLOP/s), or the fallback bf16 figure when no measured file is present."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    bf16, src = 1.9e15, "fallback 1.9 PFLOP/s bf16"
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        if j.get("bf16_tflops"):
+            bf16, src = float(j["bf16_tflops"]) * 1e12, f"measured {j['bf16_tflops']} TFLOP/s bf16 burst"
+    return bf16 * 1.1 / 2.25, src + " x 1.1/2.25 (nominal TF32/bf16)"
+
+
 def pinned_traffic(key):
     """ncu DRAM bytes per launch for NCU_TRAFFIC[key], or None once the kernel source has changed."""
     tr = NCU_TRAFFIC[key]
@@ -697,6 +710,9 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
         gdn.gdn_prefill_seq(S, q, k, v, a, bt, o, batch=PB, seq_len=T, nk=NK, nv=NV, d=D, stream=sp)
 
     s = time_fn(torch, stream, pf, 3, warm=1)
+    # the same recurrence in chunks of 64 tokens on the tensor cores (gdn_prefill_chunked)
+    s_tc = time_fn(torch, stream, lambda: gdn.gdn_prefill_chunked(S, q, k, v, a, bt, o, batch=PB, seq_len=T, nk=NK,
+                                                                  nv=NV, d=D, stream=sp), 3, warm=1)
     # the same call on an fp16 state (widened once on load, carried in fp32, rounded once on store)
     S16 = torch.zeros((PB, NV, D, D), dtype=torch.float16, device=dev)
     s16 = time_fn(torch, stream, lambda: gdn.gdn_prefill_seq(S16, q, k, v, a, bt, o, batch=PB, seq_len=T, nk=NK,
@@ -719,6 +735,11 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     clk = (pk.get("sm_max_mhz") or 2070.0) * 1e6
     fma_peak = sms * 128 * clk          # FP32 FMA lanes x max clock: FMA per second
+    # chunked kernel: executed TF32 MMA work per 64-token chunk and head, three split passes each:
+    # G 128x64x128, Y 128x128x128, Delta 128x64x64, P Delta 128x64x64, Z 128x128x64 (multiply-adds)
+    tc_flop = 2 * 3 * (128 * 64 * 128 + 128 * 128 * 128 + 128 * 64 * 64 + 128 * 64 * 64 + 128 * 128 * 64) \
+        * PB * NV * ((T + 63) // 64)
+    tf32_peak, tf32_basis = tf32_peak_flops(pk)
     del q, k, v, a, bt, o, S, S16
     torch.cuda.empty_cache()
     return {"prefill": {"config": f"B=8 T={T} NK=16 NV=48 D=128 fp32, state on chip",
@@ -729,10 +750,19 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
                         "gate_norm_q8_of_outputs": {"us": s_q8 * 1e6, "achieved_gbs": q8_bytes / s_q8 / 1e9,
                                                     "frac_of_hbm_peak": q8_bytes / s_q8 / 1e9 / pk["hbm_gbs"],
                                                     "algorithmic_bytes": q8_bytes},
+                        "chunked_tensor_core": {
+                            "ms": s_tc * 1e3, "token_heads_per_s": th / s_tc, "speedup_vs_token_loop": s / s_tc,
+                            "roofline": {"bound": "tensor", "achieved": tc_flop / s_tc / 1e12,
+                                         "peak": tf32_peak / 1e12, "unit": "TFLOP/s (TF32 MMA, executed)",
+                                         "frac": tc_flop / s_tc / tf32_peak, "peak_basis": tf32_basis}},
                         "ms": s * 1e3, "token_heads_per_s": th / s,
                         "roofline": {"bound": "alu", "achieved": fma / s / 1e12, "peak": fma_peak / 1e12,
                                      "unit": "T FP32 FMA/s", "frac": fma / s / fma_peak,
-                                     "peak_basis": f"{sms} SMs x 128 FP32 lanes x {clk / 1e6:.0f} MHz"},
+                                     "frac_4d2_count": 4 / 3 * fma / s / fma_peak,
+                                     "peak_basis": f"{sms} SMs x 128 FP32 lanes x {clk / 1e6:.0f} MHz",
+                                     "count_basis": "frac: 3 D^2 FMA per token-head (S.k, the rank-1 write, S.q); "
+                                                    "frac_4d2_count: 4 D^2 FP32 instructions per token-head "
+                                                    "(the decay multiply counted apart)"},
                         "achieved_gbs": io / s / 1e9}}
 
 

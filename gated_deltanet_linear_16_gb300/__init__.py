@@ -23,6 +23,7 @@ __all__ = [
     "GdnError", "load", "build", "library_path",
     "GDN_STATE_F32", "GDN_STATE_F16", "STATUS",
     "gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
+    "gdn_prefill_chunked", "gdn_device_wait_timeouts",
     "gdn_decode_conv_norm_noalloc", "GDN_NOALLOC_MAX_KEY_HEADS", "gdn_decode_norm_q8",
     "gdn_gate_norm", "gdn_gate_norm_q8",
     "gdn_h_f32_to_f16", "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error",
@@ -73,9 +74,12 @@ def _declare(lib):
                                       i64, i64, i64, i64, P]
     lib.gdn_prefill_seq.argtypes = [P, i32, i64, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                     i64, i64, i64, i64, P]
+    lib.gdn_prefill_chunked.argtypes = lib.gdn_prefill_seq.argtypes
+    lib.gdn_device_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.gdn_h_f32_to_f16.argtypes = [P, P, u64, P]
     lib.gdn_h_f16_to_f32.argtypes = [P, P, u64, P]
     for fn in ("gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
+               "gdn_prefill_chunked", "gdn_device_wait_timeouts",
                "gdn_decode_conv_norm_noalloc", "gdn_decode_norm_q8", "gdn_gate_norm", "gdn_gate_norm_q8",
                "gdn_h_f32_to_f16",
                "gdn_h_f16_to_f32"):
@@ -291,13 +295,12 @@ def gdn_decode_chunk2(state, state_mid, q, k, v, alpha, beta, o, *, batch, nk, n
     _check("gdn_decode_chunk2", st)
 
 
-def gdn_prefill_seq(state, q, k, v, alpha, beta, o, *, batch, seq_len, nk, nv, d,
-                    state_pitch=None, state_dtype=None,
-                    qk_stride=None, v_stride=None, gb_stride=None, o_stride=None, stream=None):
-    """seq_len tokens per sequence in one launch (token rows b*seq_len + t); raw fp32 o."""
+def _prefill(fn, state, q, k, v, alpha, beta, o, *, batch, seq_len, nk, nv, d,
+             state_pitch=None, state_dtype=None,
+             qk_stride=None, v_stride=None, gb_stride=None, o_stride=None, stream=None):
     lib = load()
     sd = _state_dtype(state, state_dtype)
-    st = lib.gdn_prefill_seq(
+    st = getattr(lib, fn)(
         _ptr(state), sd, state_pitch if state_pitch is not None else nv * d * d,
         _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o),
         batch, seq_len, nk, nv, d,
@@ -306,7 +309,24 @@ def gdn_prefill_seq(state, q, k, v, alpha, beta, o, *, batch, seq_len, nk, nv, d
         gb_stride if gb_stride is not None else nv,
         o_stride if o_stride is not None else nv * d,
         _stream(stream))
-    _check("gdn_prefill_seq", st)
+    _check(fn, st)
+
+
+def gdn_prefill_seq(state, q, k, v, alpha, beta, o, **kw):
+    """seq_len tokens per sequence in one launch (token rows b*seq_len + t), token by token; raw fp32 o."""
+    _prefill("gdn_prefill_seq", state, q, k, v, alpha, beta, o, **kw)
+
+
+def gdn_prefill_chunked(state, q, k, v, alpha, beta, o, **kw):
+    """gdn_prefill_seq regrouped into chunks of 64 tokens on the tensor cores (D = 128); same arguments."""
+    _prefill("gdn_prefill_chunked", state, q, k, v, alpha, beta, o, **kw)
+
+
+def gdn_device_wait_timeouts() -> int:
+    """Bounded MMA-completion waits that ran out on the current device (0 when healthy); synchronises."""
+    c = ctypes.c_uint(0)
+    _check("gdn_device_wait_timeouts", load().gdn_device_wait_timeouts(ctypes.byref(c)))
+    return c.value
 
 
 def gdn_h_f32_to_f16(src, dst, n=None, stream=None):

@@ -28,7 +28,7 @@ NVCC_FLAGS = ARCH + [
 ]
 LINK_FLAGS = ARCH + ["-shared", "-cudart", "static"]
 SOURCES = ["gdn_abi.cu", "gdn_decode.cu", "gdn_chunk2.cu", "gdn_conv_norm.cu", "gdn_prefill.cu", "gdn_convert.cu",
-           "gdn_noalloc.cu", "gdn_norm.cu"]
+           "gdn_noalloc.cu", "gdn_norm.cu", "gdn_prefill_tc.cu"]
 
 
 def nvcc() -> str:

@@ -8,6 +8,7 @@
 
 #include "gdn.h"
 #include "gdn_internal.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 
@@ -292,6 +293,54 @@ int norm_entry(const float *o, const float *z, const float *gn, float eps, NormP
 
 }  // namespace
 
+// gdn_prefill_seq and gdn_prefill_chunked: the same checks; `chunked` takes the
+// tensor-core kernel where it applies (D == 128, 16-byte k and q rows).
+int prefill_entry(void *state, int state_dtype, int64_t state_pitch,
+                  const float *q, const float *k, const float *v,
+                  const float *alpha, const float *beta, float *o,
+                  int batch, int seq_len, int nk, int nv, int d,
+                  int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                  int64_t o_stride, void *stream, bool chunked)
+{
+    int st = check_common(batch, nk, nv, d, state_pitch, state_dtype);
+    if (st != GDN_OK) return st;
+    if (seq_len < 0) return GDN_ERR_ARG;
+    const int64_t selem = state_dtype == GDN_STATE_F16 ? 2 : 4;
+    const int64_t B = batch, R = (int64_t)batch * seq_len;
+    const int64_t hv = (int64_t)nv * d, hk = (int64_t)nk * d;
+    Operand ops[7] = {
+        {state, B, (int64_t)nv * d * d, state_pitch, selem},
+        {o, R, hv, o_stride, 4},
+        {q, R, hk, qk_stride, 4},
+        {k, R, hk, qk_stride, 4},
+        {v, R, hv, v_stride, 4},
+        {alpha, R, nv, gb_stride, 4},
+        {beta, R, nv, gb_stride, 4},
+    };
+    if (R == 0) {
+        for (auto &op : ops) if (op.p == nullptr) return GDN_ERR_ARG;
+        return GDN_OK;
+    }
+    st = check_operands(ops, 7, 2);
+    if (st != GDN_OK) return st;
+
+    PrefillParams p{};
+    p.state = state; p.pitch = state_pitch;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.o = o;
+    p.qk_stride = qk_stride; p.v_stride = v_stride; p.gb_stride = gb_stride; p.o_stride = o_stride;
+    p.batch = batch; p.seq_len = seq_len; p.nk = nk; p.nv = nv; p.d = d;
+    p.inv_sqrt_d = inv_sqrt(d);
+    p.zero = 0;
+    // D == 128 path: 16-byte state rows, 16-byte k/q rows and 16-byte v row blocks
+    const bool fast = d == 128 && vec16(state) && (state_pitch * selem) % 16 == 0 &&
+                      vec16(q) && vec16(k) && (qk_stride * 4) % 16 == 0 &&
+                      vec16(v) && (v_stride * 4) % 16 == 0;
+    if (chunked && d == 128 && vec16(q) && vec16(k) && (qk_stride * 4) % 16 == 0)
+        return cuda_status(launch_prefill_tc(p, state_dtype == GDN_STATE_F16, (cudaStream_t)stream));
+    return cuda_status(launch_prefill(p, state_dtype == GDN_STATE_F16, fast, (cudaStream_t)stream));
+}
+
+
 }  // namespace gdn
 
 using namespace gdn;
@@ -410,40 +459,25 @@ GDN_API int gdn_prefill_seq(void *state, gdn_state_dtype state_dtype, int64_t st
                             int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
                             int64_t o_stride, void *stream)
 {
-    int st = check_common(batch, nk, nv, d, state_pitch, state_dtype);
-    if (st != GDN_OK) return st;
-    if (seq_len < 0) return GDN_ERR_ARG;
-    const int64_t selem = state_dtype == GDN_STATE_F16 ? 2 : 4;
-    const int64_t B = batch, R = (int64_t)batch * seq_len;
-    const int64_t hv = (int64_t)nv * d, hk = (int64_t)nk * d;
-    Operand ops[7] = {
-        {state, B, (int64_t)nv * d * d, state_pitch, selem},
-        {o, R, hv, o_stride, 4},
-        {q, R, hk, qk_stride, 4},
-        {k, R, hk, qk_stride, 4},
-        {v, R, hv, v_stride, 4},
-        {alpha, R, nv, gb_stride, 4},
-        {beta, R, nv, gb_stride, 4},
-    };
-    if (R == 0) {
-        for (auto &op : ops) if (op.p == nullptr) return GDN_ERR_ARG;
-        return GDN_OK;
-    }
-    st = check_operands(ops, 7, 2);
-    if (st != GDN_OK) return st;
+    return prefill_entry(state, state_dtype, state_pitch, q, k, v, alpha, beta, o, batch, seq_len, nk, nv, d,
+                         qk_stride, v_stride, gb_stride, o_stride, stream, false);
+}
 
-    PrefillParams p{};
-    p.state = state; p.pitch = state_pitch;
-    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.o = o;
-    p.qk_stride = qk_stride; p.v_stride = v_stride; p.gb_stride = gb_stride; p.o_stride = o_stride;
-    p.batch = batch; p.seq_len = seq_len; p.nk = nk; p.nv = nv; p.d = d;
-    p.inv_sqrt_d = inv_sqrt(d);
-    p.zero = 0;
-    // D == 128 path: 16-byte state rows, 16-byte k/q rows and 16-byte v row blocks
-    const bool fast = d == 128 && vec16(state) && (state_pitch * selem) % 16 == 0 &&
-                      vec16(q) && vec16(k) && (qk_stride * 4) % 16 == 0 &&
-                      vec16(v) && (v_stride * 4) % 16 == 0;
-    return cuda_status(launch_prefill(p, state_dtype == GDN_STATE_F16, fast, (cudaStream_t)stream));
+GDN_API int gdn_prefill_chunked(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
+                                const float *q, const float *k, const float *v,
+                                const float *alpha, const float *beta, float *o,
+                                int batch, int seq_len, int nk, int nv, int d,
+                                int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                                int64_t o_stride, void *stream)
+{
+    return prefill_entry(state, state_dtype, state_pitch, q, k, v, alpha, beta, o, batch, seq_len, nk, nv, d,
+                         qk_stride, v_stride, gb_stride, o_stride, stream, true);
+}
+
+GDN_API int gdn_device_wait_timeouts(unsigned *count)
+{
+    if (count == nullptr) return GDN_ERR_ARG;
+    return cuda_status(tc_wait_timeouts(count));
 }
 
 GDN_API int gdn_gate_norm(const float *o, const float *z, const float *gn, float eps, uint16_t *out,

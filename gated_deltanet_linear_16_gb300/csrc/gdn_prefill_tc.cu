@@ -1,0 +1,653 @@
+// gdn_prefill_tc.cu -- the prefill recurrence regrouped into chunks of 64
+// tokens, with the chunk's matrix products on the fifth-generation tensor
+// cores (tcgen05, TF32 operands split in two for fp32-level accuracy).
+//
+// The recurrence is the one of logicaffeine_compile/codegen_cuda/gdn.rs,
+// kernel `gdn_step`, applied token by token as
+// metrale_model_layers/layers/ops/ssm_gdn_a.rs, `gdn_prefill_regresident`,
+// does: S_t = alpha_t S_{t-1} + delta_t k_t^T with
+// delta_t = beta_t (v_t - alpha_t S_{t-1} k_t), o_t = S_t q_t / sqrt(D).
+// Unrolled over a chunk of C tokens from the state S at its start (gamma_t =
+// alpha_1 ... alpha_t, rho(t,i) = gamma_t / gamma_i = alpha_{i+1} ... alpha_t):
+//
+//   S_t   = gamma_t S + sum_{i<=t} rho(t,i) delta_i k_i^T
+//   delta_t + beta_t sum_{i<t} rho(t,i) (k_t.k_i) delta_i = beta_t (v_t - gamma_t S k_t)
+//   o_t   = (gamma_t S q_t + sum_{i<=t} rho(t,i) (q_t.k_i) delta_i) / sqrt(D)
+//
+// i.e. (I + A) Delta = R with A[t][i] = beta_t rho(t,i) k_t.k_i (i < t), so
+// Delta = T R with T = (I + A)^-1 (unit lower triangular), and at the chunk's
+// end S <- gamma_C S + Delta^T Ktilde with Ktilde[t] = rho(C,t) k_t.  This is
+// the same arithmetic in real numbers (the chunked "WY" form of the delta
+// rule); only the fp32 rounding differs.  Per chunk and head, in order:
+//
+//   MMA-1  G = [K;Q] K^T (128 x 64)  and  Y = S [K;Q]^T (128 x 128, S from TMEM)
+//   SIMT   A and P[t][i] = rho(t,i) q_t.k_i from G;  R^T = beta (v - gamma Y_K)
+//          into TMEM;  T = (I + A)^-1;  Ktilde^T;  P, T, Ktilde^T to smem
+//   MMA-2  Delta^T = R^T T^T (128 x 64)
+//   SIMT   Delta^T split into TMEM
+//   MMA-3  P Delta as (Delta^T P^T) (128 x 64)  and  Z = Delta^T Ktilde (128 x 128)
+//   SIMT   o_t = (gamma_t Y_Q + P Delta) / sqrt(D);  S <- gamma_C S + Z, split into TMEM
+//
+// Every MMA operand x is split as x = hi + lo with hi and lo TF32 values, and
+// a product is taken as hi*hi + hi*lo + lo*hi (three MMAs), which carries about
+// 22 significant bits per product; the accumulators are fp32 in tensor memory.
+// The exact fp32 state stays in registers (thread = row a of the head, half of
+// its columns); only its split copy is in tensor memory.
+//
+// One CTA (8 warps) per (sequence, value head); warp w owns tensor-memory lanes
+// 32*(w%4).. (rows of the state) and half w/4 of the columns it loads.  Thread
+// 64 (lane 0 of warp 2, a warp with no part in the inversion) issues the MMAs,
+// so the other warps go on while the tensor core takes them.  The next chunk's
+// k, q, alpha and beta are copied into shared memory (cp.async) during the
+// current chunk.  The CTA holds all 512 tensor-memory columns and ~210 KB of
+// shared memory, so an SM runs one such CTA at a time.  The only waits are on the CTA's own MMA
+// completions (an mbarrier armed by tcgen05.commit), each bounded: if a bound
+// ran out, the CTA stops, counts the event in g_tc_wait_timeouts and writes
+// NaN to its outputs.
+#include "gdn_internal.cuh"
+#include "gdn_tc.cuh"
+
+__device__ unsigned int g_tc_wait_timeouts;
+
+namespace gdn {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kC = 64;                       // tokens per chunk
+constexpr int kThreads = 256;
+// MMA-issuing threads: lane 0 of warps 2, 3 and 6 (no part in building A or in the inversion).  One
+// thread issues about one MMA per ~140 cycles whatever its N, while the tensor core takes MMAs from
+// several threads at once, so each product is split over up to three issuers, each pass of the
+// precision split (hi*hi, hi*lo, lo*hi) into its own accumulator, summed by the SIMT phase after.
+constexpr int kIss0 = 64, kIss1 = 96, kIss2 = 192;
+constexpr uint32_t kWaitLimit = 1u << 22;    // polls of an mbarrier phase before giving up
+
+// shared memory (1024-aligned), byte offsets
+constexpr uint32_t kKQHi = 0, kKQLo = 65536;           // [K;Q]: 128 rows x 128, until MMA-1 is done
+constexpr uint32_t kTHi = 0, kTLo = 16384;             // T: 64 rows (t) x 64 (i), after MMA-1
+// B operand of MMA-3, 192 rows x 64 (K = t or i): rows 0-127 Ktilde^T (row c), rows 128-191 P (row t)
+constexpr uint32_t kBHi = 32768, kBLo = 81920;
+constexpr int kBRows = 192;
+constexpr uint32_t kStage = 131072;                    // next chunk's raw [K;Q], 128 rows x 512 B
+// fp32 64 x 64 work matrix W (row stride kAS): A in its strict lower triangle, T = (I + A)^-1
+// transposed in its upper triangle and diagonal (T[t][j] at W[j][t]); then a 32 x 33 scratch.
+constexpr int kAS = 65, kXS = 33;
+constexpr uint32_t kWOff = kStage + 65536, kXsOff = kWOff + kC * kAS * 4;
+constexpr uint32_t kSmemBytes = kXsOff + 32 * kXS * 4 + 1024;          // + alignment slack
+
+// tensor-memory columns
+constexpr uint32_t kSHi = 0, kSLo = 128;     // split state (A operand of Y)
+constexpr uint32_t kY = 256, kYQ = 320;      // Y = S [K;Q]^T: columns t of K, then of Q (all three passes)
+constexpr uint32_t kG = 384, kGb = 448;      // G = [K;Q] K^T: passes hh + hl, and pass lh
+constexpr uint32_t kRHi = 384, kRLo = 448;   // split R^T (after G is read)
+constexpr uint32_t kD1 = 128, kD2 = 0, kD3 = 64;   // Delta^T = R^T T^T, one accumulator per pass (after Y)
+constexpr uint32_t kDtHi = 192, kDtLo = 256; // split Delta^T
+// Delta^T [Ktilde | P^T] (N = 192): passes hh + hl at kM3a, pass lh at kM3b; Z in the first 128
+// columns of each, (P Delta)^T in the last 64
+constexpr uint32_t kM3a = 0, kM3b = 320;
+
+struct __align__(16) ChunkScalars {
+    float gamma[kC];          // gamma_t = alpha_0 ... alpha_t (chunk-local, t from 0)
+    float rho_last[kC];       // rho(C-1, t) = alpha_{t+1} ... alpha_{C-1}
+    float sigma[kC];          // sigma_i = alpha_32 ... alpha_i for i >= 32 (= rho(i, 31))
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t a)
+{
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void cp_async16_s(uint32_t saddr, const void *gmem)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4_s(uint32_t saddr, const void *gmem)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(saddr), "l"(gmem) : "memory");
+}
+// Four split values stored as 16-byte hi and lo vectors.
+__device__ __forceinline__ void st_split4(uint32_t hi_addr, uint32_t lo_addr, float a, float b, float c, float d)
+{
+    uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+    tc::split_tf32(a, h0, l0); tc::split_tf32(b, h1, l1);
+    tc::split_tf32(c, h2, l2); tc::split_tf32(d, h3, l3);
+    st_shared_v4(hi_addr, h0, h1, h2, h3);
+    st_shared_v4(lo_addr, l0, l1, l2, l3);
+}
+
+// Passes [p0, p1) of the split product over K/8 steps: pass 0 = A_hi B_hi, 1 = A_hi B_lo, 2 =
+// A_lo B_hi, all into D (the first MMA overwrites it).  A in shared memory (a_hi/a_lo descriptors'
+// base addresses) or tensor memory.  Issued by one thread.  The loops stay rolled: this kernel's
+// code is run once per chunk by few warps, so its size (instruction fetch) matters more than the
+// loop overhead.
+template <bool A_TMEM>
+__device__ __forceinline__ void mma_passes(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
+                                           uint32_t a_block, uint32_t b_block, int ksteps, uint32_t idesc,
+                                           int p0, int p1)
+{
+#pragma unroll 1
+    for (int pass = p0; pass < p1; ++pass) {
+        const uint32_t a = pass == 2 ? a_lo : a_hi;
+        const uint32_t b = pass == 1 ? b_lo : b_hi;
+#pragma unroll 1
+        for (int kk = 0; kk < ksteps; ++kk) {
+            const uint32_t acc = (pass > p0 || kk > 0) ? 1u : 0u;
+            const uint64_t bd = tc::smem_desc_sw128(b + (kk >> 2) * b_block + (kk & 3) * 32);
+            if constexpr (A_TMEM) {
+                tc::mma_ts(d, a + kk * 8, bd, idesc, acc);
+            } else {
+                tc::mma_ss(d, tc::smem_desc_sw128(a + (kk >> 2) * a_block + (kk & 3) * 32), bd, idesc, acc);
+            }
+        }
+    }
+}
+
+// Every thread: tensor-core ops and shared-memory writes so far are visible to
+// the MMA-issuing thread after this.
+__device__ __forceinline__ void sync_for_mma()
+{
+    tc::fence_smem_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+}
+// Every thread waits for the mbarrier phase; the CTA agrees on the outcome.
+__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t parity)
+{
+    const bool ok = __syncthreads_and(tc::mbar_wait(bar, parity, kWaitLimit)) != 0;
+    tc::fence_after_sync();
+    return ok;
+}
+
+// Copy chunk [c0, c0 + n) of k, q (raw rows into the staging buffer, row-major)
+// and alpha, beta (into ab[0], ab[1]) with cp.async; padding tokens get k = q =
+// 0, alpha = 1, beta = 0.  Warp w copies rows 16w .. 16w+15 (K rows t, then Q
+// rows), lane l their 16-byte chunk l; the same thread later splits exactly
+// these chunks, so only its own cp.async wait is needed before it reads them.
+__device__ __forceinline__ void prefetch_chunk(uint32_t stage, float (*ab)[kC], const float *kbase, const float *qbase,
+                                               const PrefillParams &p, int seq, int h, int c0, int n, int warp,
+                                               int lane, int tid)
+{
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+        const int row = 16 * warp + i, t = row & (kC - 1);
+        const uint32_t dst = stage + row * 512 + lane * 16;
+        if (t < n) cp_async16_s(dst, (row < kC ? kbase : qbase) + (int64_t)(c0 + t) * p.qk_stride + 4 * lane);
+        else st_shared_v4(dst, 0u, 0u, 0u, 0u);
+    }
+    if (tid < kC) {
+        const uint32_t sa = (uint32_t)__cvta_generic_to_shared(&ab[0][tid]);
+        const uint32_t sb = (uint32_t)__cvta_generic_to_shared(&ab[1][tid]);
+        if (tid < n) {
+            const int64_t row = (int64_t)seq * p.seq_len + c0 + tid;
+            cp_async4_s(sa, p.alpha + row * p.gb_stride + h);
+            cp_async4_s(sb, p.beta + row * p.gb_stride + h);
+        } else {
+            st_shared_b32(sa, __float_as_uint(1.0f));
+            st_shared_b32(sb, 0u);
+        }
+    }
+    cp_async_commit();
+}
+
+// Barrier among the 128 threads of warps 0, 1, 4 and 5 (named barrier 1).
+__device__ __forceinline__ void sync_a_warps() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// T = (I + A)^-1 for the strictly lower triangular 64 x 64 A in W (row stride
+// kAS); T[t][j] (t >= j) is written to W[j][t], the upper triangle and the
+// diagonal, which A leaves free.  By the 128 threads of warps 0, 1, 4, 5 (it =
+// 0..127): the four 16 x 16 diagonal blocks by forward substitution (a thread
+// per column), then the blocks under the diagonal from [[M11, 0], [M21, M22]]^-1
+// = [[T11, 0], [-T22 M21 T11, T22]]: the two 16 x 16 ones, then the 32 x 32 one,
+// each product with several output columns per thread.  Xs: 32 x 33 scratch.
+__device__ __forceinline__ void invert_unit_lower(float *W, float *Xs, int it)
+{
+    auto A = [&](int t, int i) -> float { return W[t * kAS + i]; };
+    auto Tr = [&](int t, int j) -> float & { return W[j * kAS + t]; };
+    if (it < kC) {
+        const int kb = it >> 4, jj = it & 15, base = 16 * kb;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = i == jj ? 1.0f : 0.0f;
+#pragma unroll
+        for (int t = 1; t < 16; ++t) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int i = 0; i + 1 < t; i += 2) {
+                a0 = fmaf(A(base + t, base + i), x[i], a0);
+                a1 = fmaf(A(base + t, base + i + 1), x[i + 1], a1);
+            }
+            if (t & 1) a0 = fmaf(A(base + t, base + t - 1), x[t - 1], a0);
+            if (t > jj) x[t] = -(a0 + a1);
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            if (t >= jj) Tr(base + t, base + jj) = x[t];
+    }
+    sync_a_warps();
+    {   // X = M21 T11 for the pairs (rows 16..31, cols 0..15) and (rows 48..63, cols 32..47): row t, cols 4 jq..+3
+        const int b = it >> 6, t = (it >> 2) & 15, j0 = 4 * (it & 3), base = 32 * b;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float a = A(base + 16 + t, base + i);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                acc[e] = fmaf(a, i >= j0 + e ? Tr(base + i, base + j0 + e) : 0.0f, acc[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) Xs[(16 * b + t) * kXS + j0 + e] = acc[e];
+    }
+    sync_a_warps();
+    {   // T21 = -T22 X for the two pairs
+        const int b = it >> 6, t = (it >> 2) & 15, j0 = 4 * (it & 3), base = 32 * b;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float tv = i <= t ? Tr(base + 16 + t, base + 16 + i) : 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = fmaf(tv, Xs[(16 * b + i) * kXS + j0 + e], acc[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) Tr(base + 16 + t, base + j0 + e) = -acc[e];
+    }
+    sync_a_warps();
+    {   // X = M21 T11 for the 32 x 32 halves: row t, cols 8 jq .. +7
+        const int t = it >> 2, j0 = 8 * (it & 3);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+            const float a = A(32 + t, i);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(a, i >= j0 + e ? Tr(i, j0 + e) : 0.0f, acc[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) Xs[t * kXS + j0 + e] = acc[e];
+    }
+    sync_a_warps();
+    {   // T21 = -T22 X
+        const int t = it >> 2, j0 = 8 * (it & 3);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+            const float tv = i <= t ? Tr(32 + t, 32 + i) : 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(tv, Xs[i * kXS + j0 + e], acc[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) Tr(32 + t, j0 + e) = -acc[e];
+    }
+}
+
+template <typename TS>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_d128(const PrefillParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    float *W = reinterpret_cast<float *>(smem + kWOff);
+    float *Xs = reinterpret_cast<float *>(smem + kXsOff);
+    __shared__ ChunkScalars sc;
+    __shared__ __align__(16) float ab[2][2][kC];    // [chunk parity][alpha, beta][t]
+    __shared__ uint64_t bars[4];                    // G (2 issuers), Y (1), MMA-2 (3), MMA-3 (2)
+    __shared__ uint32_t tmem_base;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, hf = warp >> 2;
+    const int r = 32 * quad + lane;                 // tensor-memory lane = state row a = token row
+    const uint32_t lanebase = (uint32_t)(32 * quad) << 16;
+    const int head = blockIdx.x;
+    const int seq = head / p.nv;
+    const int h = head - seq * p.nv;
+    const int g = h % p.nk;
+    const int T = p.seq_len;
+    const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+
+    const float *kbase = p.k + (int64_t)seq * T * p.qk_stride + (int64_t)g * kD;
+    const float *qbase = p.q + (int64_t)seq * T * p.qk_stride + (int64_t)g * kD;
+    const float *vbase = p.v + (int64_t)seq * T * p.v_stride + (int64_t)h * kD;
+    float *obase = p.o + (int64_t)seq * T * p.o_stride + (int64_t)h * kD;
+
+    prefetch_chunk(sbase + kStage, ab[0], kbase, qbase, p, seq, h, 0, min(kC, T), warp, lane, tid);
+    if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
+    if (tid == 0) {
+        tc::mbar_init(&bars[0], 2);
+        tc::mbar_init(&bars[1], 1);
+        tc::mbar_init(&bars[2], 3);
+        tc::mbar_init(&bars[3], 2);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = tmem_base + lanebase;       // this warp's lanes
+    uint32_t ph = 0;                                // parity of this chunk's phase of each barrier
+
+    // the exact state: row r, columns 64*hf .. +63, in registers
+    TS *srow = reinterpret_cast<TS *>(p.state) + seq * p.pitch + (int64_t)h * kD * kD + (int64_t)r * kD + 64 * hf;
+    float S[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) S[j] = to_f32<TS>(srow[j]);
+    bool ok = true;
+
+    for (int c0 = 0, par = 0; c0 < T && ok; c0 += kC, par ^= 1) {
+        const int n = min(kC, T - c0);
+        const float *alpha = ab[par][0], *beta = ab[par][1];
+        // ---- 0. the state, split, into tensor memory (A operand of Y) ----
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) tc::split_tf32(S[32 * cb + j], hi[j], lo[j]);
+            tc::tmem_st32(tm + kSHi + 64 * hf + 32 * cb, hi);
+            tc::tmem_st32(tm + kSLo + 64 * hf + 32 * cb, lo);
+        }
+        tc::st_wait();
+        // ---- 1. this thread's staged [K;Q] chunks, split into the operand buffer ----
+        cp_async_wait<0>();
+#pragma unroll 2
+        for (int i = 0; i < 16; ++i) {
+            const int row = 16 * warp + i;
+            const uint4 x = ld_shared_v4(sbase + kStage + row * 512 + lane * 16);
+            const uint32_t off = tc::sw128_offset(row, 4 * lane, 128);
+            st_split4(sbase + kKQHi + off, sbase + kKQLo + off, __uint_as_float(x.x), __uint_as_float(x.y),
+                      __uint_as_float(x.z), __uint_as_float(x.w));
+        }
+        __syncthreads();                                   // alpha, beta landed (their copiers waited)
+        if (warp < 3) {   // products of the decays: gamma (prefix), rho(C-1, .) (suffix), sigma (prefix from 32)
+            if (warp == 2) {
+                float pr = alpha[32 + lane];
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const float y = __shfl_up_sync(kFull, pr, d);
+                    if (lane >= d) pr = y * pr;
+                }
+                sc.sigma[32 + lane] = pr;
+            } else {
+                const float a0 = alpha[2 * lane], a1 = alpha[2 * lane + 1];
+                float pr = a0 * a1;
+                if (warp == 0) {
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const float y = __shfl_up_sync(kFull, pr, d);
+                        if (lane >= d) pr = y * pr;
+                    }
+                    float ex = __shfl_up_sync(kFull, pr, 1);
+                    if (lane == 0) ex = 1.0f;
+                    const float g0 = ex * a0;
+                    sc.gamma[2 * lane] = g0;
+                    sc.gamma[2 * lane + 1] = g0 * a1;
+                } else {
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const float y = __shfl_down_sync(kFull, pr, d);
+                        if (lane + d < 32) pr = y * pr;
+                    }
+                    float ex = __shfl_down_sync(kFull, pr, 1);
+                    if (lane == 31) ex = 1.0f;
+                    sc.rho_last[2 * lane + 1] = ex;
+                    sc.rho_last[2 * lane] = a1 * ex;
+                }
+            }
+        }
+
+        // ---- MMA-1: G = [K;Q] K^T (two issuers, bars[0]) and Y = S [K;Q]^T (one issuer, bars[1]) ----
+        sync_for_mma();
+        if (tid == kIss0 || tid == kIss2) {
+            const bool first = tid == kIss0;
+            mma_passes<false>(tmem_base + (first ? kG : kGb), sbase + kKQHi, sbase + kKQLo, sbase + kKQHi,
+                              sbase + kKQLo, 128 * 128, 128 * 128, kD / 8, tc::idesc_tf32(128, 64),
+                              first ? 0 : 2, first ? 2 : 3);
+            tc::mma_commit(&bars[0]);
+        } else if (tid == kIss1) {
+            mma_passes<true>(tmem_base + kY, tmem_base + kSHi, tmem_base + kSLo, sbase + kKQHi, sbase + kKQLo,
+                             0, 128 * 128, kD / 8, tc::idesc_tf32(128, 128), 0, 3);
+            tc::mma_commit(&bars[1]);
+        }
+        __syncwarp();
+        // the next chunk's inputs on their way while this one is computed
+        if (c0 + kC < T)
+            prefetch_chunk(sbase + kStage, ab[par ^ 1], kbase, qbase, p, seq, h, c0 + kC, min(kC, T - c0 - kC),
+                           warp, lane, tid);
+        // v_t[a] for t = 32 hf + j, a = r (coalesced across the warp's lanes)
+        float vv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int t = 32 * hf + j;
+            vv[j] = t < n ? __ldg(vbase + (int64_t)(c0 + t) * p.v_stride + r) : 0.0f;
+        }
+        // ---- 2. A from G and T = (I + A)^-1, by warps 0, 1, 4, 5 (lanes 0-63) while Y is still on the
+        //         tensor core; the issuer's warp 2 and the others wait for Y ----
+        bool ok_g = true;
+        if (r < kC) {
+            ok_g = tc::mbar_wait(&bars[0], ph, kWaitLimit);
+            tc::fence_after_sync();
+            // A[t][i] = beta_t rho(t,i) k_t.k_i, t = r, i = 32 hf + 8 grp + e, walked downwards
+            const int t = r;
+            float pr = (hf == 0 && t >= 32) ? sc.sigma[t] : 1.0f;
+            const float bt = beta[t];
+#pragma unroll 1
+            for (int grp = 3; grp >= 0; --grp) {
+                float gv[8], gw[8];
+                tc::tmem_ld8(tm + kG + 32 * hf + 8 * grp, gv);
+                tc::tmem_ld8(tm + kGb + 32 * hf + 8 * grp, gw);
+                tc::ld_wait();
+#pragma unroll
+                for (int e = 7; e >= 0; --e) {
+                    const int i = 32 * hf + 8 * grp + e;
+                    if (i < t) W[t * kAS + i] = bt * pr * (gv[e] + gw[e]);
+                    if (i <= t) pr *= alpha[i];
+                }
+            }
+            sync_a_warps();                                // A complete
+            invert_unit_lower(W, Xs, (warp & 1) * 32 + lane + 64 * hf);
+            tc::fence_before_sync();
+        }
+        ok = __syncthreads_and(ok_g && tc::mbar_wait(&bars[1], ph, kWaitLimit)) != 0;    // T complete, Y done
+        tc::fence_after_sync();
+        if (!ok) break;
+        // k_t[c] = hi + lo (exact) from the operand buffer before T overwrites it; t = 32 hf + j, c = r
+        float kv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t off = tc::sw128_offset(32 * hf + j, r, 128);
+            kv[j] = ld_shared_f32(sbase + kKQHi + off) + ld_shared_f32(sbase + kKQLo + off);
+        }
+        __syncthreads();
+
+        // ---- 2b. operands of MMA-2 and MMA-3: T, P, Ktilde^T to shared memory, R^T to tensor memory ----
+        {   // T: row t = tid / 4, columns 16 (tid % 4) .. +15 (zero above the diagonal)
+            const int t = tid >> 2, cb = (tid & 3) * 16;
+#pragma unroll 1
+            for (int jc = 0; jc < 4; ++jc) {
+                const int c = cb + 4 * jc;
+                const uint32_t off = tc::sw128_offset(t, c, kC);
+                st_split4(sbase + kTHi + off, sbase + kTLo + off,
+                          c <= t ? W[c * kAS + t] : 0.0f, c + 1 <= t ? W[(c + 1) * kAS + t] : 0.0f,
+                          c + 2 <= t ? W[(c + 2) * kAS + t] : 0.0f, c + 3 <= t ? W[(c + 3) * kAS + t] : 0.0f);
+            }
+        }
+        if (r >= kC) {    // P[t][i] = rho(t,i) q_t.k_i from G row 64 + t, i = 32 hf + 8 grp + e (zero for i > t)
+            const int t = r - kC;
+            float pr = (hf == 0 && t >= 32) ? sc.sigma[t] : 1.0f;
+#pragma unroll 1
+            for (int grp = 3; grp >= 0; --grp) {
+                float gv[8], gw[8];
+                tc::tmem_ld8(tm + kG + 32 * hf + 8 * grp, gv);
+                tc::tmem_ld8(tm + kGb + 32 * hf + 8 * grp, gw);
+                tc::ld_wait();
+#pragma unroll
+                for (int e = 7; e >= 0; --e) {
+                    const int i = 32 * hf + 8 * grp + e;
+                    gv[e] = i <= t ? pr * (gv[e] + gw[e]) : 0.0f;
+                    if (i <= t) pr *= alpha[i];
+                }
+                const uint32_t off = tc::sw128_offset(128 + t, 32 * hf + 8 * grp, kBRows);
+                st_split4(sbase + kBHi + off, sbase + kBLo + off, gv[0], gv[1], gv[2], gv[3]);
+                const uint32_t off2 = tc::sw128_offset(128 + t, 32 * hf + 8 * grp + 4, kBRows);
+                st_split4(sbase + kBHi + off2, sbase + kBLo + off2, gv[4], gv[5], gv[6], gv[7]);
+            }
+        }
+        {   // Ktilde^T[c][t] = rho(C-1, t) k_t[c]: row c = r, columns t = 32 hf + j (one K block)
+#pragma unroll
+            for (int jc = 0; jc < 8; ++jc) {
+                const float4 rl = *reinterpret_cast<const float4 *>(sc.rho_last + 32 * hf + 4 * jc);
+                const uint32_t off = tc::sw128_offset(r, 32 * hf + 4 * jc, kBRows);
+                st_split4(sbase + kBHi + off, sbase + kBLo + off, rl.x * kv[4 * jc], rl.y * kv[4 * jc + 1],
+                          rl.z * kv[4 * jc + 2], rl.w * kv[4 * jc + 3]);
+            }
+        }
+        {   // R^T[a][t] = beta_t (v_t[a] - gamma_t Y_K[a][t]), t = 32 hf + j, over G's columns (each
+            // warp writes only the columns it alone read, or that no warp reads)
+            float yk[32];
+            tc::tmem_ld32(tm + kY + 32 * hf, yk);
+            tc::ld_wait();
+            uint32_t rhi[32], rlo[32];
+#pragma unroll
+            for (int jc = 0; jc < 8; ++jc) {
+                const float4 bt = *reinterpret_cast<const float4 *>(beta + 32 * hf + 4 * jc);
+                const float4 gm = *reinterpret_cast<const float4 *>(sc.gamma + 32 * hf + 4 * jc);
+                const int j = 4 * jc;
+                tc::split_tf32(bt.x * (vv[j] - gm.x * yk[j]), rhi[j], rlo[j]);
+                tc::split_tf32(bt.y * (vv[j + 1] - gm.y * yk[j + 1]), rhi[j + 1], rlo[j + 1]);
+                tc::split_tf32(bt.z * (vv[j + 2] - gm.z * yk[j + 2]), rhi[j + 2], rlo[j + 2]);
+                tc::split_tf32(bt.w * (vv[j + 3] - gm.w * yk[j + 3]), rhi[j + 3], rlo[j + 3]);
+            }
+            tc::tmem_st32(tm + kRHi + 32 * hf, rhi);
+            tc::tmem_st32(tm + kRLo + 32 * hf, rlo);
+            tc::st_wait();
+        }
+
+        // ---- MMA-2: Delta^T = R^T T^T, one pass per issuer and accumulator ----
+        sync_for_mma();
+        if (tid == kIss0 || tid == kIss1 || tid == kIss2) {
+            const int pass = tid == kIss0 ? 0 : (tid == kIss1 ? 1 : 2);
+            mma_passes<true>(tmem_base + (pass == 0 ? kD1 : (pass == 1 ? kD2 : kD3)), tmem_base + kRHi,
+                             tmem_base + kRLo, sbase + kTHi, sbase + kTLo, 0, kC * 128, kC / 8,
+                             tc::idesc_tf32(128, 64), pass, pass + 1);
+            tc::mma_commit(&bars[2]);
+        }
+        __syncwarp();
+        ok = wait_mma(&bars[2], ph);
+        if (!ok) break;
+
+        // ---- 3. Delta^T = sum of the three passes, split; Y_Q kept for the outputs ----
+        float yq[32];
+        tc::tmem_ld32(tm + kYQ + 32 * hf, yq);
+#pragma unroll 1
+        for (int grp = 0; grp < 4; ++grp) {
+            float d1[8], d2[8], d3[8];
+            tc::tmem_ld8(tm + kD1 + 32 * hf + 8 * grp, d1);
+            tc::tmem_ld8(tm + kD2 + 32 * hf + 8 * grp, d2);
+            tc::tmem_ld8(tm + kD3 + 32 * hf + 8 * grp, d3);
+            tc::ld_wait();
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tc::split_tf32(d1[e] + (d2[e] + d3[e]), hi[e], lo[e]);
+            tc::tmem_st8(tm + kDtHi + 32 * hf + 8 * grp, hi);
+            tc::tmem_st8(tm + kDtLo + 32 * hf + 8 * grp, lo);
+        }
+        tc::st_wait();
+
+        // ---- MMA-3: [Z | (P Delta)^T] = Delta^T [Ktilde | P^T] (N = 192), two issuers ----
+        sync_for_mma();
+        if (tid == kIss0 || tid == kIss1) {
+            const bool first = tid == kIss0;
+            mma_passes<true>(tmem_base + (first ? kM3a : kM3b), tmem_base + kDtHi, tmem_base + kDtLo, sbase + kBHi,
+                             sbase + kBLo, 0, kBRows * 128, kC / 8, tc::idesc_tf32(128, kBRows),
+                             first ? 0 : 2, first ? 2 : 3);
+            tc::mma_commit(&bars[3]);
+        }
+        __syncwarp();
+        ok = wait_mma(&bars[3], ph);
+        if (!ok) break;
+
+        // ---- 4. outputs and the new state ----
+#pragma unroll
+        for (int grp = 0; grp < 4; ++grp) {
+            float pa[8], pb[8];
+            tc::tmem_ld8(tm + kM3a + 128 + 32 * hf + 8 * grp, pa);
+            tc::tmem_ld8(tm + kM3b + 128 + 32 * hf + 8 * grp, pb);
+            tc::ld_wait();
+            const int t0 = 32 * hf + 8 * grp;
+            float *op = obase + (int64_t)(c0 + t0) * p.o_stride + r;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (t0 + e < n)
+                    __stcs(op + (int64_t)e * p.o_stride,
+                           fmaf(sc.gamma[t0 + e], yq[8 * grp + e], pa[e] + pb[e]) * p.inv_sqrt_d);
+        }
+        {
+            const float gC = sc.gamma[kC - 1];
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+                float za[32], zb[32];
+                tc::tmem_ld32(tm + kM3a + 64 * hf + 32 * cb, za);
+                tc::tmem_ld32(tm + kM3b + 64 * hf + 32 * cb, zb);
+                tc::ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) S[32 * cb + j] = fmaf(gC, S[32 * cb + j], za[j] + zb[j]);
+            }
+        }
+        ph ^= 1u;
+        tc::fence_before_sync();
+        __syncthreads();                                   // scalars and the operand buffer are reused
+        tc::fence_after_sync();
+    }
+    cp_async_wait<0>();                                    // no copy left in flight
+
+    if (!ok) {
+        if (tid == 0) atomicAdd(&g_tc_wait_timeouts, 1u);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) S[j] = __int_as_float(0x7fc00000);
+    }
+#pragma unroll
+    for (int j = 0; j < 64; ++j) srow[j] = from_f32<TS>(S[j]);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <typename TS>
+cudaError_t launch_typed(const PrefillParams &p, cudaStream_t s)
+{
+    constexpr auto kern = prefill_tc_d128<TS>;
+    const cudaError_t e = allow_dynamic_smem<kern>((int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)((int64_t)p.batch * p.nv), kThreads, kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillParams &p, bool f16_state, cudaStream_t s)
+{
+    return f16_state ? launch_typed<__half>(p, s) : launch_typed<float>(p, s);
+}
+
+cudaError_t tc_wait_timeouts(unsigned *count)
+{
+    const cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyFromSymbol(count, g_tc_wait_timeouts, sizeof(unsigned));
+}
+
+}  // namespace gdn

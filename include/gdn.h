@@ -79,7 +79,9 @@ extern "C" {
 #define GDN_ERR_ALIAS 4        /* an output overlaps another operand */
 #define GDN_ERR_CUDA 5         /* the CUDA launch failed (see gdn_last_cuda_error) */
 /* There is no timeout status: no kernel of the library waits on a flag, a
- * counter or another block (only on its own barriers and copy groups).  A
+ * counter or another block (only on its own barriers, copy groups and, in
+ * gdn_prefill_chunked, the completion of its own MMAs, a bounded wait counted
+ * by gdn_device_wait_timeouts).  A
  * base, stride or pitch that rules out the 16-byte vector kernels is not an
  * error either: the general kernel runs instead (GDN_ERR_ALIGN is only for a
  * pointer not aligned to its own element size). */
@@ -334,6 +336,44 @@ GDN_API int gdn_prefill_seq(void *state, gdn_state_dtype state_dtype, int64_t st
                             int batch, int seq_len, int nk, int nv, int d,
                             int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
                             int64_t o_stride, void *stream);
+
+/*
+ * gdn_prefill_chunked -- gdn_prefill_seq computed in chunks of 64 tokens with
+ * the chunk's matrix products on the tensor cores.
+ *   Defined by: the same recurrence as gdn_prefill_seq (gdn.rs `gdn_step`,
+ *   token by token as ssm_gdn_a.rs `gdn_prefill_regresident`), unrolled over
+ *   a chunk from the state at its start: with gamma_t the product of the
+ *   chunk's alphas up to t and rho(t,i) = gamma_t / gamma_i, the chunk's
+ *   deltas solve (I + A) Delta = R, A[t][i] = beta_t rho(t,i) k_t.k_i (i < t),
+ *   R[t] = beta_t (v_t - gamma_t S k_t); o_t = (gamma_t S q_t + sum_{i<=t}
+ *   rho(t,i) q_t.k_i delta_i) / sqrt(D); at the chunk's end S <- gamma_C S +
+ *   sum_t rho(C,t) delta_t k_t^T.  Equal to the token loop in exact
+ *   arithmetic; in floating point every product is taken from operands split
+ *   into two TF32 parts (three MMAs, about 22 significant bits), accumulated
+ *   in fp32, and the state itself is carried in fp32.
+ *   Taken for D == 128 with k and q rows 16-byte aligned (base and stride);
+ *   any other call runs gdn_prefill_seq's kernels.  Arguments, layouts,
+ *   results (up to fp32 rounding) and errors as gdn_prefill_seq.
+ *   The kernel's only waits are on the completion of its own MMAs, each
+ *   bounded; see gdn_device_wait_timeouts.
+ */
+GDN_API int gdn_prefill_chunked(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
+                                const float *q, const float *k, const float *v,
+                                const float *alpha, const float *beta, float *o,
+                                int batch, int seq_len, int nk, int nv, int d,
+                                int64_t qk_stride, int64_t v_stride, int64_t gb_stride,
+                                int64_t o_stride, void *stream);
+
+/*
+ * gdn_device_wait_timeouts -- how many times, on the current device since
+ * the library was loaded, a tensor-core kernel's bounded wait for its own
+ * MMAs ran out (the kernel then stops and writes NaN to its state; 0 in every
+ * healthy run).  Synchronises the current device first.  No counterpart on
+ * the source pages: a health check of this library's kernels.
+ *   count        host pointer, written.
+ *   Errors: GDN_ERR_ARG (count NULL), GDN_ERR_CUDA.
+ */
+GDN_API int gdn_device_wait_timeouts(unsigned *count);
 
 /*
  * gdn_h_f32_to_f16 -- n h-state elements binary32 -> binary16, round to

@@ -193,9 +193,10 @@ def check_decode(res, f16, norm):
 
 
 def run_prefill_case(B, NK, NV, D, T, *, seed=0, init="zero", pad=(0, 0, 0, 0), pitch_pad=0, misalign=0,
-                     splits=None, alpha=None, beta=None, f16=False):
+                     splits=None, alpha=None, beta=None, f16=False, chunked=False):
     """Prefill of T tokens on the GPU (one call, or per-sequence calls over `splits`)
-    and in the oracle; returns error metrics."""
+    and in the oracle; returns error metrics.  chunked: through gdn_prefill_chunked."""
+    prefill = gdn.gdn_prefill_chunked if chunked else gdn.gdn_prefill_seq
     sdt = np.float16 if f16 else np.float32
     if init == "zero":
         S0 = np.zeros((B, NV, D, D), sdt)
@@ -221,18 +222,18 @@ def run_prefill_case(B, NK, NV, D, T, *, seed=0, init="zero", pad=(0, 0, 0, 0), 
                   state_dtype=gdn.GDN_STATE_F16 if f16 else gdn.GDN_STATE_F32,
                   qk_stride=qb.stride, v_stride=vb.stride, gb_stride=ab.stride, o_stride=ob.stride)
     if splits is None:
-        gdn.gdn_prefill_seq(pool.ptr, qb.ptr, kb.ptr, vb.ptr, ab.ptr, bb.ptr, ob.ptr, batch=B, seq_len=T, **common)
+        prefill(pool.ptr, qb.ptr, kb.ptr, vb.ptr, ab.ptr, bb.ptr, ob.ptr, batch=B, seq_len=T, **common)
     else:
         e32, es = 4, (2 if f16 else 4)
         for b in range(B):
             t0 = 0
             for n in splits:
                 row = b * T + t0
-                gdn.gdn_prefill_seq(pool.ptr + b * pool.stride * es,
-                                    qb.ptr + row * qb.stride * e32, kb.ptr + row * kb.stride * e32,
-                                    vb.ptr + row * vb.stride * e32, ab.ptr + row * ab.stride * e32,
-                                    bb.ptr + row * bb.stride * e32, ob.ptr + row * ob.stride * e32,
-                                    batch=1, seq_len=n, **common)
+                prefill(pool.ptr + b * pool.stride * es,
+                        qb.ptr + row * qb.stride * e32, kb.ptr + row * kb.stride * e32,
+                        vb.ptr + row * vb.stride * e32, ab.ptr + row * ab.stride * e32,
+                        bb.ptr + row * bb.stride * e32, ob.ptr + row * ob.stride * e32,
+                        batch=1, seq_len=n, **common)
                 t0 += n
             assert t0 == T
     ref = S0.astype(np.float64)

@@ -42,7 +42,7 @@ def test_exports_match_header(built):
     want = declared_symbols()
     assert want == sorted(["gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm",
                            "gdn_decode_conv_norm_noalloc", "gdn_decode_norm_q8", "gdn_gate_norm",
-                           "gdn_gate_norm_q8", "gdn_prefill_seq",
+                           "gdn_gate_norm_q8", "gdn_prefill_seq", "gdn_prefill_chunked", "gdn_device_wait_timeouts",
                            "gdn_h_f32_to_f16",
                            "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error"])
     out = subprocess.run(["nm", "-D", "--defined-only", gdn.library_path()], capture_output=True, text=True,
@@ -179,10 +179,11 @@ def prefill(lib, **kw):
     a = dict(state=A, dt=0, pitch=3 * 128 * 128, q=A + (1 << 30), k=A + (2 << 30), v=A + (3 << 30),
              alpha=A + (4 << 30), beta=A + (5 << 30), o=A + (6 << 30), batch=2, T=5, nk=1, nv=3, d=128,
              qk=128, vs=3 * 128, gb=3, os=3 * 128)
+    chunked = kw.pop("chunked", False)
     a.update(kw)
-    return lib.gdn_prefill_seq(a["state"], a["dt"], a["pitch"], a["q"], a["k"], a["v"], a["alpha"], a["beta"],
-                               a["o"], a["batch"], a["T"], a["nk"], a["nv"], a["d"], a["qk"], a["vs"], a["gb"],
-                               a["os"], None)
+    fn = lib.gdn_prefill_chunked if chunked else lib.gdn_prefill_seq
+    return fn(a["state"], a["dt"], a["pitch"], a["q"], a["k"], a["v"], a["alpha"], a["beta"],
+              a["o"], a["batch"], a["T"], a["nk"], a["nv"], a["d"], a["qk"], a["vs"], a["gb"], a["os"], None)
 
 
 @pytest.mark.parametrize("kw,want", [
@@ -280,13 +281,23 @@ def test_gate_norm_empty_is_ok(lib):
     (dict(dt=2), UNSUP), (dict(T=-1), ARG), (dict(o=None), ARG), (dict(state=A + 1, dt=1), ALIGN),
     (dict(os=10), ARG), (dict(o=A + 100), ALIAS),
 ])
-def test_prefill_rejects(lib, kw, want):
-    assert prefill(lib, **kw) == want
+@pytest.mark.parametrize("chunked", [False, True])
+def test_prefill_rejects(lib, kw, want, chunked):
+    """gdn_prefill_chunked shares gdn_prefill_seq's checks."""
+    assert prefill(lib, chunked=chunked, **kw) == want
 
 
-def test_prefill_empty_is_ok(lib):
-    assert prefill(lib, T=0) == OK
-    assert prefill(lib, batch=0) == OK
+@pytest.mark.parametrize("chunked", [False, True])
+def test_prefill_empty_is_ok(lib, chunked):
+    assert prefill(lib, T=0, chunked=chunked) == OK
+    assert prefill(lib, batch=0, chunked=chunked) == OK
+
+
+def test_device_wait_timeouts_without_device(lib):
+    import ctypes
+    assert lib.gdn_device_wait_timeouts(None) == ARG
+    c = ctypes.c_uint(7)
+    assert lib.gdn_device_wait_timeouts(ctypes.byref(c)) == CUDA
 
 
 def test_converters_reject(lib):

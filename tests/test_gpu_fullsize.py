@@ -158,8 +158,10 @@ def test_fp16_pool_16_steps_and_converters():
     assert torch.isfinite(pool).all().item()
 
 
-def test_prefill_4096_tokens():
-    """Batch 8, T = 4096 tokens in one call, fp32 state from zero; sampled heads over every token."""
+@pytest.mark.parametrize("chunked", [False, True])
+def test_prefill_4096_tokens(chunked):
+    """Batch 8, T = 4096 tokens in one call, fp32 state from zero; sampled heads over every token.
+    chunked: gdn_prefill_chunked (64-token chunks on the tensor cores), else gdn_prefill_seq."""
     B, T = 8, 4096
     R = B * T
     dev = torch.device("cuda")
@@ -181,8 +183,10 @@ def test_prefill_4096_tokens():
         bt[rows] = torch.from_numpy(xs["beta"][i]).to(dev)
     o = torch.empty((R, NV * D), device=dev)
     S = torch.zeros((B, NV, D, D), device=dev)
-    gdn.gdn_prefill_seq(S, q, k, v, a, bt, o, batch=B, seq_len=T, nk=NK, nv=NV, d=D)
+    (gdn.gdn_prefill_chunked if chunked else gdn.gdn_prefill_seq)(S, q, k, v, a, bt, o, batch=B, seq_len=T,
+                                                                   nk=NK, nv=NV, d=D)
     torch.cuda.synchronize()
+    assert gdn.gdn_device_wait_timeouts() == 0
     assert torch.isfinite(o).all().item() and torch.isfinite(S).all().item()
     heads = [(0, 0), (0, 17), (0, 47), (1, 3), (1, 16), (1, 40)]
 

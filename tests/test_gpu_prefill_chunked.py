@@ -1,0 +1,93 @@
+"""GPU parity: gdn_prefill_chunked (the prefill regrouped into chunks of 64 tokens, products on the
+tensor cores with operands split into two TF32 parts) against the fp64 oracle's token-sequential
+prefill, at the fp32 bar (1e-4 of max |ref| for o and the final state).
+
+Token counts straddle the chunk (1, 63, 64, 65, 130, 200: one partial chunk, exact chunks, ragged
+tails); the decays cover the typical ~0.86, decays small enough that products over a chunk underflow
+fp32, and exact zeros; alpha = 1, beta = 0 must leave the state bit for bit unchanged (every delta is
+then exactly zero).  No call may end with a timed-out MMA wait."""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_16_gb300 as gdn
+from tests.gpu_helpers import TOL_F32, TOL_REL_L2, run_prefill_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _lib(cuda_lib):
+    yield cuda_lib
+    assert gdn.gdn_device_wait_timeouts() == 0
+
+
+def check(r):
+    assert r["intact"], "guard band or padding overwritten"
+    assert r["state_max_rel"] <= TOL_F32, r["state_max_rel"]
+    assert r["o_max_rel"] <= TOL_F32, r["o_max_rel"]
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130, 200])
+def test_chunk_boundaries(T):
+    """NV = 3 over NK = 2, random initial state."""
+    check(run_prefill_case(2, 2, 3, 128, T, seed=400 + T, init="normal", chunked=True))
+
+
+def test_from_zero_state_with_strides_and_pitch():
+    check(run_prefill_case(2, 2, 5, 128, 97, seed=410, pad=(4, 8, 1, 3), pitch_pad=4096, chunked=True))
+
+
+def test_long_sequence():
+    check(run_prefill_case(1, 2, 4, 128, 1000, seed=411, init="normal", chunked=True))
+
+
+def test_split_calls_equal_one_call():
+    """Consecutive calls per sequence (70 + 59 tokens, chunk boundaries inside both) match the
+    oracle's single pass."""
+    check(run_prefill_case(2, 2, 3, 128, 129, seed=412, init="normal", splits=(70, 59), chunked=True))
+
+
+def test_low_and_zero_decay():
+    """Decays in [1e-3, 0.3] (a chunk's product underflows fp32 many times over) with exact zeros."""
+    rng = np.random.default_rng(413)
+    B, NV, T = 2, 3, 200
+    a = rng.uniform(1e-3, 0.3, size=(B, T, NV)).astype(np.float32)
+    a[:, ::7, :] = 0.0
+    check(run_prefill_case(B, 2, NV, 128, T, seed=413, init="normal", alpha=a, chunked=True))
+
+
+def test_alpha_one_beta_zero_leaves_state_bitwise():
+    r = run_prefill_case(2, 2, 3, 128, 100, seed=414, init="normal", alpha=1.0, beta=0.0, chunked=True)
+    assert r["intact"]
+    assert np.array_equal(r["S_gpu"], r["S_ref"])
+    assert r["o_max_rel"] <= TOL_F32
+
+
+def test_many_heads():
+    """B * NV = 320 CTAs (more than one per SM in turn), NV = 80 over NK = 16."""
+    check(run_prefill_case(4, 16, 80, 128, 70, seed=415, init="normal", chunked=True))
+
+
+@pytest.mark.parametrize("T", [1, 64, 150])
+def test_f16_state(T):
+    """fp16 state: widened once, carried in fp32 across the call, rounded once on store."""
+    r = run_prefill_case(2, 2, 3, 128, T, seed=420 + T, init="normal", f16=True, pitch_pad=4096, chunked=True)
+    assert r["intact"]
+    assert r["state_rel_l2"] <= TOL_REL_L2, r["state_rel_l2"]
+    assert r["state_max_rel"] <= 2.0 ** -10, r["state_max_rel"]
+    assert r["o_max_rel"] <= TOL_F32, r["o_max_rel"]
+
+
+@pytest.mark.parametrize("D,misalign", [(64, 0), (128, 1)])
+def test_other_shapes_take_the_token_kernels(D, misalign):
+    check(run_prefill_case(2, 2, 3, D, 40, seed=430 + D, init="normal", misalign=misalign,
+                           pad=(1 if misalign else 0, 0, 0, 0), chunked=True))
+
+
+def test_matches_token_kernel_closely():
+    """Both kernels on the same inputs: far inside the bar of each other."""
+    a = run_prefill_case(2, 2, 3, 128, 150, seed=440, init="normal", chunked=True)
+    b = run_prefill_case(2, 2, 3, 128, 150, seed=440, init="normal", chunked=False)
+    scale = np.max(np.abs(a["S_ref"]))
+    assert np.max(np.abs(a["S_gpu"] - b["S_gpu"])) <= TOL_F32 * scale
