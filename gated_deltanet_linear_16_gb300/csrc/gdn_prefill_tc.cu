@@ -57,8 +57,8 @@ constexpr int kC = 64;                       // tokens per chunk
 constexpr int kThreads = 256;
 // MMA-issuing threads: lane 0 of warps 2, 3 and 6 (no part in building A or in the inversion).  One
 // thread issues about one MMA per ~140 cycles whatever its N, while the tensor core takes MMAs from
-// several threads at once, so each product is split over up to three issuers, each pass of the
-// precision split (hi*hi, hi*lo, lo*hi) into its own accumulator, summed by the SIMT phase after.
+// several threads at once, so each product is split over up to three issuers, each part (a range
+// of K, or a pass of the precision split) into its own accumulator, summed by the SIMT phase after.
 constexpr int kIss0 = 64, kIss1 = 96, kIss2 = 192;
 constexpr uint32_t kWaitLimit = 1u << 22;    // polls of an mbarrier phase before giving up
 
@@ -78,12 +78,12 @@ constexpr uint32_t kSmemBytes = kXsOff + 32 * kXS * 4 + 1024;          // + alig
 // tensor-memory columns
 constexpr uint32_t kSHi = 0, kSLo = 128;     // split state (A operand of Y)
 constexpr uint32_t kY = 256, kYQ = 320;      // Y = S [K;Q]^T: columns t of K, then of Q (all three passes)
-constexpr uint32_t kG = 384, kGb = 448;      // G = [K;Q] K^T: passes hh + hl, and pass lh
+constexpr uint32_t kG = 384, kGb = 448;      // G = [K;Q] K^T over the first and the second half of K
 constexpr uint32_t kRHi = 384, kRLo = 448;   // split R^T (after G is read)
 constexpr uint32_t kD1 = 128, kD2 = 0, kD3 = 64;   // Delta^T = R^T T^T, one accumulator per pass (after Y)
 constexpr uint32_t kDtHi = 192, kDtLo = 256; // split Delta^T
-// Delta^T [Ktilde | P^T] (N = 192): passes hh + hl at kM3a, pass lh at kM3b; Z in the first 128
-// columns of each, (P Delta)^T in the last 64
+// Delta^T [Ktilde | P^T] (N = 192) over the first and the second half of K (t) at kM3a and kM3b;
+// Z in the first 128 columns of each, (P Delta)^T in the last 64
 constexpr uint32_t kM3a = 0, kM3b = 320;
 
 struct __align__(16) ChunkScalars {
@@ -130,14 +130,14 @@ __device__ __forceinline__ void st_split4(uint32_t hi_addr, uint32_t lo_addr, fl
     st_shared_v4(lo_addr, l0, l1, l2, l3);
 }
 
-// Passes [p0, p1) of the split product over K/8 steps: pass 0 = A_hi B_hi, 1 = A_hi B_lo, 2 =
-// A_lo B_hi, all into D (the first MMA overwrites it).  A in shared memory (a_hi/a_lo descriptors'
-// base addresses) or tensor memory.  Issued by one thread.  The loops stay rolled: this kernel's
-// code is run once per chunk by few warps, so its size (instruction fetch) matters more than the
-// loop overhead.
+// Passes [p0, p1) of the split product over the K/8 steps [k0, k1): pass 0 = A_hi B_hi, 1 = A_hi
+// B_lo, 2 = A_lo B_hi, all into D (the first MMA overwrites it).  A in shared memory (a_hi/a_lo
+// descriptors' base addresses) or tensor memory.  Issued by one thread.  The loops stay rolled:
+// this kernel's code is run once per chunk by few warps, so its size (instruction fetch) matters
+// more than the loop overhead.
 template <bool A_TMEM>
 __device__ __forceinline__ void mma_passes(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
-                                           uint32_t a_block, uint32_t b_block, int ksteps, uint32_t idesc,
+                                           uint32_t a_block, uint32_t b_block, int k0, int k1, uint32_t idesc,
                                            int p0, int p1)
 {
 #pragma unroll 1
@@ -145,8 +145,8 @@ __device__ __forceinline__ void mma_passes(uint32_t d, uint32_t a_hi, uint32_t a
         const uint32_t a = pass == 2 ? a_lo : a_hi;
         const uint32_t b = pass == 1 ? b_lo : b_hi;
 #pragma unroll 1
-        for (int kk = 0; kk < ksteps; ++kk) {
-            const uint32_t acc = (pass > p0 || kk > 0) ? 1u : 0u;
+        for (int kk = k0; kk < k1; ++kk) {
+            const uint32_t acc = (pass > p0 || kk > k0) ? 1u : 0u;
             const uint64_t bd = tc::smem_desc_sw128(b + (kk >> 2) * b_block + (kk & 3) * 32);
             if constexpr (A_TMEM) {
                 tc::mma_ts(d, a + kk * 8, bd, idesc, acc);
@@ -210,87 +210,88 @@ __device__ __forceinline__ void sync_a_warps() { asm volatile("bar.sync 1, 128;"
 
 // T = (I + A)^-1 for the strictly lower triangular 64 x 64 A in W (row stride
 // kAS); T[t][j] (t >= j) is written to W[j][t], the upper triangle and the
-// diagonal, which A leaves free.  By the 128 threads of warps 0, 1, 4, 5 (it =
-// 0..127): the four 16 x 16 diagonal blocks by forward substitution (a thread
-// per column), then the blocks under the diagonal from [[M11, 0], [M21, M22]]^-1
-// = [[T11, 0], [-T22 M21 T11, T22]]: the two 16 x 16 ones, then the 32 x 32 one,
-// each product with several output columns per thread.  Xs: 32 x 33 scratch.
-__device__ __forceinline__ void invert_unit_lower(float *W, float *Xs, int it)
+// diagonal, which A leaves free.  First the four 16 x 16 diagonal blocks by
+// forward substitution (64 threads, one per column: invert_diag_blocks), then
+// the blocks under the diagonal from [[M11, 0], [M21, M22]]^-1 = [[T11, 0],
+// [-T22 M21 T11, T22]] (all 256 threads: invert_off_diag): the two 16 x 16
+// ones, then the 32 x 32 one.  Xs: 32 x 33 scratch.
+__device__ __forceinline__ float w_a(const float *W, int t, int i) { return W[t * kAS + i]; }
+__device__ __forceinline__ float &w_t(float *W, int t, int j) { return W[j * kAS + t]; }
+
+__device__ __forceinline__ void invert_diag_blocks(float *W, int it)
 {
-    auto A = [&](int t, int i) -> float { return W[t * kAS + i]; };
-    auto Tr = [&](int t, int j) -> float & { return W[j * kAS + t]; };
-    if (it < kC) {
-        const int kb = it >> 4, jj = it & 15, base = 16 * kb;
-        float x[16];
+    const int kb = it >> 4, jj = it & 15, base = 16 * kb;
+    float x[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = i == jj ? 1.0f : 0.0f;
+    for (int i = 0; i < 16; ++i) x[i] = i == jj ? 1.0f : 0.0f;
 #pragma unroll
-        for (int t = 1; t < 16; ++t) {
-            float a0 = 0.f, a1 = 0.f;
+    for (int t = 1; t < 16; ++t) {
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int i = 0; i + 1 < t; i += 2) {
-                a0 = fmaf(A(base + t, base + i), x[i], a0);
-                a1 = fmaf(A(base + t, base + i + 1), x[i + 1], a1);
-            }
-            if (t & 1) a0 = fmaf(A(base + t, base + t - 1), x[t - 1], a0);
-            if (t > jj) x[t] = -(a0 + a1);
+        for (int i = 0; i + 1 < t; i += 2) {
+            a0 = fmaf(w_a(W, base + t, base + i), x[i], a0);
+            a1 = fmaf(w_a(W, base + t, base + i + 1), x[i + 1], a1);
         }
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-            if (t >= jj) Tr(base + t, base + jj) = x[t];
+        if (t & 1) a0 = fmaf(w_a(W, base + t, base + t - 1), x[t - 1], a0);
+        if (t > jj) x[t] = -(a0 + a1);
     }
-    sync_a_warps();
-    {   // X = M21 T11 for the pairs (rows 16..31, cols 0..15) and (rows 48..63, cols 32..47): row t, cols 4 jq..+3
-        const int b = it >> 6, t = (it >> 2) & 15, j0 = 4 * (it & 3), base = 32 * b;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int t = 0; t < 16; ++t)
+        if (t >= jj) w_t(W, base + t, base + jj) = x[t];
+}
+
+__device__ __forceinline__ void invert_off_diag(float *W, float *Xs, int tid)
+{
+    {   // X = M21 T11 for the pairs (rows 16..31, cols 0..15) and (rows 48..63, cols 32..47): row t, cols j0, j0+1
+        const int b = tid >> 7, t = (tid >> 3) & 15, j0 = 2 * (tid & 7), base = 32 * b;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const float a = A(base + 16 + t, base + i);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc[e] = fmaf(a, i >= j0 + e ? Tr(base + i, base + j0 + e) : 0.0f, acc[e]);
+            const float a = w_a(W, base + 16 + t, base + i);
+            a0 = fmaf(a, i >= j0 ? w_t(W, base + i, base + j0) : 0.0f, a0);
+            a1 = fmaf(a, i >= j0 + 1 ? w_t(W, base + i, base + j0 + 1) : 0.0f, a1);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) Xs[(16 * b + t) * kXS + j0 + e] = acc[e];
+        Xs[(16 * b + t) * kXS + j0] = a0;
+        Xs[(16 * b + t) * kXS + j0 + 1] = a1;
     }
-    sync_a_warps();
+    __syncthreads();
     {   // T21 = -T22 X for the two pairs
-        const int b = it >> 6, t = (it >> 2) & 15, j0 = 4 * (it & 3), base = 32 * b;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int b = tid >> 7, t = (tid >> 3) & 15, j0 = 2 * (tid & 7), base = 32 * b;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const float tv = i <= t ? Tr(base + 16 + t, base + 16 + i) : 0.0f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = fmaf(tv, Xs[(16 * b + i) * kXS + j0 + e], acc[e]);
+            const float tv = i <= t ? w_t(W, base + 16 + t, base + 16 + i) : 0.0f;
+            a0 = fmaf(tv, Xs[(16 * b + i) * kXS + j0], a0);
+            a1 = fmaf(tv, Xs[(16 * b + i) * kXS + j0 + 1], a1);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) Tr(base + 16 + t, base + j0 + e) = -acc[e];
+        w_t(W, base + 16 + t, base + j0) = -a0;
+        w_t(W, base + 16 + t, base + j0 + 1) = -a1;
     }
-    sync_a_warps();
-    {   // X = M21 T11 for the 32 x 32 halves: row t, cols 8 jq .. +7
-        const int t = it >> 2, j0 = 8 * (it & 3);
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    __syncthreads();
+    {   // X = M21 T11 for the 32 x 32 halves: row t, cols 4 jq .. +3
+        const int t = tid >> 3, j0 = 4 * (tid & 7);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
         for (int i = 0; i < 32; ++i) {
-            const float a = A(32 + t, i);
+            const float a = w_a(W, 32 + t, i);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(a, i >= j0 + e ? Tr(i, j0 + e) : 0.0f, acc[e]);
+            for (int e = 0; e < 4; ++e) acc[e] = fmaf(a, i >= j0 + e ? w_t(W, i, j0 + e) : 0.0f, acc[e]);
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) Xs[t * kXS + j0 + e] = acc[e];
+        for (int e = 0; e < 4; ++e) Xs[t * kXS + j0 + e] = acc[e];
     }
-    sync_a_warps();
+    __syncthreads();
     {   // T21 = -T22 X
-        const int t = it >> 2, j0 = 8 * (it & 3);
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const int t = tid >> 3, j0 = 4 * (tid & 7);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
         for (int i = 0; i < 32; ++i) {
-            const float tv = i <= t ? Tr(32 + t, 32 + i) : 0.0f;
+            const float tv = i <= t ? w_t(W, 32 + t, 32 + i) : 0.0f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(tv, Xs[i * kXS + j0 + e], acc[e]);
+            for (int e = 0; e < 4; ++e) acc[e] = fmaf(tv, Xs[i * kXS + j0 + e], acc[e]);
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) Tr(32 + t, j0 + e) = -acc[e];
+        for (int e = 0; e < 4; ++e) w_t(W, 32 + t, j0 + e) = -acc[e];
     }
 }
 
@@ -357,7 +358,6 @@ prefill_tc_d128(const PrefillParams p)
             tc::tmem_st32(tm + kSHi + 64 * hf + 32 * cb, hi);
             tc::tmem_st32(tm + kSLo + 64 * hf + 32 * cb, lo);
         }
-        tc::st_wait();
         // ---- 1. this thread's staged [K;Q] chunks, split into the operand buffer ----
         cp_async_wait<0>();
 #pragma unroll 2
@@ -368,6 +368,7 @@ prefill_tc_d128(const PrefillParams p)
             st_split4(sbase + kKQHi + off, sbase + kKQLo + off, __uint_as_float(x.x), __uint_as_float(x.y),
                       __uint_as_float(x.z), __uint_as_float(x.w));
         }
+        tc::st_wait();                                     // the split state is in tensor memory
         __syncthreads();                                   // alpha, beta landed (their copiers waited)
         if (warp < 3) {   // products of the decays: gamma (prefix), rho(C-1, .) (suffix), sigma (prefix from 32)
             if (warp == 2) {
@@ -408,15 +409,15 @@ prefill_tc_d128(const PrefillParams p)
 
         // ---- MMA-1: G = [K;Q] K^T (two issuers, bars[0]) and Y = S [K;Q]^T (one issuer, bars[1]) ----
         sync_for_mma();
-        if (tid == kIss0 || tid == kIss2) {
+        if (tid == kIss0 || tid == kIss2) {       // G over the first / second half of K
             const bool first = tid == kIss0;
             mma_passes<false>(tmem_base + (first ? kG : kGb), sbase + kKQHi, sbase + kKQLo, sbase + kKQHi,
-                              sbase + kKQLo, 128 * 128, 128 * 128, kD / 8, tc::idesc_tf32(128, 64),
-                              first ? 0 : 2, first ? 2 : 3);
+                              sbase + kKQLo, 128 * 128, 128 * 128, first ? 0 : kD / 16, first ? kD / 16 : kD / 8,
+                              tc::idesc_tf32(128, 64), 0, 3);
             tc::mma_commit(&bars[0]);
         } else if (tid == kIss1) {
             mma_passes<true>(tmem_base + kY, tmem_base + kSHi, tmem_base + kSLo, sbase + kKQHi, sbase + kKQLo,
-                             0, 128 * 128, kD / 8, tc::idesc_tf32(128, 128), 0, 3);
+                             0, 128 * 128, 0, kD / 8, tc::idesc_tf32(128, 128), 0, 3);
             tc::mma_commit(&bars[1]);
         }
         __syncwarp();
@@ -431,8 +432,8 @@ prefill_tc_d128(const PrefillParams p)
             const int t = 32 * hf + j;
             vv[j] = t < n ? __ldg(vbase + (int64_t)(c0 + t) * p.v_stride + r) : 0.0f;
         }
-        // ---- 2. A from G and T = (I + A)^-1, by warps 0, 1, 4, 5 (lanes 0-63) while Y is still on the
-        //         tensor core; the issuer's warp 2 and the others wait for Y ----
+        // ---- 2. A from G by warps 0, 1, 4, 5 (lanes 0-63), the diagonal blocks of T = (I + A)^-1 by
+        //         warps 0 and 1, the rest of T by all warps, while Y is still on the tensor core ----
         bool ok_g = true;
         if (r < kC) {
             ok_g = tc::mbar_wait(&bars[0], ph, kWaitLimit);
@@ -455,9 +456,11 @@ prefill_tc_d128(const PrefillParams p)
                 }
             }
             sync_a_warps();                                // A complete
-            invert_unit_lower(W, Xs, (warp & 1) * 32 + lane + 64 * hf);
+            if (hf == 0) invert_diag_blocks(W, (warp & 1) * 32 + lane);
             tc::fence_before_sync();
         }
+        __syncthreads();                                   // diagonal blocks of T done; issuers done issuing
+        invert_off_diag(W, Xs, tid);
         ok = __syncthreads_and(ok_g && tc::mbar_wait(&bars[1], ph, kWaitLimit)) != 0;    // T complete, Y done
         tc::fence_after_sync();
         if (!ok) break;
@@ -538,7 +541,7 @@ prefill_tc_d128(const PrefillParams p)
         if (tid == kIss0 || tid == kIss1 || tid == kIss2) {
             const int pass = tid == kIss0 ? 0 : (tid == kIss1 ? 1 : 2);
             mma_passes<true>(tmem_base + (pass == 0 ? kD1 : (pass == 1 ? kD2 : kD3)), tmem_base + kRHi,
-                             tmem_base + kRLo, sbase + kTHi, sbase + kTLo, 0, kC * 128, kC / 8,
+                             tmem_base + kRLo, sbase + kTHi, sbase + kTLo, 0, kC * 128, 0, kC / 8,
                              tc::idesc_tf32(128, 64), pass, pass + 1);
             tc::mma_commit(&bars[2]);
         }
@@ -566,11 +569,11 @@ prefill_tc_d128(const PrefillParams p)
 
         // ---- MMA-3: [Z | (P Delta)^T] = Delta^T [Ktilde | P^T] (N = 192), two issuers ----
         sync_for_mma();
-        if (tid == kIss0 || tid == kIss1) {
+        if (tid == kIss0 || tid == kIss1) {       // over the first / second half of K (t)
             const bool first = tid == kIss0;
             mma_passes<true>(tmem_base + (first ? kM3a : kM3b), tmem_base + kDtHi, tmem_base + kDtLo, sbase + kBHi,
-                             sbase + kBLo, 0, kBRows * 128, kC / 8, tc::idesc_tf32(128, kBRows),
-                             first ? 0 : 2, first ? 2 : 3);
+                             sbase + kBLo, 0, kBRows * 128, first ? 0 : kC / 16, first ? kC / 16 : kC / 8,
+                             tc::idesc_tf32(128, kBRows), 0, 3);
             tc::mma_commit(&bars[3]);
         }
         __syncwarp();
