@@ -382,6 +382,9 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+E2E_GROUP = 8
+
+
 def run_e2e(args, torch, gdn, state, x, outb, dev, stream, graph=True):
     """Same workload through the public API with per-step host<->device copies: every layer's
     token inputs from pinned host memory to the device, the layer calls, every layer's bf16 output
@@ -399,11 +402,16 @@ def run_e2e(args, torch, gdn, state, x, outb, dev, stream, graph=True):
 
     L = outb.shape[0]
     copy = torch.cuda.Stream(device=dev)
+    # The outputs go back per group of E2E_GROUP layers (and after each of the last two layers): an
+    # event recorded between two consecutive kernels of the graph costs their programmatic
+    # (early-launch) overlap, and recording after every layer measured 0.4 % slower per step.
+    # The inputs' per-layer waits cost nothing measurable.
+    record_after = {l for l in range(L) if l % E2E_GROUP == E2E_GROUP - 1 or l >= L - 2}
 
     def launches():
         cur = torch.cuda.current_stream()
         copy.wait_stream(cur)                     # fork the copy stream off the step
-        ready, done = [], []
+        ready = []
         with torch.cuda.stream(copy):
             for l in range(L):
                 for k, v in host.items():
@@ -411,16 +419,23 @@ def run_e2e(args, torch, gdn, state, x, outb, dev, stream, graph=True):
                 ev = torch.cuda.Event()
                 ev.record(copy)
                 ready.append(ev)
+        done = {}
         for l in range(L):
             cur.wait_event(ready[l])
             layer_launch(gdn, state, dev_in, outb, l, None)
-            ev = torch.cuda.Event()
-            ev.record(cur)
-            done.append(ev)
+            if l in record_after:
+                ev = torch.cuda.Event()
+                ev.record(cur)
+                done[l] = ev
         with torch.cuda.stream(copy):
+            pending = []
             for l in range(L):
-                copy.wait_event(done[l])
-                host_out[l].copy_(outb[l], non_blocking=True)
+                pending.append(l)
+                if l in done:
+                    copy.wait_event(done[l])
+                    for m in pending:
+                        host_out[m].copy_(outb[m], non_blocking=True)
+                    pending = []
         cur.wait_stream(copy)                     # join: the step ends when the last output landed
 
     step, used = graphed(torch, launches, torch.cuda.Stream(device=dev), enable=graph)
@@ -436,8 +451,9 @@ def run_e2e(args, torch, gdn, state, x, outb, dev, stream, graph=True):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     return {"value": B * NV * outb.shape[0] / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
-            "submission": ("one CUDA graph replay per step; per-layer copies on a second stream overlap the "
-                           "layers' kernels") if used else "eager, per-layer copies on a second stream",
+            "submission": (f"one CUDA graph replay per step; per-layer input copies on a second stream overlap "
+                           f"the layers' kernels, outputs copied back per group of {E2E_GROUP} layers")
+                          if used else "eager, per-layer copies on a second stream",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
