@@ -23,7 +23,7 @@ __all__ = [
     "GdnError", "load", "build", "library_path",
     "GDN_STATE_F32", "GDN_STATE_F16", "STATUS",
     "gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
-    "gdn_prefill_chunked", "gdn_device_wait_timeouts",
+    "gdn_prefill_chunked", "gdn_device_wait_timeouts", "gdn_set_wait_polls", "GDN_DEFAULT_WAIT_POLLS",
     "gdn_decode_conv_norm_noalloc", "GDN_NOALLOC_MAX_KEY_HEADS", "gdn_decode_norm_q8",
     "gdn_gate_norm", "gdn_gate_norm_q8",
     "gdn_h_f32_to_f16", "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error",
@@ -32,6 +32,7 @@ __all__ = [
 GDN_STATE_F32 = 0
 GDN_STATE_F16 = 1
 GDN_NOALLOC_MAX_KEY_HEADS = 16384     # batch * NK limit of gdn_decode_conv_norm_noalloc
+GDN_DEFAULT_WAIT_POLLS = 4194304      # default bound of the tensor-core kernels' MMA-completion waits
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIGN",
           4: "GDN_ERR_ALIAS", 5: "GDN_ERR_CUDA"}
 
@@ -76,6 +77,8 @@ def _declare(lib):
                                     i64, i64, i64, i64, P]
     lib.gdn_prefill_chunked.argtypes = lib.gdn_prefill_seq.argtypes
     lib.gdn_device_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    lib.gdn_set_wait_polls.argtypes = [ctypes.c_uint]
+    lib.gdn_set_wait_polls.restype = None
     lib.gdn_h_f32_to_f16.argtypes = [P, P, u64, P]
     lib.gdn_h_f16_to_f32.argtypes = [P, P, u64, P]
     for fn in ("gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
@@ -320,6 +323,11 @@ def gdn_prefill_seq(state, q, k, v, alpha, beta, o, **kw):
 def gdn_prefill_chunked(state, q, k, v, alpha, beta, o, **kw):
     """gdn_prefill_seq regrouped into chunks of 64 tokens on the tensor cores (D = 128); same arguments."""
     _prefill("gdn_prefill_chunked", state, q, k, v, alpha, beta, o, **kw)
+
+
+def gdn_set_wait_polls(polls: int) -> None:
+    """Polls of an MMA completion before a tensor-core kernel gives up (0: at once, to test that path)."""
+    load().gdn_set_wait_polls(polls)
 
 
 def gdn_device_wait_timeouts() -> int:

@@ -42,8 +42,11 @@
 // current chunk.  The CTA holds all 512 tensor-memory columns and ~210 KB of
 // shared memory, so an SM runs one such CTA at a time.  The only waits are on the CTA's own MMA
 // completions (an mbarrier armed by tcgen05.commit), each bounded: if a bound
-// ran out, the CTA stops, counts the event in g_tc_wait_timeouts and writes
-// NaN to its outputs.
+// ran out (or the bound was set to 0 to test this path), the CTA stops, lets
+// the MMAs it issued finish (again bounded), counts the event in
+// g_tc_wait_timeouts and writes NaN to its state.
+#include <atomic>
+
 #include "gdn_internal.cuh"
 #include "gdn_tc.cuh"
 
@@ -167,11 +170,20 @@ __device__ __forceinline__ void sync_for_mma()
     tc::fence_after_sync();
 }
 // Every thread waits for the mbarrier phase; the CTA agrees on the outcome.
-__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t parity)
+__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t parity, uint32_t polls)
 {
-    const bool ok = __syncthreads_and(tc::mbar_wait(bar, parity, kWaitLimit)) != 0;
+    const bool ok = __syncthreads_and(tc::mbar_wait(bar, parity, polls)) != 0;
     tc::fence_after_sync();
     return ok;
+}
+// AND of `pred` over the 128 threads of warps 0, 1, 4, 5 (named barrier 1).
+__device__ __forceinline__ bool and_a_warps(bool pred)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)pred) : "memory");
+    return r != 0;
 }
 
 // Copy chunk [c0, c0 + n) of k, q (raw rows into the staging buffer, row-major)
@@ -297,7 +309,7 @@ __device__ __forceinline__ void invert_off_diag(float *W, float *Xs, int tid)
 
 template <typename TS>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_d128(const PrefillParams p)
+prefill_tc_d128(const PrefillParams p, const uint32_t polls)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -345,6 +357,7 @@ prefill_tc_d128(const PrefillParams p)
 #pragma unroll
     for (int j = 0; j < 64; ++j) S[j] = to_f32<TS>(srow[j]);
     bool ok = true;
+    uint32_t pend = 0;                              // barriers with a committed phase not yet seen complete
 
     for (int c0 = 0, par = 0; c0 < T && ok; c0 += kC, par ^= 1) {
         const int n = min(kC, T - c0);
@@ -421,6 +434,7 @@ prefill_tc_d128(const PrefillParams p)
             tc::mma_commit(&bars[1]);
         }
         __syncwarp();
+        pend = 0x3u;
         // the next chunk's inputs on their way while this one is computed
         if (c0 + kC < T)
             prefetch_chunk(sbase + kStage, ab[par ^ 1], kbase, qbase, p, seq, h, c0 + kC, min(kC, T - c0 - kC),
@@ -436,14 +450,15 @@ prefill_tc_d128(const PrefillParams p)
         //         warps 0 and 1, the rest of T by all warps, while Y is still on the tensor core ----
         bool ok_g = true;
         if (r < kC) {
-            ok_g = tc::mbar_wait(&bars[0], ph, kWaitLimit);
+            ok_g = and_a_warps(tc::mbar_wait(&bars[0], ph, polls));
             tc::fence_after_sync();
-            // A[t][i] = beta_t rho(t,i) k_t.k_i, t = r, i = 32 hf + 8 grp + e, walked downwards
+            // A[t][i] = beta_t rho(t,i) k_t.k_i, t = r, i = 32 hf + 8 grp + e, walked downwards (G is
+            // read only once it is known complete: after a timeout, A stays as it was)
             const int t = r;
             float pr = (hf == 0 && t >= 32) ? sc.sigma[t] : 1.0f;
             const float bt = beta[t];
 #pragma unroll 1
-            for (int grp = 3; grp >= 0; --grp) {
+            for (int grp = ok_g ? 3 : -1; grp >= 0; --grp) {
                 float gv[8], gw[8];
                 tc::tmem_ld8(tm + kG + 32 * hf + 8 * grp, gv);
                 tc::tmem_ld8(tm + kGb + 32 * hf + 8 * grp, gw);
@@ -461,9 +476,10 @@ prefill_tc_d128(const PrefillParams p)
         }
         __syncthreads();                                   // diagonal blocks of T done; issuers done issuing
         invert_off_diag(W, Xs, tid);
-        ok = __syncthreads_and(ok_g && tc::mbar_wait(&bars[1], ph, kWaitLimit)) != 0;    // T complete, Y done
+        ok = __syncthreads_and(ok_g && tc::mbar_wait(&bars[1], ph, polls)) != 0;         // T complete, Y done
         tc::fence_after_sync();
         if (!ok) break;
+        pend = 0;
         // k_t[c] = hi + lo (exact) from the operand buffer before T overwrites it; t = 32 hf + j, c = r
         float kv[32];
 #pragma unroll
@@ -546,8 +562,10 @@ prefill_tc_d128(const PrefillParams p)
             tc::mma_commit(&bars[2]);
         }
         __syncwarp();
-        ok = wait_mma(&bars[2], ph);
+        pend = 0x4u;
+        ok = wait_mma(&bars[2], ph, polls);
         if (!ok) break;
+        pend = 0;
 
         // ---- 3. Delta^T = sum of the three passes, split; Y_Q kept for the outputs ----
         float yq[32];
@@ -577,8 +595,10 @@ prefill_tc_d128(const PrefillParams p)
             tc::mma_commit(&bars[3]);
         }
         __syncwarp();
-        ok = wait_mma(&bars[3], ph);
+        pend = 0x8u;
+        ok = wait_mma(&bars[3], ph, polls);
         if (!ok) break;
+        pend = 0;
 
         // ---- 4. outputs and the new state ----
 #pragma unroll
@@ -615,6 +635,11 @@ prefill_tc_d128(const PrefillParams p)
     cp_async_wait<0>();                                    // no copy left in flight
 
     if (!ok) {
+        // a wait gave up: let the MMAs still in flight finish (again bounded) before the tensor memory
+        // they write is freed; count the event; the state of this head becomes NaN
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i)
+            if (pend & (1u << i)) tc::mbar_wait(&bars[i], ph, kWaitLimit);
         if (tid == 0) atomicAdd(&g_tc_wait_timeouts, 1u);
 #pragma unroll
         for (int j = 0; j < 64; ++j) S[j] = __int_as_float(0x7fc00000);
@@ -629,13 +654,15 @@ prefill_tc_d128(const PrefillParams p)
     }
 }
 
+std::atomic<uint32_t> g_wait_polls{kWaitLimit};
+
 template <typename TS>
 cudaError_t launch_typed(const PrefillParams &p, cudaStream_t s)
 {
     constexpr auto kern = prefill_tc_d128<TS>;
     const cudaError_t e = allow_dynamic_smem<kern>((int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)((int64_t)p.batch * p.nv), kThreads, kSmemBytes, s>>>(p);
+    kern<<<(unsigned)((int64_t)p.batch * p.nv), kThreads, kSmemBytes, s>>>(p, g_wait_polls.load());
     return cudaGetLastError();
 }
 
@@ -645,6 +672,8 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, bool f16_state, cudaStream
 {
     return f16_state ? launch_typed<__half>(p, s) : launch_typed<float>(p, s);
 }
+
+void tc_set_wait_polls(uint32_t polls) { g_wait_polls.store(polls); }
 
 cudaError_t tc_wait_timeouts(unsigned *count)
 {

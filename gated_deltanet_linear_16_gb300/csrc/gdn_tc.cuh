@@ -191,5 +191,7 @@ struct PrefillParams;
 cudaError_t launch_prefill_tc(const PrefillParams &p, bool f16_state, cudaStream_t s);
 // Count of bounded MMA-completion waits that ran out on the current device.
 cudaError_t tc_wait_timeouts(unsigned *count);
+// Polls of an MMA completion before a tensor-core kernel launched after this call gives up.
+void tc_set_wait_polls(uint32_t polls);
 
 }  // namespace gdn

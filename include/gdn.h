@@ -376,6 +376,20 @@ GDN_API int gdn_prefill_chunked(void *state, gdn_state_dtype state_dtype, int64_
 GDN_API int gdn_device_wait_timeouts(unsigned *count);
 
 /*
+ * gdn_set_wait_polls -- how many times a tensor-core kernel launched after
+ * this call polls for the completion of its own MMAs before it gives up
+ * (default GDN_DEFAULT_WAIT_POLLS, a second or more).  0 makes every such
+ * wait give up at once: the kernel then lets the MMAs it issued finish
+ * (bounded by the default), writes NaN to its state, counts the event for
+ * gdn_device_wait_timeouts and returns, so the timeout path can be tested
+ * without any fault and the context stays usable.  Process-wide; calls that
+ * are already launched keep their value.  No counterpart on the source
+ * pages.
+ */
+#define GDN_DEFAULT_WAIT_POLLS 4194304u
+GDN_API void gdn_set_wait_polls(unsigned polls);
+
+/*
  * gdn_h_f32_to_f16 -- n h-state elements binary32 -> binary16, round to
  * nearest, ties to even (overflow to +-inf, subnormals kept, NaN stays NaN).
  *   Defined by: ssm_gdn_a.rs, launcher `ssm_h_state_f32_to_f16`.

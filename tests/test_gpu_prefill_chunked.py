@@ -17,9 +17,11 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(autouse=True)
-def _lib(cuda_lib):
+def _lib(request, cuda_lib):
+    before = gdn.gdn_device_wait_timeouts()
     yield cuda_lib
-    assert gdn.gdn_device_wait_timeouts() == 0
+    if "timeout_path" not in request.node.name:
+        assert gdn.gdn_device_wait_timeouts() == before, "a bounded MMA wait ran out"
 
 
 def check(r):
@@ -91,3 +93,30 @@ def test_matches_token_kernel_closely():
     b = run_prefill_case(2, 2, 3, 128, 150, seed=440, init="normal", chunked=False)
     scale = np.max(np.abs(a["S_ref"]))
     assert np.max(np.abs(a["S_gpu"] - b["S_gpu"])) <= TOL_F32 * scale
+
+
+def test_wait_timeout_path_reports_and_leaves_the_context_usable():
+    """With the poll bound at 0 every CTA's first MMA wait gives up at once: the kernel drains its
+    MMAs, writes NaN to its state and counts one event per CTA; nothing faults, and with the default
+    bound restored the next call is correct again."""
+    B, NK, NV, D, T = 1, 2, 3, 128, 70
+    before = gdn.gdn_device_wait_timeouts()
+    dev = torch.device("cuda")
+    S = torch.zeros((B, NV, D, D), device=dev)
+    q = torch.nn.functional.normalize(torch.randn((B * T, NK, D), device=dev), dim=-1).reshape(B * T, NK * D)
+    k = torch.nn.functional.normalize(torch.randn((B * T, NK, D), device=dev), dim=-1).reshape(B * T, NK * D)
+    v = torch.randn((B * T, NV * D), device=dev)
+    a = torch.full((B * T, NV), 0.9, device=dev)
+    b = torch.full((B * T, NV), 0.5, device=dev)
+    o = torch.zeros((B * T, NV * D), device=dev)
+    try:
+        gdn.gdn_set_wait_polls(0)
+        gdn.gdn_prefill_chunked(S, q, k, v, a, b, o, batch=B, seq_len=T, nk=NK, nv=NV, d=D)
+        torch.cuda.synchronize()
+    finally:
+        gdn.gdn_set_wait_polls(gdn.GDN_DEFAULT_WAIT_POLLS)
+    assert gdn.gdn_device_wait_timeouts() == before + B * NV
+    assert torch.isnan(S).all().item()
+    r = run_prefill_case(2, 2, 3, 128, 65, seed=450, init="normal", chunked=True)
+    check(r)
+    assert gdn.gdn_device_wait_timeouts() == before + B * NV
