@@ -462,12 +462,15 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls)
                 float gv[8], gw[8];
                 tc::tmem_ld8(tm + kG + 32 * hf + 8 * grp, gv);
                 tc::tmem_ld8(tm + kGb + 32 * hf + 8 * grp, gw);
+                const float4 a_lo = *reinterpret_cast<const float4 *>(alpha + 32 * hf + 8 * grp);
+                const float4 a_hi = *reinterpret_cast<const float4 *>(alpha + 32 * hf + 8 * grp + 4);
+                const float al[8] = {a_lo.x, a_lo.y, a_lo.z, a_lo.w, a_hi.x, a_hi.y, a_hi.z, a_hi.w};
                 tc::ld_wait();
 #pragma unroll
                 for (int e = 7; e >= 0; --e) {
                     const int i = 32 * hf + 8 * grp + e;
                     if (i < t) W[t * kAS + i] = bt * pr * (gv[e] + gw[e]);
-                    if (i <= t) pr *= alpha[i];
+                    if (i <= t) pr *= al[e];
                 }
             }
             sync_a_warps();                                // A complete
@@ -482,10 +485,15 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls)
         pend = 0;
         // k_t[c] = hi + lo (exact) from the operand buffer before T overwrites it; t = 32 hf + j, c = r
         float kv[32];
+        {   // element (row 32 hf + j, column r) of the 128-row K-major tile: a row step is 128 bytes and
+            // the 16-byte chunk is XOR-ed with the row's low three bits
+            const uint32_t base = sbase + kKQHi + (r >> 5) * 128 * 128 + 32 * hf * 128 + ((r & 3) << 2);
+            const uint32_t chunk = (r & 31) >> 2;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const uint32_t off = tc::sw128_offset(32 * hf + j, r, 128);
-            kv[j] = ld_shared_f32(sbase + kKQHi + off) + ld_shared_f32(sbase + kKQLo + off);
+            for (int j = 0; j < 32; ++j) {
+                const uint32_t a = base + j * 128 + ((chunk ^ (uint32_t)(j & 7)) << 4);
+                kv[j] = ld_shared_f32(a) + ld_shared_f32(a + (kKQLo - kKQHi));
+            }
         }
         __syncthreads();
 
@@ -509,12 +517,15 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls)
                 float gv[8], gw[8];
                 tc::tmem_ld8(tm + kG + 32 * hf + 8 * grp, gv);
                 tc::tmem_ld8(tm + kGb + 32 * hf + 8 * grp, gw);
+                const float4 a_lo = *reinterpret_cast<const float4 *>(alpha + 32 * hf + 8 * grp);
+                const float4 a_hi = *reinterpret_cast<const float4 *>(alpha + 32 * hf + 8 * grp + 4);
+                const float al[8] = {a_lo.x, a_lo.y, a_lo.z, a_lo.w, a_hi.x, a_hi.y, a_hi.z, a_hi.w};
                 tc::ld_wait();
 #pragma unroll
                 for (int e = 7; e >= 0; --e) {
                     const int i = 32 * hf + 8 * grp + e;
                     gv[e] = i <= t ? pr * (gv[e] + gw[e]) : 0.0f;
-                    if (i <= t) pr *= alpha[i];
+                    if (i <= t) pr *= al[e];
                 }
                 const uint32_t off = tc::sw128_offset(128 + t, 32 * hf + 8 * grp, kBRows);
                 st_split4(sbase + kBHi + off, sbase + kBLo + off, gv[0], gv[1], gv[2], gv[3]);
@@ -609,11 +620,13 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls)
             tc::ld_wait();
             const int t0 = 32 * hf + 8 * grp;
             float *op = obase + (int64_t)(c0 + t0) * p.o_stride + r;
+            const float4 g_lo = *reinterpret_cast<const float4 *>(sc.gamma + t0);
+            const float4 g_hi = *reinterpret_cast<const float4 *>(sc.gamma + t0 + 4);
+            const float gm[8] = {g_lo.x, g_lo.y, g_lo.z, g_lo.w, g_hi.x, g_hi.y, g_hi.z, g_hi.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 if (t0 + e < n)
-                    __stcs(op + (int64_t)e * p.o_stride,
-                           fmaf(sc.gamma[t0 + e], yq[8 * grp + e], pa[e] + pb[e]) * p.inv_sqrt_d);
+                    __stcs(op + (int64_t)e * p.o_stride, fmaf(gm[e], yq[8 * grp + e], pa[e] + pb[e]) * p.inv_sqrt_d);
         }
         {
             const float gC = sc.gamma[kC - 1];
