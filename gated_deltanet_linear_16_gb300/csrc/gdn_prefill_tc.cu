@@ -225,8 +225,9 @@ __device__ __forceinline__ void sync_a_warps() { asm volatile("bar.sync 1, 128;"
 // diagonal, which A leaves free.  First the four 16 x 16 diagonal blocks by
 // forward substitution (64 threads, one per column: invert_diag_blocks), then
 // the blocks under the diagonal from [[M11, 0], [M21, M22]]^-1 = [[T11, 0],
-// [-T22 M21 T11, T22]] (all 256 threads: invert_off_diag): the two 16 x 16
-// ones, then the 32 x 32 one.  Xs: 32 x 33 scratch.
+// [-T22 M21 T11, T22]]: the two 16 x 16 ones by the 128 threads that built A
+// (invert_off_diag16, before Y's issuing warp is free), then the 32 x 32 one by
+// all 256 threads (invert_off_diag32).  Xs: 32 x 33 scratch.
 __device__ __forceinline__ float w_a(const float *W, int t, int i) { return W[t * kAS + i]; }
 __device__ __forceinline__ float &w_t(float *W, int t, int j) { return W[j * kAS + t]; }
 
@@ -252,34 +253,39 @@ __device__ __forceinline__ void invert_diag_blocks(float *W, int it)
         if (t >= jj) w_t(W, base + t, base + jj) = x[t];
 }
 
-__device__ __forceinline__ void invert_off_diag(float *W, float *Xs, int tid)
+// The two 16 x 16 blocks by the 128 threads of warps 0, 1, 4, 5 (it = 0..127, four outputs each).
+__device__ __forceinline__ void invert_off_diag16(float *W, float *Xs, int it)
 {
-    {   // X = M21 T11 for the pairs (rows 16..31, cols 0..15) and (rows 48..63, cols 32..47): row t, cols j0, j0+1
-        const int b = tid >> 7, t = (tid >> 3) & 15, j0 = 2 * (tid & 7), base = 32 * b;
-        float a0 = 0.f, a1 = 0.f;
+    {   // X = M21 T11 for the pairs (rows 16..31, cols 0..15) and (rows 48..63, cols 32..47): row t, cols j0..+3
+        const int b = it >> 6, t = (it >> 2) & 15, j0 = 4 * (it & 3), base = 32 * b;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const float a = w_a(W, base + 16 + t, base + i);
-            a0 = fmaf(a, i >= j0 ? w_t(W, base + i, base + j0) : 0.0f, a0);
-            a1 = fmaf(a, i >= j0 + 1 ? w_t(W, base + i, base + j0 + 1) : 0.0f, a1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = fmaf(a, i >= j0 + e ? w_t(W, base + i, base + j0 + e) : 0.0f, acc[e]);
         }
-        Xs[(16 * b + t) * kXS + j0] = a0;
-        Xs[(16 * b + t) * kXS + j0 + 1] = a1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) Xs[(16 * b + t) * kXS + j0 + e] = acc[e];
     }
-    __syncthreads();
+    sync_a_warps();
     {   // T21 = -T22 X for the two pairs
-        const int b = tid >> 7, t = (tid >> 3) & 15, j0 = 2 * (tid & 7), base = 32 * b;
-        float a0 = 0.f, a1 = 0.f;
+        const int b = it >> 6, t = (it >> 2) & 15, j0 = 4 * (it & 3), base = 32 * b;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const float tv = i <= t ? w_t(W, base + 16 + t, base + 16 + i) : 0.0f;
-            a0 = fmaf(tv, Xs[(16 * b + i) * kXS + j0], a0);
-            a1 = fmaf(tv, Xs[(16 * b + i) * kXS + j0 + 1], a1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = fmaf(tv, Xs[(16 * b + i) * kXS + j0 + e], acc[e]);
         }
-        w_t(W, base + 16 + t, base + j0) = -a0;
-        w_t(W, base + 16 + t, base + j0 + 1) = -a1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w_t(W, base + 16 + t, base + j0 + e) = -acc[e];
     }
-    __syncthreads();
+}
+
+// The 32 x 32 block by all 256 threads (four outputs each).
+__device__ __forceinline__ void invert_off_diag32(float *W, float *Xs, int tid)
+{
     {   // X = M21 T11 for the 32 x 32 halves: row t, cols 4 jq .. +3
         const int t = tid >> 3, j0 = 4 * (tid & 7);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -475,10 +481,12 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls)
             }
             sync_a_warps();                                // A complete
             if (hf == 0) invert_diag_blocks(W, (warp & 1) * 32 + lane);
+            sync_a_warps();                                // diagonal blocks of T done
+            invert_off_diag16(W, Xs, (warp & 1) * 32 + lane + 64 * hf);
             tc::fence_before_sync();
         }
-        __syncthreads();                                   // diagonal blocks of T done; issuers done issuing
-        invert_off_diag(W, Xs, tid);
+        __syncthreads();                                   // 16 x 16 blocks done; Y's issuer done issuing
+        invert_off_diag32(W, Xs, tid);
         ok = __syncthreads_and(ok_g && tc::mbar_wait(&bars[1], ph, polls)) != 0;         // T complete, Y done
         tc::fence_after_sync();
         if (!ok) break;
