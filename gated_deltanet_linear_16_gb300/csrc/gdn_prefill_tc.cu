@@ -169,13 +169,6 @@ __device__ __forceinline__ void sync_for_mma()
     __syncthreads();
     tc::fence_after_sync();
 }
-// Every thread waits for the mbarrier phase; the CTA agrees on the outcome.
-__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t parity, uint32_t polls)
-{
-    const bool ok = __syncthreads_and(tc::mbar_wait(bar, parity, polls)) != 0;
-    tc::fence_after_sync();
-    return ok;
-}
 // AND of `pred` over the 128 threads of warps 0, 1, 4, 5 (named barrier 1).
 __device__ __forceinline__ bool and_a_warps(bool pred)
 {
@@ -582,9 +575,8 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls)
         }
         __syncwarp();
         pend = 0x4u;
-        ok = wait_mma(&bars[2], ph, polls);
-        if (!ok) break;
-        pend = 0;
+        const bool ok2 = tc::mbar_wait(&bars[2], ph, polls);   // agreed on before MMA-3 is issued
+        tc::fence_after_sync();
 
         // ---- 3. Delta^T = sum of the three passes, split; Y_Q kept for the outputs ----
         float yq[32];
@@ -605,7 +597,10 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls)
         tc::st_wait();
 
         // ---- MMA-3: [Z | (P Delta)^T] = Delta^T [Ktilde | P^T] (N = 192), two issuers ----
-        sync_for_mma();
+        tc::fence_before_sync();
+        ok = __syncthreads_and(ok2) != 0;
+        tc::fence_after_sync();
+        if (!ok) break;
         if (tid == kIss0 || tid == kIss1) {       // over the first / second half of K (t)
             const bool first = tid == kIss0;
             mma_passes<true>(tmem_base + (first ? kM3a : kM3b), tmem_base + kDtHi, tmem_base + kDtLo, sbase + kBHi,
@@ -615,9 +610,8 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls)
         }
         __syncwarp();
         pend = 0x8u;
-        ok = wait_mma(&bars[3], ph, polls);
-        if (!ok) break;
-        pend = 0;
+        const bool ok3 = tc::mbar_wait(&bars[3], ph, polls);   // agreed on at the end of the chunk
+        tc::fence_after_sync();
 
         // ---- 4. outputs and the new state ----
 #pragma unroll
@@ -648,10 +642,12 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls)
                 for (int j = 0; j < 32; ++j) S[32 * cb + j] = fmaf(gC, S[32 * cb + j], za[j] + zb[j]);
             }
         }
-        ph ^= 1u;
         tc::fence_before_sync();
-        __syncthreads();                                   // scalars and the operand buffer are reused
+        ok = __syncthreads_and(ok3) != 0;                  // also: scalars and the operand buffer are reused
         tc::fence_after_sync();
+        if (!ok) break;
+        pend = 0;
+        ph ^= 1u;
     }
     cp_async_wait<0>();                                    // no copy left in flight
 
