@@ -8,7 +8,8 @@
 // does: S_t = alpha_t S_{t-1} + delta_t k_t^T with
 // delta_t = beta_t (v_t - alpha_t S_{t-1} k_t), o_t = S_t q_t / sqrt(D).
 // Unrolled over a chunk of C tokens from the state S at its start (gamma_t =
-// alpha_1 ... alpha_t, rho(t,i) = gamma_t / gamma_i = alpha_{i+1} ... alpha_t):
+// alpha_0 ... alpha_t with t counted from 0 in the chunk, rho(t,i) = alpha_{i+1}
+// ... alpha_t, taken as a product, never as the ratio gamma_t / gamma_i):
 //
 //   S_t   = gamma_t S + sum_{i<=t} rho(t,i) delta_i k_i^T
 //   delta_t + beta_t sum_{i<t} rho(t,i) (k_t.k_i) delta_i = beta_t (v_t - gamma_t S k_t)
@@ -20,30 +21,39 @@
 // the same arithmetic in real numbers (the chunked "WY" form of the delta
 // rule); only the fp32 rounding differs.  Per chunk and head, in order:
 //
-//   MMA-1  G = [K;Q] K^T (128 x 64)  and  Y = S [K;Q]^T (128 x 128, S from TMEM)
-//   SIMT   A and P[t][i] = rho(t,i) q_t.k_i from G;  R^T = beta (v - gamma Y_K)
-//          into TMEM;  T = (I + A)^-1;  Ktilde^T;  P, T, Ktilde^T to smem
-//   MMA-2  Delta^T = R^T T^T (128 x 64)
-//   SIMT   Delta^T split into TMEM
-//   MMA-3  P Delta as (Delta^T P^T) (128 x 64)  and  Z = Delta^T Ktilde (128 x 128)
-//   SIMT   o_t = (gamma_t Y_Q + P Delta) / sqrt(D);  S <- gamma_C S + Z, split into TMEM
+//   SIMT   the state, split, into TMEM; the chunk's [K;Q] (prefetched), split,
+//          into shared memory; gamma, rho(C,.) by warp scans
+//   MMA-1  G = [K;Q] K^T (128 x 64, two issuers over the halves of K) and
+//          Y = S [K;Q]^T (128 x 128, S from TMEM, one issuer)
+//   SIMT   A from G (warps 0, 1, 4, 5, while Y runs); T = (I + A)^-1 (16 x 16
+//          diagonal blocks, then block products); P from G; R^T = beta (v -
+//          gamma Y_K) into TMEM; T, P, Ktilde^T into shared memory
+//   MMA-2  Delta^T = R^T T^T (128 x 64, one issuer and accumulator per pass)
+//   SIMT   Delta^T = sum of the passes, split into TMEM
+//   MMA-3  [Z | (P Delta)^T] = Delta^T [Ktilde | P^T] (128 x 192, two issuers
+//          over the halves of K)
+//   SIMT   o_t = (gamma_t Y_Q + P Delta) / sqrt(D);  S <- gamma_C S + Z (fp32)
 //
-// Every MMA operand x is split as x = hi + lo with hi and lo TF32 values, and
-// a product is taken as hi*hi + hi*lo + lo*hi (three MMAs), which carries about
-// 22 significant bits per product; the accumulators are fp32 in tensor memory.
-// The exact fp32 state stays in registers (thread = row a of the head, half of
-// its columns); only its split copy is in tensor memory.
+// Every MMA operand x is split as x = hi + lo with hi the nearest TF32 value and
+// lo = x - hi (read as TF32 by the tensor core), and a product is taken as
+// hi*hi + hi*lo + lo*hi (three passes), which carries about 21 significant bits
+// per product; the accumulators are fp32 in tensor memory.  The exact fp32
+// state stays in registers (thread = row a of the head, half of its columns);
+// only its split copy is in tensor memory.
 //
 // One CTA (8 warps) per (sequence, value head); warp w owns tensor-memory lanes
-// 32*(w%4).. (rows of the state) and half w/4 of the columns it loads.  Thread
-// 64 (lane 0 of warp 2, a warp with no part in the inversion) issues the MMAs,
-// so the other warps go on while the tensor core takes them.  The next chunk's
-// k, q, alpha and beta are copied into shared memory (cp.async) during the
-// current chunk.  The CTA holds all 512 tensor-memory columns and ~210 KB of
-// shared memory, so an SM runs one such CTA at a time.  The only waits are on the CTA's own MMA
-// completions (an mbarrier armed by tcgen05.commit), each bounded: if a bound
-// ran out (or the bound was set to 0 to test this path), the CTA stops, lets
-// the MMAs it issued finish (again bounded), counts the event in
+// 32*(w%4).. (rows of the state) and half w/4 of the columns it loads.  Lane 0
+// of warps 2, 3 and 6 issue the MMAs (one thread issues one MMA per ~140 cycles
+// whatever its N, and MMAs from several warps proceed together), so each
+// product is split over two or three issuers, each part into its own
+// accumulator.  The next chunk's k, q, alpha and beta are copied into shared
+// memory (cp.async) during the current chunk.  The CTA holds all 512
+// tensor-memory columns and ~218 KB of shared memory, so an SM runs one such
+// CTA at a time.  Loops stay rolled where they can: the chunk body runs once
+// per chunk on few warps, so instruction fetch is a cost.  The only waits are
+// on the CTA's own MMA completions (mbarriers armed by tcgen05.commit), each
+// bounded: if a bound ran out (or was set to 0 to test this path), the CTA
+// stops, lets the MMAs it issued finish (again bounded), counts the event in
 // g_tc_wait_timeouts and writes NaN to its state.
 #include <atomic>
 
