@@ -17,13 +17,16 @@
 // the decode kernel's shape (8 warps x 16 rows), so the 64 KB-per-head state
 // stream is unchanged and no CTA waits for another (fp16 states take the
 // page's per-key-head shape, conv_norm_kh below, which measured faster there):
-//  * every CTA issues its state loads first, then updates the ring rows of its
-//    own value head's v channels and computes v (one writer per ring row);
-//  * every CTA also computes the key head's q and k (conv, silu, L2: 256
-//    channels) from the ring as it was, without writing it, and keeps the
-//    shifted rows in shared memory;
+//  * every CTA issues its conv inputs first (ring entries, token values, tap
+//    weights: a few KB that would otherwise queue behind the state stream),
+//    then its state loads, then computes while the state streams in;
+//  * it updates the ring rows of its own value head's v channels and computes
+//    v (one writer per ring row);
+//  * it also computes the key head's q and k (conv, silu, L2: 256 channels)
+//    from the ring as it was, without writing it, and keeps the shifted rows in
+//    shared memory;
 //  * after reading, a CTA counts itself in a per-(sequence, key head) counter
-//    (fence + atomic add, by a thread with no global stores to drain, its
+//    (fence + atomic add by one thread as its last batch of rows begins, the
 //    result read only after the step); the CTA that completes the count is the
 //    last reader of those ring rows, so it writes them and resets the counter.
 // No barrier spans CTAs and nothing spins.  (Thread-block clusters, tried
@@ -40,57 +43,106 @@ constexpr int kRowsPerWarp = kD / kWarps;   // 16
 
 constexpr int kMaxTaps = 8;                 // the host rejects more
 
-// One channel through the conv ring: shift up by one, append x, reduce with the
-// taps, silu.  The caller is the only thread touching this channel.  All stored
-// entries are read before any is written (one load latency, not one per tap).
+// One channel's stored inputs: the taps - 1 ring entries that stay in the ring
+// (oldest first) and the token's value; MT bounds the tap count (the arrays
+// live in registers, so a call with few taps takes an instance with a small
+// MT).  Callers load every channel they own first, then compute, then store
+// the shifted rows: a store through a generic pointer between two loads would
+// keep the later load behind it, costing a second memory latency.
+template <int MT>
+struct ConvIn {
+    float val[MT - 1];
+    float xv;
+};
+
+template <int MT>
+__device__ __forceinline__ void conv_load(ConvIn<MT> &in, const float *ring, const float *x, int64_t c, int64_t C,
+                                          int taps) {
+#pragma unroll
+    for (int t = 0; t + 1 < MT; ++t) in.val[t] = t + 1 < taps ? ring[(int64_t)(t + 1) * C + c] : 0.f;
+    in.xv = __ldg(x + c);
+}
+
+// The conv over the shifted ring (taps in order, the new token last) and silu.
+template <int MT>
+__device__ __forceinline__ float conv_silu(const ConvIn<MT> &in, const float *w, int64_t c, int64_t C, int taps) {
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t + 1 < MT; ++t)
+        if (t + 1 < taps) acc = fmaf(in.val[t], __ldg(w + (int64_t)t * C + c), acc);
+    acc = fmaf(in.xv, __ldg(w + (int64_t)(taps - 1) * C + c), acc);
+    return silu(acc);
+}
+
+// The ring's new contents (shift up by one, append the token) to `dst` (taps
+// entries, stride `stride`): the ring itself for the channel's only writer, or
+// a shared-memory copy for a later writer.
+template <int MT>
+__device__ __forceinline__ void conv_shift(const ConvIn<MT> &in, float *dst, int64_t stride, int taps) {
+#pragma unroll
+    for (int t = 0; t + 1 < MT; ++t)
+        if (t + 1 < taps) dst[(int64_t)t * stride] = in.val[t];
+    dst[(int64_t)(taps - 1) * stride] = in.xv;
+}
+
+// A channel's stored inputs with its taps' weights, all loaded at once (the
+// per-value-head kernel issues these before its state stream, which would
+// otherwise queue ahead of them).
+template <int MT>
+struct ConvInW {
+    ConvIn<MT> in;
+    float wt[MT - 1];
+    float wx;
+};
+
+template <int MT>
+__device__ __forceinline__ void conv_load_w(ConvInW<MT> &c, const float *ring, const float *x, const float *w,
+                                            int64_t ch, int64_t C, int taps) {
+    conv_load(c.in, ring, x, ch, C, taps);
+#pragma unroll
+    for (int t = 0; t + 1 < MT; ++t) c.wt[t] = t + 1 < taps ? __ldg(w + (int64_t)t * C + ch) : 0.f;
+    c.wx = __ldg(w + (int64_t)(taps - 1) * C + ch);
+}
+
+// conv_silu over preloaded weights (the same arithmetic in the same order).
+template <int MT>
+__device__ __forceinline__ float conv_silu_w(const ConvInW<MT> &c, int taps) {
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t + 1 < MT; ++t)
+        if (t + 1 < taps) acc = fmaf(c.in.val[t], c.wt[t], acc);
+    acc = fmaf(c.in.xv, c.wx, acc);
+    return silu(acc);
+}
+
+// One channel through the conv ring in place: shift, append, reduce, silu.
+// The caller is the only thread touching this channel.
 __device__ __forceinline__ float conv_silu_channel(float *ring, const float *x, const float *w,
                                                    int64_t c, int64_t C, int taps) {
-    float val[kMaxTaps - 1];
-#pragma unroll
-    for (int t = 0; t + 1 < kMaxTaps; ++t) val[t] = t + 1 < taps ? ring[(int64_t)(t + 1) * C + c] : 0.f;
-    const float xv = __ldg(x + c);
-    float acc = 0.f;
-#pragma unroll
-    for (int t = 0; t + 1 < kMaxTaps; ++t) {
-        if (t + 1 < taps) {
-            ring[(int64_t)t * C + c] = val[t];
-            acc = fmaf(val[t], __ldg(w + (int64_t)t * C + c), acc);
-        }
-    }
-    ring[(int64_t)(taps - 1) * C + c] = xv;
-    acc = fmaf(xv, __ldg(w + (int64_t)(taps - 1) * C + c), acc);
-    return silu(acc);
+    ConvIn<kMaxTaps> in;
+    conv_load(in, ring, x, c, C, taps);
+    const float y = conv_silu(in, w, c, C, taps);
+    conv_shift(in, ring + c, C, taps);
+    return y;
 }
-
-// The same channel computed from the ring without writing it; the shifted
-// entries (the ring's new contents) go to `keep` (taps entries, stride kstride)
-// for the owner to store later.
-__device__ __forceinline__ float conv_silu_channel_ro(const float *ring, const float *x, const float *w,
-                                                      int64_t c, int64_t C, int taps,
-                                                      float *keep, int kstride) {
-    float val[kMaxTaps - 1];
-#pragma unroll
-    for (int t = 0; t + 1 < kMaxTaps; ++t) val[t] = t + 1 < taps ? ring[(int64_t)(t + 1) * C + c] : 0.f;
-    const float xv = __ldg(x + c);
-    float acc = 0.f;
-#pragma unroll
-    for (int t = 0; t + 1 < kMaxTaps; ++t) {
-        if (t + 1 < taps) {
-            keep[t * kstride] = val[t];
-            acc = fmaf(val[t], __ldg(w + (int64_t)t * C + c), acc);
-        }
-    }
-    keep[(taps - 1) * kstride] = xv;
-    acc = fmaf(xv, __ldg(w + (int64_t)(taps - 1) * C + c), acc);
-    return silu(acc);
-}
-
 
 __device__ __forceinline__ void gates(const ConvNormParams &p, int seq, int h, float &alpha, float &beta) {
     const float br = __ldg(p.br + seq * p.gate_stride + h);
     const float ar = __ldg(p.ar + seq * p.gate_stride + h);
     beta = 1.0f / (1.0f + expf(-br));
     alpha = powf(1.0f + expf(ar + __ldg(p.dt + h)), __ldg(p.rate + h));
+}
+
+// The gates' four inputs, loaded apart from their arithmetic (gates_of) so the
+// loads can be in flight with a thread's other producer loads.
+struct GateIn { float br, ar, dt, rate; };
+__device__ __forceinline__ GateIn gate_load(const ConvNormParams &p, int seq, int h) {
+    return {__ldg(p.br + seq * p.gate_stride + h), __ldg(p.ar + seq * p.gate_stride + h), __ldg(p.dt + h),
+            __ldg(p.rate + h)};
+}
+__device__ __forceinline__ void gates_of(const GateIn &g, float &alpha, float &beta) {
+    beta = 1.0f / (1.0f + expf(-g.br));
+    alpha = powf(1.0f + expf(g.ar + g.dt), g.rate);
 }
 
 constexpr int kGroups = 4;                 // cp.async commit groups per lane (staged)
@@ -100,7 +152,7 @@ constexpr int stage_bytes() { return kD * kD * (int)sizeof(TS); }
 
 // STAGED: the head's state goes to shared memory by cp.async, every load in
 // flight at once (as the staged decode kernel); otherwise NB register batches.
-template <typename TS, bool STAGED, int NB, int MINB, bool EARLY>
+template <typename TS, bool STAGED, int NB, int MINB, bool EARLY, int MT>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
 conv_norm_d128(const ConvNormParams p)
 {
@@ -137,7 +189,26 @@ conv_norm_d128(const ConvNormParams p)
     TS *rowp = head + (int64_t)(row0 + sub) * kD + col;
     early_start<EARLY>(head, p.pf_bytes);
 
-    // 1. state loads in flight before the producers run
+    // 1. the producers' inputs: a few KB per CTA, issued before the state stream so that they do not
+    //    queue behind it.  Threads 0..127: channel i of this value head's v (ring rows written below,
+    //    by their only writer) and thread 0 the gate inputs; threads 128..255: channel i of the key
+    //    head's q and of its k (read only; the last reader writes them, step 6).
+    float *ring = p.ring + seq * p.ring_pitch;
+    const float *x = p.x + seq * p.x_stride;
+    const int pi = tid & (kD - 1);
+    const int64_t cv = 2 * (int64_t)p.nk * kD + (int64_t)h * kD + pi;
+    const int64_t cq = (int64_t)kh * kD + pi, ck = (int64_t)(p.nk + kh) * kD + pi;
+    ConvInW<MT> ca, cb;
+    GateIn gi{};
+    if (tid < kD) {
+        conv_load_w(ca, ring, x, p.w, cv, C, p.taps);
+        if (tid == 0) gi = gate_load(p, seq, h);
+    } else {
+        conv_load_w(ca, ring, x, p.w, cq, C, p.taps);
+        conv_load_w(cb, ring, x, p.w, ck, C, p.taps);
+    }
+
+    // 2. the state loads
     extern __shared__ __align__(16) unsigned char smem_raw[];   // staged: [kD rows][VPR]
     uint4 *mine = reinterpret_cast<uint4 *>(smem_raw) + (row0 + sub) * VPR + (lane % LPR);
     uint4 raw[STAGED ? 1 : (NB > 1 ? 2 : 1)][STAGED ? 1 : PER];
@@ -156,35 +227,24 @@ conv_norm_d128(const ConvNormParams p)
         for (int i = 0; i < PER; ++i) raw[0][i] = ld_stream16(rowp + (int64_t)i * RPL * kD);
     }
 
-    // 2. producers: v of this head (threads 0..127, ring rows written now: their only writer);
-    //    q and k of the key head (threads 128..255) from the ring as it was, not written yet
-    float *ring = p.ring + seq * p.ring_pitch;
-    const float *x = p.x + seq * p.x_stride;
+    // 3. the producers' arithmetic while the state streams in
     if (tid < kD) {
-        v_s[tid] = conv_silu_channel(ring, x, p.w, 2 * (int64_t)p.nk * kD + (int64_t)h * kD + tid, C, p.taps);
+        v_s[pi] = conv_silu_w(ca, p.taps);
+        conv_shift(ca.in, ring + cv, C, p.taps);
+        if (tid == 0) gates_of(gi, gate_s[0], gate_s[1]);
     } else {
-        const int i = tid - kD;
-        const float qv = conv_silu_channel_ro(ring, x, p.w, (int64_t)kh * kD + i, C, p.taps, &ring_new[0][0][i], kD);
-        const float kv = conv_silu_channel_ro(ring, x, p.w, (int64_t)(p.nk + kh) * kD + i, C, p.taps,
-                                              &ring_new[1][0][i], kD);
+        const float qv = conv_silu_w(ca, p.taps), kv = conv_silu_w(cb, p.taps);
+        conv_shift(ca.in, &ring_new[0][0][pi], kD, p.taps);
+        conv_shift(cb.in, &ring_new[1][0][pi], kD, p.taps);
         const float sq = group_sum<32>(qv * qv), sk = group_sum<32>(kv * kv);
         if (lane == 0) { red_q[warp - 4] = sq; red_k[warp - 4] = sk; }
         asm volatile("bar.sync 1, 128;" ::: "memory");  // the four producer warps
         const float tq = (red_q[0] + red_q[1]) + (red_q[2] + red_q[3]);
         const float tk = (red_k[0] + red_k[1]) + (red_k[2] + red_k[3]);
-        q_s[i] = qv / sqrtf(tq + p.l2_eps);
-        k_s[i] = kv / sqrtf(tk + p.l2_eps);
+        q_s[pi] = qv / sqrtf(tq + p.l2_eps);
+        k_s[pi] = kv / sqrtf(tk + p.l2_eps);
     }
-    if (tid == 0) gates(p, seq, h, gate_s[0], gate_s[1]);
     __syncthreads();                                     // this CTA is done reading the q/k ring rows
-    // The count is taken by a q/k producer thread (it has no global stores for
-    // its fence to drain); its result is needed only after the step.
-    constexpr int kCounter = kWarps * 32 - 1;
-    int seen = 0;
-    if (tid == kCounter) {
-        __threadfence();                                 // the reads above come before the count
-        seen = atomicAdd(p.counters + cl, 1);
-    }
 
     float kx[EPV], qx[EPV];
 #pragma unroll
@@ -234,6 +294,21 @@ conv_norm_d128(const ConvNormParams p)
             }
         }
     };
+    // This CTA's reads of the key head's q/k ring rows ended at the __syncthreads after step 3.  It
+    // counts itself (fence + atomic add, one thread) as its last batch of rows begins: the fence
+    // waits for the counting thread's own memory operations in flight, which by then are only the
+    // loads of that batch, needed next anyway, and the add's round trip overlaps the batch.  (Taken
+    // right after step 3, the fence held the thread's warp until all its first loads had landed:
+    // 38.3 us a launch at batch 32; after the rows, 35.1 us; here, 34.2 us.)  Its result is first
+    // needed after the norm's barrier.
+    constexpr int kCounter = kWarps * 32 - 1;
+    int seen = 0;
+    auto count_reader = [&](int bt) {
+        if (bt == NBAT - 1 && tid == kCounter) {
+            __threadfence();                             // every read of the ring comes before the count
+            seen = atomicAdd(p.counters + cl, 1);
+        }
+    };
 #pragma unroll
     for (int bt = 0; bt < NBAT; ++bt) {
         if constexpr (STAGED) {
@@ -241,6 +316,7 @@ conv_norm_d128(const ConvNormParams p)
             else if (bt == 1) cp_async_wait<kGroups - 2>();
             else if (bt == 2) cp_async_wait<kGroups - 3>();
             else cp_async_wait<0>();
+            count_reader(bt);
 #pragma unroll
             for (int ii = 0; ii < PER; ++ii) row_step(mine[(bt * PER + ii) * RPL * VPR], bt * PER + ii);
         } else {
@@ -249,6 +325,7 @@ conv_norm_d128(const ConvNormParams p)
                 for (int i = 0; i < PER; ++i)
                     raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * PER + i) * RPL * kD);
             }
+            count_reader(bt);
 #pragma unroll
             for (int ii = 0; ii < PER; ++ii) row_step(raw[bt & 1][ii], bt * PER + ii);
         }
@@ -559,8 +636,10 @@ conv_norm_generic(const ConvNormParams p)
 // Shapes of the per-value-head D == 128 kernel, by measurement on GB300 (one
 // layer at batch 32 fp32, 256-slot fp16 pool): fp32 register batches (4 x 4
 // loads, 4 CTAs per SM: a CTA spends part of its life in the producer phase,
-// so more of them keep the state streaming); fp16 staged in shared memory
-// (32 KB + 10 KB a CTA, 5 CTAs per SM) -- used for fp16 only when NV/NK > 8.
+// so more of them keep the state streaming; 34.2 us a launch, against 42.4 us
+// for 2 x 8 loads at 3 CTAs per SM and 39.3 us staged in shared memory at 3);
+// fp16 staged in shared memory (32 KB + 10 KB a CTA, 5 CTAs per SM) -- used
+// for fp16 only when NV/NK > 8.
 template <typename TS> struct ConvShape {
     static constexpr bool kStaged = false;
     static constexpr int kBatches = 4, kMinBlocks = 4;
@@ -569,6 +648,33 @@ template <> struct ConvShape<__half> {
     static constexpr bool kStaged = true;
     static constexpr int kBatches = 1, kMinBlocks = 5;
 };
+
+// The per-value-head kernel with tap bound MT.
+template <typename TS, int MT>
+cudaError_t launch_d128(const ConvNormParams &p, cudaStream_t s)
+{
+    using F = ConvShape<TS>;
+    const int dyn = F::kStaged ? stage_bytes<TS>() : 0;
+    const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
+    // early launch (grids of a few waves) with the whole head asked of the L2: these CTAs run
+    // the conv and gate producers before they need the state (measured: whole 32.6 us, half 34.3)
+    if (early_grid(grid, F::kMinBlocks)) {
+        ConvNormParams q = p;
+        q.pf_bytes = (unsigned)(kD * kD * sizeof(TS));
+        constexpr auto kern = conv_norm_d128<TS, F::kStaged, F::kBatches, F::kMinBlocks, true, MT>;
+        if (F::kStaged) {
+            const cudaError_t e = allow_dynamic_smem<kern>(dyn);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_early(kern, grid, kWarps * 32, dyn, s, true, q);
+    }
+    constexpr auto kern = conv_norm_d128<TS, F::kStaged, F::kBatches, F::kMinBlocks, false, MT>;
+    if (F::kStaged) {
+        const cudaError_t e = allow_dynamic_smem<kern>(dyn);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_early(kern, grid, kWarps * 32, dyn, s, false, p);
+}
 
 template <typename TS>
 cudaError_t launch_typed(const ConvNormParams &p, bool fast, cudaStream_t s)
@@ -584,29 +690,7 @@ cudaError_t launch_typed(const ConvNormParams &p, bool fast, cudaStream_t s)
             return cudaGetLastError();
         }
     }
-    if (fast) {
-        using F = ConvShape<TS>;
-        const int dyn = F::kStaged ? stage_bytes<TS>() : 0;
-        const unsigned grid = (unsigned)((int64_t)p.batch * p.nv);
-        // early launch (grids of a few waves) with the whole head asked of the L2: these CTAs run
-        // the conv and gate producers before they need the state (measured: whole 32.6 us, half 34.3)
-        if (early_grid(grid, F::kMinBlocks)) {
-            ConvNormParams q = p;
-            q.pf_bytes = (unsigned)(kD * kD * sizeof(TS));
-            constexpr auto kern = conv_norm_d128<TS, F::kStaged, F::kBatches, F::kMinBlocks, true>;
-            if (F::kStaged) {
-                const cudaError_t e = allow_dynamic_smem<kern>(dyn);
-                if (e != cudaSuccess) return e;
-            }
-            return launch_early(kern, grid, kWarps * 32, dyn, s, true, q);
-        }
-        constexpr auto kern = conv_norm_d128<TS, F::kStaged, F::kBatches, F::kMinBlocks, false>;
-        if (F::kStaged) {
-            const cudaError_t e = allow_dynamic_smem<kern>(dyn);
-            if (e != cudaSuccess) return e;
-        }
-        return launch_early(kern, grid, kWarps * 32, dyn, s, false, p);
-    }
+    if (fast) return p.taps <= 4 ? launch_d128<TS, 4>(p, s) : launch_d128<TS, kMaxTaps>(p, s);
     const size_t smem = sizeof(float) * ((size_t)(3 + p.repeat) * p.d + 2 * (size_t)p.repeat);
     conv_norm_generic<TS><<<(unsigned)((int64_t)p.batch * p.nk), kGenWarps * 32, smem, s>>>(p);
     return cudaGetLastError();

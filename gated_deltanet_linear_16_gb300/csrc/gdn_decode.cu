@@ -143,6 +143,9 @@ decode_d128(const DecodeParams p)
 #pragma unroll
     for (int j = 0; j < EPV; ++j) kq = fmaf(kx[j], qx[j], kq);
     kq = group_sum<LPR>(kq);
+    // the norm's per-row factor gn silu(z), ready before the rows are stepped (off the
+    // latency path of a one-wave grid, where the epilogue is the tail of the launch)
+    const float gz = NORM ? gn_l * silu(z_l) : 0.f;
 
     // 3. per row: two dot products, the delta coefficient, output, write-back
     float o_keep = 0.f;                        // lane r keeps o of row row0 + r
@@ -198,13 +201,17 @@ decode_d128(const DecodeParams p)
         const float ss = group_sum<32>(o_keep * o_keep);   // lanes >= RPW hold 0
         if (lane == 0) red[warp] = ss;
         __syncthreads();
-        float tot = 0.f;
+        float part[W];                         // pairwise sum of the warps' partials
 #pragma unroll
-        for (int i = 0; i < W; ++i) tot += red[i];
-        const float rstd = rsqrtf(tot * (1.0f / kD) + p.eps);
+        for (int i = 0; i < W; ++i) part[i] = red[i];
+#pragma unroll
+        for (int n = W / 2; n >= 1; n /= 2)
+#pragma unroll
+            for (int i = 0; i < n; ++i) part[i] += part[i + n];
+        const float rstd = rsqrtf(part[0] * (1.0f / kD) + p.eps);
         if constexpr (EPI == kEpiBf16) {
             if (row_lane) {
-                const float y = gn_l * o_keep * rstd * silu(z_l);
+                const float y = gz * o_keep * rstd;
                 p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
             }
         } else {
@@ -212,7 +219,7 @@ decode_d128(const DecodeParams p)
             // values meet in shared memory and warp w < 4 quantises group w.
             __shared__ float y_s[kD];
             if (row_lane) {
-                const float y = gn_l * o_keep * rstd * silu(z_l);
+                const float y = gz * o_keep * rstd;
                 y_s[row0 + lane] = y;
                 if (p.y != nullptr) p.y[seq * p.y_stride + (int64_t)h * kD + row0 + lane] = y;
             }

@@ -94,9 +94,18 @@ def test_d128_kernel(f16, NK, NV):
     check(run(2, NK, NV, 128, 4, f16, seed=51 + NV, steps=3, pad=(4, 1, 2, 6), ring_pad=16), f16)
 
 
-@pytest.mark.parametrize("taps", [1, 2, 3, 8])
+@pytest.mark.parametrize("taps", [1, 2, 3, 4, 5, 8])
 def test_taps(taps):
+    """Up to 4 taps the per-value-head kernel holds a channel's ring entries in 3-entry register
+    arrays, above that in 7-entry ones (conv_norm_d128<float, ..., MT = 4 | 8>)."""
     check(run(2, 2, 6, 128, taps, False, seed=60 + taps), False)
+
+
+@pytest.mark.parametrize("taps", [2, 6])
+def test_taps_f16_per_value_head(taps):
+    """fp16 with NV / NK = 9 > 8 takes the per-value-head kernel (conv_norm_d128<__half, ...>) for
+    both tap bounds."""
+    check(run(2, 1, 9, 128, taps, True, seed=90 + taps), True)
 
 
 @pytest.mark.parametrize("f16", [False, True])
