@@ -770,7 +770,10 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
                             "ms": s_tc * 1e3, "token_heads_per_s": th / s_tc, "speedup_vs_token_loop": s / s_tc,
                             "roofline": {"bound": "tensor", "achieved": tc_flop / s_tc / 1e12,
                                          "peak": tf32_peak / 1e12, "unit": "TFLOP/s (TF32 MMA, executed)",
-                                         "frac": tc_flop / s_tc / tf32_peak, "peak_basis": tf32_basis}},
+                                         "frac": tc_flop / s_tc / tf32_peak, "peak_basis": tf32_basis},
+                            # the token-sequential work (4 D^2 FP32 instructions per token-head) over this
+                            # kernel's time, against the FP32 issue peak: the rate the token loop would need
+                            "token_loop_equivalent_frac_4d2": 4 / 3 * fma / s_tc / fma_peak},
                         "ms": s * 1e3, "token_heads_per_s": th / s,
                         "roofline": {"bound": "alu", "achieved": fma / s / 1e12, "peak": fma_peak / 1e12,
                                      "unit": "T FP32 FMA/s", "frac": fma / s / fma_peak,

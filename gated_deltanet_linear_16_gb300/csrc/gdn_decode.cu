@@ -149,6 +149,7 @@ decode_d128(const DecodeParams p)
 
     // 3. per row: two dot products, the delta coefficient, output, write-back
     float o_keep = 0.f;                        // lane r keeps o of row row0 + r
+    float o_sq = 0.f;                          // sum of o^2 over the rows of this lane's row group
     auto row_step = [&](const uint4 packed, const int i) {   // i: vector index within the lane's slice
         float s[EPV];
         V::unpack(packed, s);
@@ -160,6 +161,7 @@ decode_d128(const DecodeParams p)
         const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
         const float coef = beta * (va - alpha * u);
         const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
+        if constexpr (NORM) o_sq = fmaf(oa, oa, o_sq);   // every lane of the group holds oa
 #pragma unroll
         for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
         st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
@@ -198,7 +200,10 @@ decode_d128(const DecodeParams p)
     } else {
         // 4. gated RMS norm over the head's 128 outputs, in this CTA
         __shared__ float red[W];
-        const float ss = group_sum<32>(o_keep * o_keep);   // lanes >= RPW hold 0
+        // the warp's sum of squares: each row group's lanes accumulated its rows' o^2 in the loop
+        float ss = o_sq;
+#pragma unroll
+        for (int r = 1; r < RPL; ++r) ss += __shfl_sync(kFull, o_sq, r * LPR);
         if (lane == 0) red[warp] = ss;
         __syncthreads();
         float part[W];                         // pairwise sum of the warps' partials
