@@ -60,6 +60,10 @@ NCU_TRAFFIC = {
     # mean of two launches of the 256-slot fp16 pool decode (reads 413.3 MB, writes 388.7-388.8 MB)
     "decode_norm_f16_pool": {"bytes_per_launch": 802121216,
                              "src_sha256": "cf5cb0f8aa290eb7f1bbcc53616eba2ec58c3e148f0e1b9c4ffb9d38dc623d74"},
+    # mean of two launches of the batch-32 fp32 decode from projections (reads 105.7-105.9 MB, writes
+    # 102.9-104.4 MB), ncu --cache-control none
+    "conv_norm_f32": {"bytes_per_launch": 209400448, "src": ("gdn_conv_norm.cu", "gdn_internal.cuh"),
+                      "src_sha256": "e746be9c1348695371dea7fb0e256dab4f590bb665212e633313fa9606b7290e"},
 }
 
 
@@ -108,7 +112,8 @@ def tf32_peak_flops(pk):
 def pinned_traffic(key):
     """ncu DRAM bytes per launch for NCU_TRAFFIC[key], or None once the kernel source has changed."""
     tr = NCU_TRAFFIC[key]
-    return tr["bytes_per_launch"] if tr["src_sha256"] == src_sha("gdn_decode.cu", "gdn_internal.cuh") else None
+    src = tr.get("src", ("gdn_decode.cu", "gdn_internal.cuh"))
+    return tr["bytes_per_launch"] if tr["src_sha256"] == src_sha(*src) else None
 
 
 def src_sha(*names):
@@ -541,6 +546,8 @@ def row_conv_norm(torch, gdn, dev, stream, pk, taps=4):
                        + ("" if f16 else f", {nl} layers' states in turn"),
              "us_per_launch": s * 1e6, "token_heads_per_s": batch * NV / s, "achieved_gbs": by / s / 1e9,
              "frac_of_hbm_peak": by / s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by}
+        if not f16:
+            r["traffic"] = pinned_traffic("conv_norm_f32")
         if not f16:
             s2 = time_fn(torch, stream, cycling([lambda a=a: gdn.gdn_decode_conv_norm_noalloc(*a, **kw)
                                                  for a in args]), 48)
