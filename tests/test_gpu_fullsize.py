@@ -183,10 +183,11 @@ def test_prefill_4096_tokens(chunked):
         bt[rows] = torch.from_numpy(xs["beta"][i]).to(dev)
     o = torch.empty((R, NV * D), device=dev)
     S = torch.zeros((B, NV, D, D), device=dev)
+    before = gdn.gdn_device_wait_timeouts()      # other tests in this process may have forced some
     (gdn.gdn_prefill_chunked if chunked else gdn.gdn_prefill_seq)(S, q, k, v, a, bt, o, batch=B, seq_len=T,
                                                                    nk=NK, nv=NV, d=D)
     torch.cuda.synchronize()
-    assert gdn.gdn_device_wait_timeouts() == 0
+    assert gdn.gdn_device_wait_timeouts() == before
     assert torch.isfinite(o).all().item() and torch.isfinite(S).all().item()
     heads = [(0, 0), (0, 17), (0, 47), (1, 3), (1, 16), (1, 40)]
 

@@ -40,6 +40,13 @@ def test_from_zero_state_with_strides_and_pitch():
     check(run_prefill_case(2, 2, 5, 128, 97, seed=410, pad=(4, 8, 1, 3), pitch_pad=4096, chunked=True))
 
 
+@pytest.mark.parametrize("pad", [(0, 0, 0, 8), (4, 8, 1, 3)])
+def test_o_row_padding(pad):
+    """o rows padded by 8 floats (a 16-byte multiple: the outputs leave by one tensor store per chunk,
+    clipped at the sequence's end) and by 3 (plain stores); the padding must stay untouched."""
+    check(run_prefill_case(3, 2, 3, 128, 150, seed=416 + pad[3], init="normal", pad=pad, chunked=True))
+
+
 def test_long_sequence():
     check(run_prefill_case(1, 2, 4, 128, 1000, seed=411, init="normal", chunked=True))
 
