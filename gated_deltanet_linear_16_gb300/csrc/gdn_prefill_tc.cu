@@ -89,13 +89,15 @@ constexpr uint32_t kBHi = 32768, kBLo = 81920;
 constexpr int kBRows = 192;
 constexpr uint32_t kStage = 131072;                    // next chunk's raw [K;Q], 128 rows x 512 B
 // fp32 64 x 64 work matrix W (row stride kAS): A in its strict lower triangle, T = (I + A)^-1
-// transposed in its upper triangle and diagonal (T[t][j] at W[j][t]); then a 32 x 33 scratch.
-constexpr int kAS = 65, kXS = 33;
-constexpr uint32_t kWOff = kStage + 65536, kXsOff = kWOff + kC * kAS * 4;
+// transposed in its upper triangle and diagonal (T[t][j] at W[j][t]); then a 32 x 36 scratch Xs and
+// Tr, T's top-left 32 x 32 block row-major (zeros above the diagonal), both with 16-byte rows so the
+// 32 x 32 block product reads four consecutive columns in one load
+constexpr int kAS = 65, kXS = 36, kTS = 36;
+constexpr uint32_t kWOff = kStage + 65536, kXsOff = kWOff + kC * kAS * 4, kTrOff = kXsOff + 32 * kXS * 4;
 // the chunk's outputs o[t][a] (64 x 128 fp32, row-major) for one tensor store, over W and the scratch
 // after them: written in the last phase, read out by the copy engine before the next chunk builds A
 constexpr uint32_t kOStage = kWOff, kOBytes = kC * kD * 4;
-constexpr uint32_t kSmemEnd = (kXsOff + 32 * kXS * 4 > kOStage + kOBytes) ? kXsOff + 32 * kXS * 4 : kOStage + kOBytes;
+constexpr uint32_t kSmemEnd = (kTrOff + 32 * kTS * 4 > kOStage + kOBytes) ? kTrOff + 32 * kTS * 4 : kOStage + kOBytes;
 constexpr uint32_t kSmemBytes = kSmemEnd + 1024;                        // + alignment slack
 
 // tensor-memory columns
@@ -255,11 +257,11 @@ __device__ __forceinline__ void sync_a_warps() { asm volatile("bar.sync 1, 128;"
 // the blocks under the diagonal from [[M11, 0], [M21, M22]]^-1 = [[T11, 0],
 // [-T22 M21 T11, T22]]: the two 16 x 16 ones by the 128 threads that built A
 // (invert_off_diag16, before Y's issuing warp is free), then the 32 x 32 one by
-// all 256 threads (invert_off_diag32).  Xs: 32 x 33 scratch.
+// all 256 threads (invert_off_diag32).  Xs: 32 x 36 scratch; Tr: row-major copy of T[0..31][0..31].
 __device__ __forceinline__ float w_a(const float *W, int t, int i) { return W[t * kAS + i]; }
 __device__ __forceinline__ float &w_t(float *W, int t, int j) { return W[j * kAS + t]; }
 
-__device__ __forceinline__ void invert_diag_blocks(float *W, int it)
+__device__ __forceinline__ void invert_diag_blocks(float *W, float *Tr, int it)
 {
     const int kb = it >> 4, jj = it & 15, base = 16 * kb;
     float x[16];
@@ -279,10 +281,18 @@ __device__ __forceinline__ void invert_diag_blocks(float *W, int it)
 #pragma unroll
     for (int t = 0; t < 16; ++t)
         if (t >= jj) w_t(W, base + t, base + jj) = x[t];
+    if (kb < 2) {                                  // Tr: this column of the block (x[t] = 0 above it)
+#pragma unroll
+        for (int t = 0; t < 16; ++t) Tr[(base + t) * kTS + base + jj] = x[t];
+        if (kb == 0) {                             // and the zero block right of it
+#pragma unroll
+            for (int t = 0; t < 16; ++t) Tr[t * kTS + 16 + jj] = 0.0f;
+        }
+    }
 }
 
 // The two 16 x 16 blocks by the 128 threads of warps 0, 1, 4, 5 (it = 0..127, four outputs each).
-__device__ __forceinline__ void invert_off_diag16(float *W, float *Xs, int it)
+__device__ __forceinline__ void invert_off_diag16(float *W, float *Xs, float *Tr, int it)
 {
     {   // X = M21 T11 for the pairs (rows 16..31, cols 0..15) and (rows 48..63, cols 32..47): row t, cols j0..+3
         const int b = it >> 6, t = (it >> 2) & 15, j0 = 4 * (it & 3), base = 32 * b;
@@ -308,40 +318,50 @@ __device__ __forceinline__ void invert_off_diag16(float *W, float *Xs, int it)
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) w_t(W, base + 16 + t, base + j0 + e) = -acc[e];
+        if (b == 0) {                              // the block under T's first diagonal block, into Tr
+#pragma unroll
+            for (int e = 0; e < 4; ++e) Tr[(16 + t) * kTS + j0 + e] = -acc[e];
+        }
     }
 }
 
-// The 32 x 32 block by all 256 threads (four outputs each).
-__device__ __forceinline__ void invert_off_diag32(float *W, float *Xs, int tid)
+// The 32 x 32 block by all 256 threads (four outputs each): T11 from Tr and X from Xs four columns
+// at a time.
+__device__ __forceinline__ void invert_off_diag32(float *W, float *Xs, const float *Tr, int tid)
 {
-    {   // X = M21 T11 for the 32 x 32 halves: row t, cols 4 jq .. +3
-        const int t = tid >> 3, j0 = 4 * (tid & 7);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int t = tid >> 3, j0 = 4 * (tid & 7);
+    {   // X = M21 T11 for the 32 x 32 halves: row t, cols j0 .. j0 + 3
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int i = 0; i < 32; ++i) {
             const float a = w_a(W, 32 + t, i);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = fmaf(a, i >= j0 + e ? w_t(W, i, j0 + e) : 0.0f, acc[e]);
+            const float4 tr = *reinterpret_cast<const float4 *>(Tr + i * kTS + j0);
+            acc.x = fmaf(a, tr.x, acc.x);
+            acc.y = fmaf(a, tr.y, acc.y);
+            acc.z = fmaf(a, tr.z, acc.z);
+            acc.w = fmaf(a, tr.w, acc.w);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) Xs[t * kXS + j0 + e] = acc[e];
+        *reinterpret_cast<float4 *>(Xs + t * kXS + j0) = acc;
     }
     __syncthreads();
     {   // T21 = -T22 X
-        const int t = tid >> 3, j0 = 4 * (tid & 7);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int i = 0; i < 32; ++i) {
             const float tv = i <= t ? w_t(W, 32 + t, 32 + i) : 0.0f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = fmaf(tv, Xs[i * kXS + j0 + e], acc[e]);
+            const float4 x = *reinterpret_cast<const float4 *>(Xs + i * kXS + j0);
+            acc.x = fmaf(tv, x.x, acc.x);
+            acc.y = fmaf(tv, x.y, acc.y);
+            acc.z = fmaf(tv, x.z, acc.z);
+            acc.w = fmaf(tv, x.w, acc.w);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) w_t(W, 32 + t, j0 + e) = -acc[e];
+        w_t(W, 32 + t, j0) = -acc.x;
+        w_t(W, 32 + t, j0 + 1) = -acc.y;
+        w_t(W, 32 + t, j0 + 2) = -acc.z;
+        w_t(W, 32 + t, j0 + 3) = -acc.w;
     }
 }
 
-// TMA_O: the outputs leave by one tensor store per chunk (o_map); otherwise by plain stores.
 template <typename TS, bool TMA_O>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_constant__ CUtensorMap o_map)
@@ -350,6 +370,7 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float *W = reinterpret_cast<float *>(smem + kWOff);
     float *Xs = reinterpret_cast<float *>(smem + kXsOff);
+    float *Tr = reinterpret_cast<float *>(smem + kTrOff);
     __shared__ ChunkScalars sc;
     __shared__ __align__(16) float ab[2][2][kC];    // [chunk parity][alpha, beta][t]
     __shared__ uint64_t bars[4];                    // G (2 issuers), Y (1), MMA-2 (3), MMA-3 (2)
@@ -510,13 +531,13 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
                 }
             }
             sync_a_warps();                                // A complete
-            if (hf == 0) invert_diag_blocks(W, (warp & 1) * 32 + lane);
+            if (hf == 0) invert_diag_blocks(W, Tr, (warp & 1) * 32 + lane);
             sync_a_warps();                                // diagonal blocks of T done
-            invert_off_diag16(W, Xs, (warp & 1) * 32 + lane + 64 * hf);
+            invert_off_diag16(W, Xs, Tr, (warp & 1) * 32 + lane + 64 * hf);
             tc::fence_before_sync();
         }
         __syncthreads();                                   // 16 x 16 blocks done; Y's issuer done issuing
-        invert_off_diag32(W, Xs, tid);
+        invert_off_diag32(W, Xs, Tr, tid);
         ok = __syncthreads_and(ok_g && tc::mbar_wait(&bars[1], ph, polls)) != 0;         // T complete, Y done
         tc::fence_after_sync();
         if (!ok) break;
