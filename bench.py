@@ -50,19 +50,19 @@ EPS = 1e-6
 SEED = 0
 REF_LAYERS_PER_STEP = 4      # oracle sample per step of the reference arm
 
-# Per-launch DRAM traffic of the decode kernel from an ncu capture (dram__bytes_read.sum +
+# Per-launch DRAM traffic of a kernel from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), valid only while the kernel source is the one it was taken on.
 NCU_TRAFFIC = {
     # mean of three mid-sequence launches of the full 48-layer workload, ncu --cache-control none
-    # (reads 102.9-103.1 MB, writes 96.4-99.6 MB), from the ncu capture of the batch-32 48-layer decode
-    "decode_norm_f32": {"bytes_per_launch": 201425664,
-                        "src_sha256": "cf5cb0f8aa290eb7f1bbcc53616eba2ec58c3e148f0e1b9c4ffb9d38dc623d74"},
-    # mean of two launches of the 256-slot fp16 pool decode (reads 413.3 MB, writes 388.7-388.8 MB)
-    "decode_norm_f16_pool": {"bytes_per_launch": 802121216,
-                             "src_sha256": "cf5cb0f8aa290eb7f1bbcc53616eba2ec58c3e148f0e1b9c4ffb9d38dc623d74"},
-    # mean of two launches of the batch-32 fp32 decode from projections (reads 105.7-105.9 MB, writes
-    # 102.9-104.4 MB), ncu --cache-control none
-    "conv_norm_f32": {"bytes_per_launch": 209400448, "src": ("gdn_conv_norm.cu", "gdn_internal.cuh"),
+    # (reads 102.9-103.1 MB, writes 96.8-99.4 MB), from the ncu capture of the batch-32 48-layer decode
+    "decode_norm_f32": {"bytes_per_launch": 201543680,
+                        "src_sha256": "72cb5c2362bd7c275f805b49794c715a6a3fe37e4882cab4c501915e6129ad0e"},
+    # mean of two launches of the 256-slot fp16 pool decode (reads 406.9 MB, writes 401.2-402.7 MB)
+    "decode_norm_f16_pool": {"bytes_per_launch": 808839680,
+                             "src_sha256": "72cb5c2362bd7c275f805b49794c715a6a3fe37e4882cab4c501915e6129ad0e"},
+    # mean of two launches of the batch-32 fp32 decode from projections (reads 105.7-105.8 MB, writes
+    # 102.6-104.5 MB), ncu --cache-control none
+    "conv_norm_f32": {"bytes_per_launch": 209314560, "src": ("gdn_conv_norm.cu", "gdn_internal.cuh"),
                       "src_sha256": "e746be9c1348695371dea7fb0e256dab4f590bb665212e633313fa9606b7290e"},
 }
 
