@@ -37,7 +37,9 @@
 // Every MMA operand x is split as x = hi + lo with hi the nearest TF32 value and
 // lo = x - hi (read as TF32 by the tensor core), and a product is taken as
 // hi*hi + hi*lo + lo*hi (three passes), which carries about 21 significant bits
-// per product; the accumulators are fp32 in tensor memory.  The exact fp32
+// per product; k and q take hi = x truncated to TF32 instead (about 19 bits
+// per product: their copies arrive in the operand layout, so only lo is
+// computed); the accumulators are fp32 in tensor memory.  The exact fp32
 // state stays in registers (thread = row a of the head, half of its columns);
 // only its split copy is in tensor memory.
 //
@@ -46,8 +48,11 @@
 // of warps 2, 3 and 6 issue the MMAs (one thread issues one MMA per ~140 cycles
 // whatever its N, and MMAs from several warps proceed together), so each
 // product is split over two or three issuers, each part into its own
-// accumulator.  The next chunk's k, q, alpha and beta are copied into shared
-// memory (cp.async) during the current chunk; the chunk's outputs leave by one
+// accumulator.  The next chunk's k and q arrive during the current chunk by
+// eight TMA tensor copies straight into the 128-byte-swizzled operand layout
+// (their fp32 bits serve as the high TF32 parts: the tensor core reads the top
+// 19 bits, and only the exact low parts x - trunc(x) are computed), alpha and
+// beta by cp.async; the chunk's outputs leave by one
 // tensor store (TMA) of a 32 KB tile, which keeps 32 scalar stores a lane per
 // chunk out of the load/store queue that the next chunk's shared-memory work
 // needs (2.82 -> 2.68 ms at batch 8, T 4096).  The CTA holds all 512
@@ -82,18 +87,20 @@ constexpr int kIss0 = 64, kIss1 = 96, kIss2 = 192;
 constexpr uint32_t kWaitLimit = 1u << 22;    // polls of an mbarrier phase before giving up
 
 // shared memory (1024-aligned), byte offsets
-constexpr uint32_t kKQHi = 0, kKQLo = 65536;           // [K;Q]: 128 rows x 128, until MMA-1 is done
+// [K;Q]: 128 rows x 128, until MMA-1 is done.  kKQHi: as the tensor copy brings it in (during the
+// previous chunk), its fp32 bits the high TF32 parts (the tensor core reads the top 19 bits);
+// kKQLo: the low parts x - trunc_tf32(x), exact
+constexpr uint32_t kKQLo = 0, kKQHi = 131072;
 constexpr uint32_t kTHi = 0, kTLo = 16384;             // T: 64 rows (t) x 64 (i), after MMA-1
 // B operand of MMA-3, 192 rows x 64 (K = t or i): rows 0-127 Ktilde^T (row c), rows 128-191 P (row t)
 constexpr uint32_t kBHi = 32768, kBLo = 81920;
 constexpr int kBRows = 192;
-constexpr uint32_t kStage = 131072;                    // next chunk's raw [K;Q], 128 rows x 512 B
 // fp32 64 x 64 work matrix W (row stride kAS): A in its strict lower triangle, T = (I + A)^-1
 // transposed in its upper triangle and diagonal (T[t][j] at W[j][t]); then a 32 x 36 scratch Xs and
 // Tr, T's top-left 32 x 32 block row-major (zeros above the diagonal), both with 16-byte rows so the
 // 32 x 32 block product reads four consecutive columns in one load
 constexpr int kAS = 65, kXS = 36, kTS = 36;
-constexpr uint32_t kWOff = kStage + 65536, kXsOff = kWOff + kC * kAS * 4, kTrOff = kXsOff + 32 * kXS * 4;
+constexpr uint32_t kWOff = kKQHi + 65536, kXsOff = kWOff + kC * kAS * 4, kTrOff = kXsOff + 32 * kXS * 4;
 // the chunk's outputs o[t][a] (64 x 128 fp32, row-major) for one tensor store, over W and the scratch
 // after them: written in the last phase, read out by the copy engine before the next chunk builds A
 constexpr uint32_t kOStage = kWOff, kOBytes = kC * kD * 4;
@@ -136,10 +143,6 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
-}
-__device__ __forceinline__ void cp_async16_s(uint32_t saddr, const void *gmem)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async4_s(uint32_t saddr, const void *gmem)
 {
@@ -201,22 +204,31 @@ __device__ __forceinline__ bool and_a_warps(bool pred)
     return r != 0;
 }
 
-// Copy chunk [c0, c0 + n) of k, q (raw rows into the staging buffer, row-major)
-// and alpha, beta (into ab[0], ab[1]) with cp.async; padding tokens get k = q =
-// 0, alpha = 1, beta = 0.  Warp w copies rows 16w .. 16w+15 (K rows t, then Q
-// rows), lane l their 16-byte chunk l; the same thread later splits exactly
-// these chunks, so only its own cp.async wait is needed before it reads them.
-__device__ __forceinline__ void prefetch_chunk(uint32_t stage, float (*ab)[kC], const float *kbase, const float *qbase,
-                                               const PrefillParams &p, int seq, int h, int c0, int n, int warp,
-                                               int lane, int tid)
+// Chunk [c0, c0 + 64) of k and q by eight tensor copies (one per 32-column block of each: 64 tokens x
+// 128 bytes with the 128-byte swizzle, the layout the MMAs read) into the [K;Q] tile at `dst`; tokens
+// past the sequence's end read as zeros.  They complete on `bar`, whose transaction count (64 KB) is
+// armed here.  One thread.
+__device__ __forceinline__ void load_kq(const CUtensorMap *kmap, const CUtensorMap *qmap, uint32_t dst, uint64_t *bar,
+                                        int g, int c0, int seq)
 {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i) {
-        const int row = 16 * warp + i, t = row & (kC - 1);
-        const uint32_t dst = stage + row * 512 + lane * 16;
-        if (t < n) cp_async16_s(dst, (row < kC ? kbase : qbase) + (int64_t)(c0 + t) * p.qk_stride + 4 * lane);
-        else st_shared_v4(dst, 0u, 0u, 0u, 0u);
+    const uint32_t b = (uint32_t)__cvta_generic_to_shared(bar);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(65536u) : "memory");
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+            asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                         " [%0], [%1, {%2, %3, %4}], [%5];"
+                         ::"r"(dst + kb * 16384 + m * 8192), "l"(m == 0 ? kmap : qmap), "r"(g * kD + kb * 32),
+                           "r"(c0), "r"(seq), "r"(b) : "memory");
     }
+}
+
+// alpha, beta of chunk [c0, c0 + n) into ab[0], ab[1] with cp.async (threads 0-63); padding tokens get
+// alpha = 1, beta = 0.  Each copier waits for its own copies before the barrier that publishes them.
+__device__ __forceinline__ void prefetch_ab(float (*ab)[kC], const PrefillParams &p, int seq, int h, int c0, int n,
+                                            int tid)
+{
     if (tid < kC) {
         const uint32_t sa = (uint32_t)__cvta_generic_to_shared(&ab[0][tid]);
         const uint32_t sb = (uint32_t)__cvta_generic_to_shared(&ab[1][tid]);
@@ -230,6 +242,12 @@ __device__ __forceinline__ void prefetch_chunk(uint32_t stage, float (*ab)[kC], 
         }
     }
     cp_async_commit();
+}
+
+// The low TF32 part of x: x minus its top 19 bits (exact).
+__device__ __forceinline__ uint32_t tf32_low(uint32_t x)
+{
+    return __float_as_uint(__uint_as_float(x) - __uint_as_float(x & 0xFFFFE000u));
 }
 
 // The chunk's o tile (shared memory, row-major [t][a]) to o[seq][c0 + t][h D + a] by one tensor store
@@ -364,7 +382,8 @@ __device__ __forceinline__ void invert_off_diag32(float *W, float *Xs, const flo
 
 template <typename TS, bool TMA_O>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_constant__ CUtensorMap o_map)
+prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_constant__ CUtensorMap o_map,
+                const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap q_map)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -373,7 +392,7 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
     float *Tr = reinterpret_cast<float *>(smem + kTrOff);
     __shared__ ChunkScalars sc;
     __shared__ __align__(16) float ab[2][2][kC];    // [chunk parity][alpha, beta][t]
-    __shared__ uint64_t bars[4];                    // G (2 issuers), Y (1), MMA-2 (3), MMA-3 (2)
+    __shared__ uint64_t bars[5];                    // G (2 issuers), Y (1), MMA-2 (3), MMA-3 (2), [K;Q] copies
     __shared__ uint32_t tmem_base;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -387,23 +406,25 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
     const int T = p.seq_len;
     const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
 
-    const float *kbase = p.k + (int64_t)seq * T * p.qk_stride + (int64_t)g * kD;
-    const float *qbase = p.q + (int64_t)seq * T * p.qk_stride + (int64_t)g * kD;
     const float *vbase = p.v + (int64_t)seq * T * p.v_stride + (int64_t)h * kD;
     float *obase = p.o + (int64_t)seq * T * p.o_stride + (int64_t)h * kD;
 
-    prefetch_chunk(sbase + kStage, ab[0], kbase, qbase, p, seq, h, 0, min(kC, T), warp, lane, tid);
+    prefetch_ab(ab[0], p, seq, h, 0, min(kC, T), tid);
     if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
     if (tid == 0) {
         tc::mbar_init(&bars[0], 2);
         tc::mbar_init(&bars[1], 1);
         tc::mbar_init(&bars[2], 3);
         tc::mbar_init(&bars[3], 2);
+        tc::mbar_init(&bars[4], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if (tid == 0) load_kq(&k_map, &q_map, sbase + kKQHi, &bars[4], g, 0, seq);
+    uint32_t kq_ph = 0;                             // parity of the [K;Q] copies' phase being awaited
+    bool kq_pend = true;                            // copies in flight not yet seen complete
     const uint32_t tm = tmem_base + lanebase;       // this warp's lanes
     uint32_t ph = 0;                                // parity of this chunk's phase of each barrier
 
@@ -427,20 +448,43 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
             tc::tmem_st32(tm + kSHi + 64 * hf + 32 * cb, hi);
             tc::tmem_st32(tm + kSLo + 64 * hf + 32 * cb, lo);
         }
-        // ---- 1. this thread's staged [K;Q] chunks, split into the operand buffer ----
-        cp_async_wait<0>();
+        // ---- 1. the low parts of the [K;Q] tile (the tensor copies brought the high parts) ----
+        const bool okk = tc::mbar_wait(&bars[4], kq_ph, polls);
+        cp_async_wait<0>();                                // this thread's alpha, beta copies
 #pragma unroll 2
         for (int i = 0; i < 16; ++i) {
-            const int row = 16 * warp + i;
-            const uint4 x = ld_shared_v4(sbase + kStage + row * 512 + lane * 16);
-            const uint32_t off = tc::sw128_offset(row, 4 * lane, 128);
-            st_split4(sbase + kKQHi + off, sbase + kKQLo + off, __uint_as_float(x.x), __uint_as_float(x.y),
-                      __uint_as_float(x.z), __uint_as_float(x.w));
+            const uint32_t off = tc::sw128_offset(16 * warp + i, 4 * lane, 128);
+            const uint4 x = ld_shared_v4(sbase + kKQHi + off);
+            st_shared_v4(sbase + kKQLo + off, tf32_low(x.x), tf32_low(x.y), tf32_low(x.z), tf32_low(x.w));
         }
         tc::st_wait();                                     // the split state is in tensor memory
-        __syncthreads();                                   // alpha, beta landed (their copiers waited)
-        if (warp < 3) {   // products of the decays: gamma (prefix), rho(C-1, .) (suffix), sigma (prefix from 32)
-            if (warp == 2) {
+        if (TMA_O && tid == 0) o_tile_read_done();        // the last chunk's o tile is out of W's space
+        // ---- MMA-1: G = [K;Q] K^T (two issuers, bars[0]) and Y = S [K;Q]^T (one issuer, bars[1]) ----
+        tc::fence_smem_async();
+        tc::fence_before_sync();
+        ok = __syncthreads_and(okk) != 0;                  // [K;Q] and alpha, beta complete
+        tc::fence_after_sync();
+        if (!ok) break;
+        kq_pend = false;
+        kq_ph ^= 1u;
+        if (tid == kIss0 || tid == kIss2) {       // G over the first / second half of K
+            const bool first = tid == kIss0;
+            mma_passes<false>(tmem_base + (first ? kG : kGb), sbase + kKQHi, sbase + kKQLo, sbase + kKQHi,
+                              sbase + kKQLo, 128 * 128, 128 * 128, first ? 0 : kD / 16, first ? kD / 16 : kD / 8,
+                              tc::idesc_tf32(128, 64), 0, 3);
+            tc::mma_commit(&bars[0]);
+        } else if (tid == kIss1) {
+            mma_passes<true>(tmem_base + kY, tmem_base + kSHi, tmem_base + kSLo, sbase + kKQHi, sbase + kKQLo,
+                             0, 128 * 128, 0, kD / 8, tc::idesc_tf32(128, 128), 0, 3);
+            tc::mma_commit(&bars[1]);
+        }
+        __syncwarp();
+        pend = 0x3u;
+        // products of the decays, by warps that build A (they wait for G next): gamma (prefix),
+        // rho(C-1, .) (suffix), sigma (prefix from 32); published by the A warps' barrier and the full
+        // barriers after
+        if (warp == 0 || warp == 1 || warp == 5) {
+            if (warp == 5) {
                 float pr = alpha[32 + lane];
 #pragma unroll
                 for (int d = 1; d < 32; d <<= 1) {
@@ -476,26 +520,9 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
             }
         }
 
-        // ---- MMA-1: G = [K;Q] K^T (two issuers, bars[0]) and Y = S [K;Q]^T (one issuer, bars[1]) ----
-        if (TMA_O && tid == 0) o_tile_read_done();        // the last chunk's o tile is out of W's space
-        sync_for_mma();
-        if (tid == kIss0 || tid == kIss2) {       // G over the first / second half of K
-            const bool first = tid == kIss0;
-            mma_passes<false>(tmem_base + (first ? kG : kGb), sbase + kKQHi, sbase + kKQLo, sbase + kKQHi,
-                              sbase + kKQLo, 128 * 128, 128 * 128, first ? 0 : kD / 16, first ? kD / 16 : kD / 8,
-                              tc::idesc_tf32(128, 64), 0, 3);
-            tc::mma_commit(&bars[0]);
-        } else if (tid == kIss1) {
-            mma_passes<true>(tmem_base + kY, tmem_base + kSHi, tmem_base + kSLo, sbase + kKQHi, sbase + kKQLo,
-                             0, 128 * 128, 0, kD / 8, tc::idesc_tf32(128, 128), 0, 3);
-            tc::mma_commit(&bars[1]);
-        }
-        __syncwarp();
-        pend = 0x3u;
-        // the next chunk's inputs on their way while this one is computed
-        if (c0 + kC < T)
-            prefetch_chunk(sbase + kStage, ab[par ^ 1], kbase, qbase, p, seq, h, c0 + kC, min(kC, T - c0 - kC),
-                           warp, lane, tid);
+        // the next chunk's alpha, beta on their way while this one is computed (k and q follow once
+        // MMA-1 and the k reads below are done with the tile)
+        if (c0 + kC < T) prefetch_ab(ab[par ^ 1], p, seq, h, c0 + kC, min(kC, T - c0 - kC), tid);
         // v_t[a] for t = 32 hf + j, a = r (coalesced across the warp's lanes)
         float vv[32];
 #pragma unroll
@@ -542,7 +569,8 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
         tc::fence_after_sync();
         if (!ok) break;
         pend = 0;
-        // k_t[c] = hi + lo (exact) from the operand buffer before T overwrites it; t = 32 hf + j, c = r
+        // k_t[c] (exact: the copied fp32 value) from the tile before the next chunk's copies overwrite it;
+        // t = 32 hf + j, c = r
         float kv[32];
         {   // element (row 32 hf + j, column r) of the 128-row K-major tile: a row step is 128 bytes and
             // the 16-byte chunk is XOR-ed with the row's low three bits
@@ -551,10 +579,14 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const uint32_t a = base + j * 128 + ((chunk ^ (uint32_t)(j & 7)) << 4);
-                kv[j] = ld_shared_f32(a) + ld_shared_f32(a + (kKQLo - kKQHi));
+                kv[j] = ld_shared_f32(a);                  // the copied fp32 value itself
             }
         }
         __syncthreads();
+        if (c0 + kC < T) {                                 // MMA-1 and the k reads are done with the tile
+            if (tid == 0) load_kq(&k_map, &q_map, sbase + kKQHi, &bars[4], g, c0 + kC, seq);
+            kq_pend = true;
+        }
 
         // ---- 2b. operands of MMA-2 and MMA-3: T, P, Ktilde^T to shared memory, R^T to tensor memory ----
         {   // T: row t = tid / 4, columns 16 (tid % 4) .. +15 (zero above the diagonal)
@@ -720,11 +752,12 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
     cp_async_wait<0>();                                    // no copy left in flight
     if (TMA_O && tid == 0) o_tile_done();
     if (!ok) {
-        // a wait gave up: let the MMAs still in flight finish (again bounded) before the tensor memory
-        // they write is freed; count the event; the state of this head becomes NaN
+        // a wait gave up: let the MMAs and tensor copies still in flight finish (again bounded) before
+        // the memory they write is freed; count the event; the state of this head becomes NaN
 #pragma unroll 1
         for (int i = 0; i < 4; ++i)
             if (pend & (1u << i)) tc::mbar_wait(&bars[i], ph, kWaitLimit);
+        if (kq_pend) tc::mbar_wait(&bars[4], kq_ph, kWaitLimit);
         if (tid == 0) atomicAdd(&g_tc_wait_timeouts, 1u);
 #pragma unroll
         for (int j = 0; j < 64; ++j) S[j] = __int_as_float(0x7fc00000);
@@ -773,22 +806,40 @@ bool o_tensor_map(const PrefillParams &p, CUtensorMap *map)
            CUDA_SUCCESS;
 }
 
+// The 3-D map of k or q for the chunk copies: (column < NK D, token < T, sequence < batch), box 32 x 64
+// x 1 (128 bytes x 64 tokens) with the 128-byte swizzle; tokens past T read as zeros.  The caller
+// guarantees a 16-byte aligned base and row pitch.
+bool kq_tensor_map(const PrefillParams &p, const float *base, CUtensorMap *map)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)p.nk * kD, (cuuint64_t)p.seq_len, (cuuint64_t)p.batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)p.qk_stride * 4, (cuuint64_t)p.qk_stride * 4 * (cuuint64_t)p.seq_len};
+    const cuuint32_t box[3] = {32, (cuuint32_t)kC, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename TS, bool TMA_O>
-cudaError_t launch_kernel(const PrefillParams &p, const CUtensorMap &map, cudaStream_t s)
+cudaError_t launch_kernel(const PrefillParams &p, const CUtensorMap &omap, const CUtensorMap &kmap,
+                          const CUtensorMap &qmap, cudaStream_t s)
 {
     constexpr auto kern = prefill_tc_d128<TS, TMA_O>;
     const cudaError_t e = allow_dynamic_smem<kern>((int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)((int64_t)p.batch * p.nv), kThreads, kSmemBytes, s>>>(p, g_wait_polls.load(), map);
+    kern<<<(unsigned)((int64_t)p.batch * p.nv), kThreads, kSmemBytes, s>>>(p, g_wait_polls.load(), omap, kmap, qmap);
     return cudaGetLastError();
 }
 
 template <typename TS>
 cudaError_t launch_typed(const PrefillParams &p, cudaStream_t s)
 {
-    CUtensorMap map{};
-    if (o_tensor_map(p, &map)) return launch_kernel<TS, true>(p, map, s);
-    return launch_kernel<TS, false>(p, map, s);
+    CUtensorMap kmap{}, qmap{}, omap{};
+    if (!kq_tensor_map(p, p.k, &kmap) || !kq_tensor_map(p, p.q, &qmap)) return cudaErrorNotSupported;
+    if (o_tensor_map(p, &omap)) return launch_kernel<TS, true>(p, omap, kmap, qmap, s);
+    return launch_kernel<TS, false>(p, omap, kmap, qmap, s);
 }
 
 }  // namespace
