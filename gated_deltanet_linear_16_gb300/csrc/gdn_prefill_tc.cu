@@ -275,7 +275,7 @@ __device__ __forceinline__ void sync_a_warps() { asm volatile("bar.sync 1, 128;"
 // the blocks under the diagonal from [[M11, 0], [M21, M22]]^-1 = [[T11, 0],
 // [-T22 M21 T11, T22]]: the two 16 x 16 ones by the 128 threads that built A
 // (invert_off_diag16, before Y's issuing warp is free), then the 32 x 32 one by
-// all 256 threads (invert_off_diag32).  Xs: 32 x 36 scratch; Tr: row-major copy of T[0..31][0..31].
+// four warps (invert_off_diag32).  Xs: 32 x 36 scratch; Tr: row-major copy of T[0..31][0..31].
 __device__ __forceinline__ float w_a(const float *W, int t, int i) { return W[t * kAS + i]; }
 __device__ __forceinline__ float &w_t(float *W, int t, int j) { return W[j * kAS + t]; }
 
@@ -343,40 +343,56 @@ __device__ __forceinline__ void invert_off_diag16(float *W, float *Xs, float *Tr
     }
 }
 
-// The 32 x 32 block by all 256 threads (four outputs each): T11 from Tr and X from Xs four columns
-// at a time.
+// The 32 x 32 block by the 128 threads of warps 0-3 (named barrier 2), a 2 x 4 block of outputs each
+// (rows 2 ti, 2 ti + 1, columns 4 tj .. +3): per step along the inner dimension two scalar loads and
+// one 16-byte load feed 8 FMAs.  Shared-memory wavefronts bound this product (a 16-byte load costs
+// four), so larger blocks on fewer warps beat four outputs on all eight.  T11 from Tr, X through Xs.
 __device__ __forceinline__ void invert_off_diag32(float *W, float *Xs, const float *Tr, int tid)
 {
-    const int t = tid >> 3, j0 = 4 * (tid & 7);
-    {   // X = M21 T11 for the 32 x 32 halves: row t, cols j0 .. j0 + 3
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int ti = tid >> 3, tj = tid & 7, t0 = 2 * ti, j0 = 4 * tj;
+    {   // X = M21 T11: rows t0, t0+1, cols j0 .. j0+3
+        float4 acc[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int i = 0; i < 32; ++i) {
-            const float a = w_a(W, 32 + t, i);
             const float4 tr = *reinterpret_cast<const float4 *>(Tr + i * kTS + j0);
-            acc.x = fmaf(a, tr.x, acc.x);
-            acc.y = fmaf(a, tr.y, acc.y);
-            acc.z = fmaf(a, tr.z, acc.z);
-            acc.w = fmaf(a, tr.w, acc.w);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float a = w_a(W, 32 + t0 + k, i);
+                acc[k].x = fmaf(a, tr.x, acc[k].x);
+                acc[k].y = fmaf(a, tr.y, acc[k].y);
+                acc[k].z = fmaf(a, tr.z, acc[k].z);
+                acc[k].w = fmaf(a, tr.w, acc[k].w);
+            }
         }
-        *reinterpret_cast<float4 *>(Xs + t * kXS + j0) = acc;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) *reinterpret_cast<float4 *>(Xs + (t0 + k) * kXS + j0) = acc[k];
     }
-    __syncthreads();
-    {   // T21 = -T22 X
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+    {   // T21 = -T22 X (T22 lower triangular: zero for i > t)
+        float4 acc[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int i = 0; i < 32; ++i) {
-            const float tv = i <= t ? w_t(W, 32 + t, 32 + i) : 0.0f;
             const float4 x = *reinterpret_cast<const float4 *>(Xs + i * kXS + j0);
-            acc.x = fmaf(tv, x.x, acc.x);
-            acc.y = fmaf(tv, x.y, acc.y);
-            acc.z = fmaf(tv, x.z, acc.z);
-            acc.w = fmaf(tv, x.w, acc.w);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float tv = i <= t0 + k ? w_t(W, 32 + t0 + k, 32 + i) : 0.0f;
+                acc[k].x = fmaf(tv, x.x, acc[k].x);
+                acc[k].y = fmaf(tv, x.y, acc[k].y);
+                acc[k].z = fmaf(tv, x.z, acc[k].z);
+                acc[k].w = fmaf(tv, x.w, acc[k].w);
+            }
         }
-        w_t(W, 32 + t, j0) = -acc.x;
-        w_t(W, 32 + t, j0 + 1) = -acc.y;
-        w_t(W, 32 + t, j0 + 2) = -acc.z;
-        w_t(W, 32 + t, j0 + 3) = -acc.w;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            w_t(W, 32 + t0 + k, j0) = -acc[k].x;
+            w_t(W, 32 + t0 + k, j0 + 1) = -acc[k].y;
+            w_t(W, 32 + t0 + k, j0 + 2) = -acc[k].z;
+            w_t(W, 32 + t0 + k, j0 + 3) = -acc[k].w;
+        }
     }
 }
 
@@ -564,7 +580,7 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
             tc::fence_before_sync();
         }
         __syncthreads();                                   // 16 x 16 blocks done; Y's issuer done issuing
-        invert_off_diag32(W, Xs, Tr, tid);
+        if (warp < 4) invert_off_diag32(W, Xs, Tr, tid);
         ok = __syncthreads_and(ok_g && tc::mbar_wait(&bars[1], ph, polls)) != 0;         // T complete, Y done
         tc::fence_after_sync();
         if (!ok) break;

@@ -47,6 +47,11 @@ def test_o_row_padding(pad):
     check(run_prefill_case(3, 2, 3, 128, 150, seed=416 + pad[3], init="normal", pad=pad, chunked=True))
 
 
+def test_v_rows_of_any_pitch():
+    """v rows padded by one float (rows not 16-byte aligned): v is read by plain loads either way."""
+    check(run_prefill_case(2, 2, 3, 128, 70, seed=417, init="normal", pad=(0, 1, 0, 0), chunked=True))
+
+
 def test_long_sequence():
     check(run_prefill_case(1, 2, 4, 128, 1000, seed=411, init="normal", chunked=True))
 
