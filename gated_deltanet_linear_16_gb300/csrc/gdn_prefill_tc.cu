@@ -21,18 +21,20 @@
 // the same arithmetic in real numbers (the chunked "WY" form of the delta
 // rule); only the fp32 rounding differs.  Per chunk and head, in order:
 //
-//   SIMT   the state, split, into TMEM; the chunk's [K;Q] (prefetched), split,
-//          into shared memory; gamma, rho(C,.) by warp scans
+//   SIMT   the state, split, into TMEM; the low parts of the chunk's [K;Q] tile
+//          (the tile itself arrived by tensor copies) into shared memory
 //   MMA-1  G = [K;Q] K^T (128 x 64, two issuers over the halves of K) and
 //          Y = S [K;Q]^T (128 x 128, S from TMEM, one issuer)
-//   SIMT   A from G (warps 0, 1, 4, 5, while Y runs); T = (I + A)^-1 (16 x 16
-//          diagonal blocks, then block products); P from G; R^T = beta (v -
-//          gamma Y_K) into TMEM; T, P, Ktilde^T into shared memory
+//   SIMT   gamma, rho(C,.) by warp scans; A from G (warps 0, 1, 4, 5, while Y
+//          runs); T = (I + A)^-1 (16 x 16 diagonal blocks, then block
+//          products); P from G; R^T = beta (v - gamma Y_K) into TMEM; T, P,
+//          Ktilde^T into shared memory
 //   MMA-2  Delta^T = R^T T^T (128 x 64, one issuer and accumulator per pass)
 //   SIMT   Delta^T = sum of the passes, split into TMEM
 //   MMA-3  [Z | (P Delta)^T] = Delta^T [Ktilde | P^T] (128 x 192, two issuers
 //          over the halves of K)
-//   SIMT   o_t = (gamma_t Y_Q + P Delta) / sqrt(D);  S <- gamma_C S + Z (fp32)
+//   SIMT   o_t = (gamma_t Y_Q + P Delta) / sqrt(D) into a shared-memory tile
+//          written out by one tensor store;  S <- gamma_C S + Z (fp32)
 //
 // Every MMA operand x is split as x = hi + lo with hi the nearest TF32 value and
 // lo = x - hi (read as TF32 by the tensor core), and a product is taken as
@@ -45,24 +47,27 @@
 //
 // One CTA (8 warps) per (sequence, value head); warp w owns tensor-memory lanes
 // 32*(w%4).. (rows of the state) and half w/4 of the columns it loads.  Lane 0
-// of warps 2, 3 and 6 issue the MMAs (one thread issues one MMA per ~140 cycles
-// whatever its N, and MMAs from several warps proceed together), so each
-// product is split over two or three issuers, each part into its own
-// accumulator.  The next chunk's k and q arrive during the current chunk by
+// of warps 2, 3 and 6 issue the MMAs (one thread issues one MMA per ~120-140
+// cycles whatever its N, and MMAs from several threads proceed together), so
+// each product is split over two or three issuers, each part into its own
+// accumulator (tensor memory, all 512 columns in use during MMA-1, keeps Y on
+// one issuer).  The next chunk's k and q arrive during the current chunk by
 // eight TMA tensor copies straight into the 128-byte-swizzled operand layout
 // (their fp32 bits serve as the high TF32 parts: the tensor core reads the top
 // 19 bits, and only the exact low parts x - trunc(x) are computed), alpha and
-// beta by cp.async; the chunk's outputs leave by one
-// tensor store (TMA) of a 32 KB tile, which keeps 32 scalar stores a lane per
-// chunk out of the load/store queue that the next chunk's shared-memory work
-// needs (2.82 -> 2.68 ms at batch 8, T 4096).  The CTA holds all 512
-// tensor-memory columns and ~218 KB of shared memory, so an SM runs one such
-// CTA at a time.  Loops stay rolled where they can: the chunk body runs once
-// per chunk on few warps, so instruction fetch is a cost.  The only waits are
-// on the CTA's own MMA completions (mbarriers armed by tcgen05.commit), each
-// bounded: if a bound ran out (or was set to 0 to test this path), the CTA
-// stops, lets the MMAs it issued finish (again bounded), counts the event in
-// g_tc_wait_timeouts and writes NaN to its state.
+// beta by cp.async; the chunk's outputs leave by one tensor store (TMA) of a
+// 32 KB tile.  Both keep per-lane global accesses out of the load/store queue
+// that the chunk's shared-memory work needs (2.82 -> 2.46 ms at batch 8, T
+// 4096); v keeps plain loads (in shared memory its reads cost wavefronts of
+// the pipe the SIMT phases are bound by).  The CTA holds all 512 tensor-memory
+// columns and ~230 KB of shared memory, so an SM runs one such CTA at a time.
+// Loops stay rolled where they can: the chunk body runs once per chunk, so
+// instruction fetch is a cost.  The only waits are on the CTA's own MMA and
+// tensor-copy completions (mbarriers armed by tcgen05.commit or by the
+// copies' transaction counts), each bounded: if a bound ran out (or was set to
+// 0 to test this path), the CTA stops, lets the MMAs and copies it issued
+// finish (again bounded), counts the event in g_tc_wait_timeouts and writes NaN
+// to its state.
 #include <atomic>
 
 #include <cuda.h>

@@ -80,8 +80,8 @@ extern "C" {
 #define GDN_ERR_CUDA 5         /* the CUDA launch failed (see gdn_last_cuda_error) */
 /* There is no timeout status: no kernel of the library waits on a flag, a
  * counter or another block (only on its own barriers, copy groups and, in
- * gdn_prefill_chunked, the completion of its own MMAs, a bounded wait counted
- * by gdn_device_wait_timeouts).  A
+ * gdn_prefill_chunked, the completion of its own MMAs and tensor copies,
+ * bounded waits counted by gdn_device_wait_timeouts).  A
  * base, stride or pitch that rules out the 16-byte vector kernels is not an
  * error either: the general kernel runs instead (GDN_ERR_ALIGN is only for a
  * pointer not aligned to its own element size). */
@@ -349,13 +349,14 @@ GDN_API int gdn_prefill_seq(void *state, gdn_state_dtype state_dtype, int64_t st
  *   rho(t,i) q_t.k_i delta_i) / sqrt(D); at the chunk's end S <- gamma_C S +
  *   sum_t rho(C,t) delta_t k_t^T.  Equal to the token loop in exact
  *   arithmetic; in floating point every product is taken from operands split
- *   into two TF32 parts (three MMAs, about 22 significant bits), accumulated
- *   in fp32, and the state itself is carried in fp32.
+ *   into two TF32 parts (three MMAs: about 22 significant bits, 20 where k or
+ *   q is an operand), accumulated in fp32, and the state itself is carried
+ *   in fp32.
  *   Taken for D == 128 with k and q rows 16-byte aligned (base and stride);
  *   any other call runs gdn_prefill_seq's kernels.  Arguments, layouts,
  *   results (up to fp32 rounding) and errors as gdn_prefill_seq.
- *   The kernel's only waits are on the completion of its own MMAs, each
- *   bounded; see gdn_device_wait_timeouts.
+ *   The kernel's only waits are on the completion of its own MMAs and of its
+ *   own tensor copies (k, q), each bounded; see gdn_device_wait_timeouts.
  */
 GDN_API int gdn_prefill_chunked(void *state, gdn_state_dtype state_dtype, int64_t state_pitch,
                                 const float *q, const float *k, const float *v,
@@ -367,9 +368,9 @@ GDN_API int gdn_prefill_chunked(void *state, gdn_state_dtype state_dtype, int64_
 /*
  * gdn_device_wait_timeouts -- how many times, on the current device since
  * the library was loaded, a tensor-core kernel's bounded wait for its own
- * MMAs ran out (the kernel then stops and writes NaN to its state; 0 in every
- * healthy run).  Synchronises the current device first.  No counterpart on
- * the source pages: a health check of this library's kernels.
+ * MMAs or tensor copies ran out (the kernel then stops and writes NaN to its
+ * state; 0 in every healthy run).  Synchronises the current device first.  No
+ * counterpart on the source pages: a health check of this library's kernels.
  *   count        host pointer, written.
  *   Errors: GDN_ERR_ARG (count NULL), GDN_ERR_CUDA.
  */
@@ -377,12 +378,12 @@ GDN_API int gdn_device_wait_timeouts(unsigned *count);
 
 /*
  * gdn_set_wait_polls -- how many times a tensor-core kernel launched after
- * this call polls for the completion of its own MMAs before it gives up
- * (default GDN_DEFAULT_WAIT_POLLS, a second or more).  0 makes every such
- * wait give up at once: the kernel then lets the MMAs it issued finish
- * (bounded by the default), writes NaN to its state, counts the event for
- * gdn_device_wait_timeouts and returns, so the timeout path can be tested
- * without any fault and the context stays usable.  Process-wide; calls that
+ * this call polls for the completion of its own MMAs or tensor copies before
+ * it gives up (default GDN_DEFAULT_WAIT_POLLS, a second or more).  0 makes
+ * every such wait give up at once: the kernel then lets the MMAs and copies
+ * it issued finish (bounded by the default), writes NaN to its state, counts
+ * the event for gdn_device_wait_timeouts and returns, so the timeout path can
+ * be tested without any fault and the context stays usable.  Process-wide; calls that
  * are already launched keep their value.  No counterpart on the source
  * pages.
  */

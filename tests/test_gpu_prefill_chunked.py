@@ -108,9 +108,9 @@ def test_matches_token_kernel_closely():
 
 
 def test_wait_timeout_path_reports_and_leaves_the_context_usable():
-    """With the poll bound at 0 every CTA's first MMA wait gives up at once: the kernel drains its
-    MMAs, writes NaN to its state and counts one event per CTA; nothing faults, and with the default
-    bound restored the next call is correct again."""
+    """With the poll bound at 0 every CTA's first wait (for its k, q tensor copies) gives up at once:
+    the kernel lets its copies finish, writes NaN to its state and counts one event per CTA; nothing
+    faults, and with the default bound restored the next call is correct again."""
     B, NK, NV, D, T = 1, 2, 3, 128, 70
     before = gdn.gdn_device_wait_timeouts()
     dev = torch.device("cuda")
