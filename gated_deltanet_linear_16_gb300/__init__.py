@@ -23,7 +23,8 @@ __all__ = [
     "GdnError", "load", "build", "library_path",
     "GDN_STATE_F32", "GDN_STATE_F16", "STATUS",
     "gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
-    "gdn_prefill_chunked", "gdn_device_wait_timeouts", "gdn_set_wait_polls", "GDN_DEFAULT_WAIT_POLLS",
+    "gdn_prefill_chunked", "gdn_device_wait_timeouts", "gdn_set_wait_polls", "gdn_set_mma_wait_polls",
+    "GDN_DEFAULT_WAIT_POLLS",
     "gdn_decode_conv_norm_noalloc", "GDN_NOALLOC_MAX_KEY_HEADS", "gdn_decode_norm_q8",
     "gdn_gate_norm", "gdn_gate_norm_q8",
     "gdn_h_f32_to_f16", "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error",
@@ -79,6 +80,8 @@ def _declare(lib):
     lib.gdn_device_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.gdn_set_wait_polls.argtypes = [ctypes.c_uint]
     lib.gdn_set_wait_polls.restype = None
+    lib.gdn_set_mma_wait_polls.argtypes = [ctypes.c_uint]
+    lib.gdn_set_mma_wait_polls.restype = None
     lib.gdn_h_f32_to_f16.argtypes = [P, P, u64, P]
     lib.gdn_h_f16_to_f32.argtypes = [P, P, u64, P]
     for fn in ("gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm", "gdn_prefill_seq",
@@ -326,8 +329,14 @@ def gdn_prefill_chunked(state, q, k, v, alpha, beta, o, **kw):
 
 
 def gdn_set_wait_polls(polls: int) -> None:
-    """Polls of an MMA completion before a tensor-core kernel gives up (0: at once, to test that path)."""
+    """Polls of an MMA or tensor-copy completion before a tensor-core kernel gives up (0: at once, to
+    test that path)."""
     load().gdn_set_wait_polls(polls)
+
+
+def gdn_set_mma_wait_polls(polls: int) -> None:
+    """As gdn_set_wait_polls for the MMA waits only (the tensor-copy waits keep their bound)."""
+    load().gdn_set_mma_wait_polls(polls)
 
 
 def gdn_device_wait_timeouts() -> int:

@@ -482,6 +482,8 @@ GDN_API int gdn_device_wait_timeouts(unsigned *count)
 
 GDN_API void gdn_set_wait_polls(unsigned polls) { tc_set_wait_polls(polls); }
 
+GDN_API void gdn_set_mma_wait_polls(unsigned polls) { tc_set_mma_wait_polls(polls); }
+
 GDN_API int gdn_gate_norm(const float *o, const float *z, const float *gn, float eps, uint16_t *out,
                           int64_t rows, int nv, int d, int64_t o_stride, int64_t z_stride,
                           int64_t out_stride, void *stream)

@@ -403,7 +403,8 @@ __device__ __forceinline__ void invert_off_diag32(float *W, float *Xs, const flo
 
 template <typename TS, bool TMA_O>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_constant__ CUtensorMap o_map,
+prefill_tc_d128(const PrefillParams p, const uint32_t polls, const uint32_t copy_polls,
+                const __grid_constant__ CUtensorMap o_map,
                 const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap q_map)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -470,7 +471,7 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
             tc::tmem_st32(tm + kSLo + 64 * hf + 32 * cb, lo);
         }
         // ---- 1. the low parts of the [K;Q] tile (the tensor copies brought the high parts) ----
-        const bool okk = tc::mbar_wait(&bars[4], kq_ph, polls);
+        const bool okk = tc::mbar_wait(&bars[4], kq_ph, copy_polls);
         cp_async_wait<0>();                                // this thread's alpha, beta copies
 #pragma unroll 2
         for (int i = 0; i < 16; ++i) {
@@ -793,7 +794,8 @@ prefill_tc_d128(const PrefillParams p, const uint32_t polls, const __grid_consta
     }
 }
 
-std::atomic<uint32_t> g_wait_polls{kWaitLimit};
+std::atomic<uint32_t> g_wait_polls{kWaitLimit};        // the MMA waits' bound
+std::atomic<uint32_t> g_copy_wait_polls{kWaitLimit};   // the tensor-copy waits' bound
 
 // cuTensorMapEncodeTiled from the driver (through the runtime's entry-point query, so the library
 // needs no link to the driver library); null if unavailable.
@@ -850,7 +852,8 @@ cudaError_t launch_kernel(const PrefillParams &p, const CUtensorMap &omap, const
     constexpr auto kern = prefill_tc_d128<TS, TMA_O>;
     const cudaError_t e = allow_dynamic_smem<kern>((int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)((int64_t)p.batch * p.nv), kThreads, kSmemBytes, s>>>(p, g_wait_polls.load(), omap, kmap, qmap);
+    kern<<<(unsigned)((int64_t)p.batch * p.nv), kThreads, kSmemBytes, s>>>(p, g_wait_polls.load(), g_copy_wait_polls.load(), omap,
+                                                                          kmap, qmap);
     return cudaGetLastError();
 }
 
@@ -870,7 +873,13 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, bool f16_state, cudaStream
     return f16_state ? launch_typed<__half>(p, s) : launch_typed<float>(p, s);
 }
 
-void tc_set_wait_polls(uint32_t polls) { g_wait_polls.store(polls); }
+void tc_set_wait_polls(uint32_t polls)
+{
+    g_wait_polls.store(polls);
+    g_copy_wait_polls.store(polls);
+}
+
+void tc_set_mma_wait_polls(uint32_t polls) { g_wait_polls.store(polls); }
 
 cudaError_t tc_wait_timeouts(unsigned *count)
 {

@@ -195,5 +195,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, bool f16_state, cudaStream
 cudaError_t tc_wait_timeouts(unsigned *count);
 // Polls of an MMA completion before a tensor-core kernel launched after this call gives up.
 void tc_set_wait_polls(uint32_t polls);
+// The bound of the MMA waits alone (the tensor-copy waits keep theirs).
+void tc_set_mma_wait_polls(uint32_t polls);
 
 }  // namespace gdn

@@ -391,6 +391,15 @@ GDN_API int gdn_device_wait_timeouts(unsigned *count);
 GDN_API void gdn_set_wait_polls(unsigned polls);
 
 /*
+ * gdn_set_mma_wait_polls -- as gdn_set_wait_polls for the waits on the
+ * kernel's own MMAs only; the waits on its tensor copies keep their bound.
+ * With 0 here (and the copies' default) the first wait to give up is one for
+ * MMAs in flight, so that path can be tested apart from the copies'.  No
+ * counterpart on the source pages.
+ */
+GDN_API void gdn_set_mma_wait_polls(unsigned polls);
+
+/*
  * gdn_h_f32_to_f16 -- n h-state elements binary32 -> binary16, round to
  * nearest, ties to even (overflow to +-inf, subnormals kept, NaN stays NaN).
  *   Defined by: ssm_gdn_a.rs, launcher `ssm_h_state_f32_to_f16`.

@@ -43,6 +43,7 @@ def test_exports_match_header(built):
     assert want == sorted(["gdn_decode", "gdn_decode_norm", "gdn_decode_chunk2", "gdn_decode_conv_norm",
                            "gdn_decode_conv_norm_noalloc", "gdn_decode_norm_q8", "gdn_gate_norm",
                            "gdn_gate_norm_q8", "gdn_prefill_seq", "gdn_prefill_chunked", "gdn_device_wait_timeouts", "gdn_set_wait_polls",
+                           "gdn_set_mma_wait_polls",
                            "gdn_h_f32_to_f16",
                            "gdn_h_f16_to_f32", "gdn_status_str", "gdn_last_cuda_error"])
     out = subprocess.run(["nm", "-D", "--defined-only", gdn.library_path()], capture_output=True, text=True,

@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 def _lib(request, cuda_lib):
     before = gdn.gdn_device_wait_timeouts()
     yield cuda_lib
-    if "timeout_path" not in request.node.name:
+    if "timeout_path" not in request.node.name:         # the two give-up tests count their own events
         assert gdn.gdn_device_wait_timeouts() == before, "a bounded MMA wait ran out"
 
 
@@ -130,5 +130,33 @@ def test_wait_timeout_path_reports_and_leaves_the_context_usable():
     assert gdn.gdn_device_wait_timeouts() == before + B * NV
     assert torch.isnan(S).all().item()
     r = run_prefill_case(2, 2, 3, 128, 65, seed=450, init="normal", chunked=True)
+    check(r)
+    assert gdn.gdn_device_wait_timeouts() == before + B * NV
+
+
+def test_mma_wait_timeout_path_drains_the_mmas_in_flight():
+    """With only the MMA waits bounded at 0 the k, q copies are awaited normally and the first wait to
+    give up is the one for G (MMA-1's G and Y in flight): the kernel lets them finish before it frees
+    tensor memory, writes NaN to its state and counts one event per CTA; nothing faults, and with the
+    default bound restored the next call is correct again."""
+    B, NK, NV, D, T = 1, 2, 3, 128, 70
+    before = gdn.gdn_device_wait_timeouts()
+    dev = torch.device("cuda")
+    S = torch.zeros((B, NV, D, D), device=dev)
+    q = torch.nn.functional.normalize(torch.randn((B * T, NK, D), device=dev), dim=-1).reshape(B * T, NK * D)
+    k = torch.nn.functional.normalize(torch.randn((B * T, NK, D), device=dev), dim=-1).reshape(B * T, NK * D)
+    v = torch.randn((B * T, NV * D), device=dev)
+    a = torch.full((B * T, NV), 0.9, device=dev)
+    b = torch.full((B * T, NV), 0.5, device=dev)
+    o = torch.zeros((B * T, NV * D), device=dev)
+    try:
+        gdn.gdn_set_mma_wait_polls(0)
+        gdn.gdn_prefill_chunked(S, q, k, v, a, b, o, batch=B, seq_len=T, nk=NK, nv=NV, d=D)
+        torch.cuda.synchronize()
+    finally:
+        gdn.gdn_set_wait_polls(gdn.GDN_DEFAULT_WAIT_POLLS)
+    assert gdn.gdn_device_wait_timeouts() == before + B * NV
+    assert torch.isnan(S).all().item()
+    r = run_prefill_case(2, 2, 3, 128, 65, seed=451, init="normal", chunked=True)
     check(r)
     assert gdn.gdn_device_wait_timeouts() == before + B * NV
