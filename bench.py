@@ -128,7 +128,8 @@ def src_sha(*names):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 5 ms (as fast as nvidia-smi delivers) while
+    running; summary() covers the samples between two marks."""
 
     Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -149,7 +150,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                          "--format=csv,noheader,nounits", "-lms", "5"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -168,12 +169,12 @@ class ClockSampler:
         """Record the wall-clock start or end of the timed region."""
         setattr(self, which, datetime.datetime.now())
 
-    def summary(self):
+    def summary(self, lo_mark="start", hi_mark="end", keep=False):
         if self.proc is None or not os.path.exists(self.path):
             return None
         sm, mx, reasons, pw = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        lo, hi = getattr(self, "start", None), getattr(self, "end", None)
+        lo, hi = getattr(self, lo_mark, None), getattr(self, hi_mark, None)
         lines = [[p.strip() for p in line.split(",")] for line in open(self.path)]
         lines = [p for p in lines if len(p) >= 9]
 
@@ -198,7 +199,8 @@ class ClockSampler:
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
-        os.unlink(self.path)
+        if not keep:
+            os.unlink(self.path)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
@@ -336,12 +338,26 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize()
         clk.mark("end")
+        # a timed region of a few tens of ms holds few clock samples: the same step replayed, untimed,
+        # for a quarter second more gives the clocks under the same load a fuller record
+        short = (clk.end - clk.start).total_seconds() < 0.25
+        if short:
+            clk.mark("after_start")
+            t_end = time.time() + 0.25
+            while time.time() < t_end:
+                step()
+                torch.cuda.synchronize()
+            clk.mark("after_end")
         time.sleep(0.05)
     if world > 1:
         dist.barrier()
     ms = e0.elapsed_time(e1)
     ms_step = max_over_ranks(ms / args.steps, world, dev)
-    clocks = clk.summary()
+    clocks = clk.summary(keep=short)
+    if short:
+        after = clk.summary("after_start", "after_end")
+        if clocks is not None:
+            clocks["after_timed_region"] = after
 
     token_heads = B * NV * L
     value = job_throughput(token_heads, world, ms_step)
