@@ -218,18 +218,30 @@ decode_d128(const DecodeParams p)
                 p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
             }
         } else {
-            // int8 groups of 32: a group spans two warps' rows, so the normed
-            // values meet in shared memory and warp w < 4 quantises group w.
-            __shared__ float y_s[kD];
+            // int8 groups of 32: a group is the rows of 32 / RPW consecutive warps.  Each warp takes the
+            // max |y| over its rows (lanes r < RPW hold them), the group's warps exchange theirs through
+            // shared memory, and every warp quantises its own rows (the same max, the same IEEE division
+            // as quant_group32: the same codes).
+            constexpr int WPG = 32 / RPW;                   // warps per group
+            __shared__ float wmax[W];
+            float y = 0.f;
             if (row_lane) {
-                const float y = gn_l * o_keep * rstd * silu(z_l);
-                y_s[row0 + lane] = y;
+                y = gn_l * o_keep * rstd * silu(z_l);
                 if (p.y != nullptr) p.y[seq * p.y_stride + (int64_t)h * kD + row0 + lane] = y;
             }
+            float am = fabsf(y);
+#pragma unroll
+            for (int off = RPW / 2; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, off));
+            if (lane == 0) wmax[warp] = am;
             __syncthreads();
-            if (warp < kD / 32)
-                quant_group32(y_s[32 * warp + lane], p.xq + seq * p.xq_stride + (int64_t)h * kD + 32 * warp + lane,
-                              p.xs + seq * p.xs_stride + (int64_t)h * (kD / 32) + warp, lane);
+            const int g0 = warp - warp % WPG;
+            float gm = wmax[g0];
+#pragma unroll
+            for (int i = 1; i < WPG; ++i) gm = fmaxf(gm, wmax[g0 + i]);
+            const float sc = gm > 0.f ? gm / 127.0f : 1.0f;
+            if (row_lane)
+                p.xq[seq * p.xq_stride + (int64_t)h * kD + row0 + lane] = (int8_t)__float2int_rn(y / sc);
+            if (warp == g0 && lane == 0) p.xs[seq * p.xs_stride + (int64_t)h * (kD / 32) + row0 / 32] = sc;
         }
     }
 }
