@@ -296,8 +296,9 @@ conv_norm_d128(const ConvNormParams p)
     };
     // This CTA's reads of the key head's q/k ring rows ended at the __syncthreads after step 3.  It
     // counts itself (fence + atomic add, one thread) as its last batch of rows begins: the fence
-    // waits for the counting thread's own memory operations in flight, which by then are only the
-    // loads of that batch, needed next anyway, and the add's round trip overlaps the batch.  (Taken
+    // waits for the counting thread's own memory operations in flight, which by then are that
+    // batch's loads (needed next anyway) and the streaming stores of earlier rows, and the add's
+    // round trip overlaps the batch.  (Taken
     // right after step 3, the fence held the thread's warp until all its first loads had landed:
     // 38.3 us a launch at batch 32; after the rows, 35.1 us; here, 34.2 us.)  Its result is first
     // needed after the norm's barrier.
