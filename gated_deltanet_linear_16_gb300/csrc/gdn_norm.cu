@@ -21,9 +21,28 @@ namespace {
 constexpr int kWarpsPerCta = 8;
 constexpr int kMaxPer = 8;                 // D <= 256: values per lane
 
+// y / s rounded to nearest (the IEEE quotient) from r = 1/s (the IEEE
+// reciprocal), by Markstein's correction (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): q0 = RN(y r), e = y - s q0 (exact in one FMA), q =
+// RN(q0 + e r).  The theorem gives RN(y / s) when r is within half an ulp of
+// 1/s and q0 within an ulp of y/s, with no underflow; the residual e is about
+// |y/s| 2^-24 s, so it stays normal for s >= 2^-60 whenever the quotient is
+// large enough to matter for an int8 code (a smaller one rounds to 0 either
+// way).  Checked on a GB300 against the IEEE division bit for bit: every float
+// y in [s/4, 127.5 s] for 256 random scales (19.3e9 quotients, no difference)
+// and 2.55e9 random pairs over scales from 2^-107 (two quotients differed,
+// both with s near 1e-32 and codes 0; those scales take the division).
+constexpr float kMinCorrectedScale = 0x1p-60f;
+__device__ __forceinline__ float quotient_rn(float y, float s, float r)
+{
+    const float q0 = __fmul_rn(y, r);
+    return __fmaf_rn(__fmaf_rn(-q0, s, y), r, q0);
+}
+
 // silu with the fast division (within 2 ulp): this kernel is an elementwise
-// stream, where the IEEE division of the gate cost 7 % of the time.  The
-// division that decides an int8 code stays an IEEE division.
+// stream, where the IEEE division of the gate cost 7 % of the time.  An int8
+// code is still that of the IEEE quotient (quotient_rn).
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 template <int EPI>
@@ -149,9 +168,9 @@ gate_norm_d128(const NormParams p)
 // of 4 consecutive units, runs a grid apart.  Against the bf16 kernel's layout
 // (a warp per unit, 4 values a lane) this cuts the per-unit reductions, the
 // address and loop work per value: 304 us over 32768 rows x 48 heads, against
-// 315 with a half-warp per unit and 365 with a warp, the quantisation's
-// divisions (IEEE, as the page decides codes) keeping the kernel bound by
-// instruction issue more than by HBM.
+// 315 with a half-warp per unit and 365 with a warp.  A code is y / scale
+// rounded, the IEEE quotient as the page decides codes, here by the corrected
+// reciprocal (quotient_rn) instead of 16 divisions a lane.
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 gate_norm_q8_hw(const NormParams p)
 {
@@ -208,8 +227,15 @@ gate_norm_q8_hw(const NormParams p)
         am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));    // a group of 32 is 2 lanes
         const float sc = am > 0.f ? am / 127.0f : 1.0f;
         unsigned w[4] = {0u, 0u, 0u, 0u};
+        if (sc >= kMinCorrectedScale) {                  // the quotients by Markstein's correction
+            const float rs = 1.0f / sc;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w[i >> 2] |= ((unsigned)(__float2int_rn(y[i] / sc) & 0xff)) << (8 * (i & 3));
+            for (int i = 0; i < 16; ++i)
+                w[i >> 2] |= ((unsigned)(__float2int_rn(quotient_rn(y[i], sc, rs)) & 0xff)) << (8 * (i & 3));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i >> 2] |= ((unsigned)(__float2int_rn(y[i] / sc) & 0xff)) << (8 * (i & 3));
+        }
         if (active) {
             unsigned *q = reinterpret_cast<unsigned *>(p.xq + r * p.xq_stride + e0);
 #pragma unroll

@@ -113,15 +113,18 @@ def test_prefill_then_norm():
     assert rel_l2(bf16_to_f64(out.cpu().numpy()).reshape(rows * NV, D), ref) <= TOL_REL_L2
 
 
-@pytest.mark.parametrize("pad,offset", [(0, 0.0), (1, 0.0), (0, 2.0 ** -15), (0, 2.0 ** -14), (0, 2.0 ** -13),
-                                        (1, 2.0 ** -14)])
-def test_q8_near_ties(pad, offset):
+@pytest.mark.parametrize("pad,offset,scale", [(0, 0.0, 1.0), (1, 0.0, 1.0), (0, 2.0 ** -15, 1.0), (0, 2.0 ** -14, 1.0),
+                                              (0, 2.0 ** -13, 1.0), (1, 2.0 ** -14, 1.0), (0, 0.0, 1e-34),
+                                              (0, 2.0 ** -14, 1e-34)])
+def test_q8_near_ties(pad, offset, scale):
     """Quotients y / scale planted within a few ulp of half-integers (the ties and near-ties of
     round-half-even), on the vector kernel (pad 0) and the general one (pad 1): with z = 20
     (silu(20) = 20 in fp32) and gn = 1, y is o times one per-head factor up to rounding, so o =
     +-(k + 1/2 + e) / 127 next to a group maximum of 1 puts 127 y / max|y| next to k + 1/2 + e.
-    e = 0, or +-offset at random: offsets around 2^-14, where the kernels stop dividing and
-    multiply by the scale's reciprocal instead.  Codes and scales must equal the oracle's fp32
+    e = 0, or +-offset at random (2^-15 .. 2^-13: quotients a few hundred ulp from a tie).  scale
+    multiplies o: at 1e-34 the norm's eps dominates and the
+    groups' scales fall far below 2^-60, where the vector kernel's quotients come from the IEEE
+    division instead of the corrected reciprocal.  Codes and scales must equal the oracle's fp32
     quantiser (IEEE quotients) on the kernel's own y bit for bit."""
     rows, nv, d = 4, 3, 128
     hv = nv * d
@@ -130,7 +133,7 @@ def test_q8_near_ties(pad, offset):
     e = rng.choice([-1.0, 1.0], size=k.shape) * offset
     o = rng.choice([-1.0, 1.0], size=k.shape) * (k + 0.5 + e) / 127.0
     o[:, :, 0] = rng.choice([-1.0, 1.0], size=(rows, hv // 32))       # the group maximum, |o| = 1
-    o = o.reshape(rows, hv).astype(np.float32)
+    o = (o.reshape(rows, hv) * scale).astype(np.float32)
     z = np.full((rows, hv), 20.0, np.float32)
     gn = np.ones(d, np.float32)
     ob, zb, gb = Rows(rows, hv, hv + pad), Rows(rows, hv, hv + pad), Rows(1, d)
