@@ -756,6 +756,8 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
     S16 = torch.zeros((PB, NV, D, D), dtype=torch.float16, device=dev)
     s16 = time_fn(torch, stream, lambda: gdn.gdn_prefill_seq(S16, q, k, v, a, bt, o, batch=PB, seq_len=T, nk=NK,
                                                              nv=NV, d=D, stream=sp), 3, warm=1)
+    s16_tc = time_fn(torch, stream, lambda: gdn.gdn_prefill_chunked(S16, q, k, v, a, bt, o, batch=PB, seq_len=T,
+                                                                    nk=NK, nv=NV, d=D, stream=sp), 3, warm=1)
     # the gated norm over every token's raw o (gdn_gate_norm, bf16 out): o and z read, out written
     z = torch.randn((R, NV * D), device=dev, generator=g)
     gn = torch.ones(D, device=dev)
@@ -782,7 +784,8 @@ def row_prefill(torch, gdn, dev, stream, pk, T=4096):
     del q, k, v, a, bt, o, S, S16
     torch.cuda.empty_cache()
     return {"prefill": {"config": f"B=8 T={T} NK=16 NV=48 D=128 fp32, state on chip",
-                        "fp16_state": {"ms": s16 * 1e3, "token_heads_per_s": th / s16},
+                        "fp16_state": {"ms": s16 * 1e3, "token_heads_per_s": th / s16,
+                                       "chunked_tensor_core_ms": s16_tc * 1e3},
                         "gate_norm_of_outputs": {"us": s_norm * 1e6, "achieved_gbs": norm_bytes / s_norm / 1e9,
                                                  "frac_of_hbm_peak": norm_bytes / s_norm / 1e9 / pk["hbm_gbs"],
                                                  "algorithmic_bytes": norm_bytes},
