@@ -84,17 +84,18 @@ namespace {
 constexpr int kD = 128;
 constexpr int kC = 64;                       // tokens per chunk
 constexpr int kThreads = 256;
-// MMA-issuing threads: lane 0 of warps 2, 3 and 6 (no part in building A or in the inversion).  One
-// thread issues about one MMA per ~140 cycles whatever its N, while the tensor core takes MMAs from
-// several threads at once, so each product is split over up to three issuers, each part (a range
-// of K, or a pass of the precision split) into its own accumulator, summed by the SIMT phase after.
+// MMA-issuing threads: lane 0 of warps 2, 3 and 6 (no part in building A).  One thread issues about
+// one MMA per ~120-140 cycles whatever its N, while the tensor core takes MMAs from several threads
+// at once, so each product is split over up to three issuers, each part (a range of K, or a pass of
+// the precision split) into its own accumulator, summed by the SIMT phase after.
 constexpr int kIss0 = 64, kIss1 = 96, kIss2 = 192;
 constexpr uint32_t kWaitLimit = 1u << 22;    // polls of an mbarrier phase before giving up
 
 // shared memory (1024-aligned), byte offsets
-// [K;Q]: 128 rows x 128, until MMA-1 is done.  kKQHi: as the tensor copy brings it in (during the
-// previous chunk), its fp32 bits the high TF32 parts (the tensor core reads the top 19 bits);
-// kKQLo: the low parts x - trunc_tf32(x), exact
+// [K;Q]: 128 rows x 128, until MMA-1 and the k reads are done.  kKQHi: as the tensor copies bring it
+// in (during the previous chunk), its fp32 bits the high TF32 parts (the tensor core reads the top 19
+// bits); kKQLo: the low parts x - trunc_tf32(x), exact.  T and the B operand of MMA-3 reuse
+// [0, 128 KB) after MMA-1; the next chunk's copies land in kKQHi once the k reads are done.
 constexpr uint32_t kKQLo = 0, kKQHi = 131072;
 constexpr uint32_t kTHi = 0, kTLo = 16384;             // T: 64 rows (t) x 64 (i), after MMA-1
 // B operand of MMA-3, 192 rows x 64 (K = t or i): rows 0-127 Ktilde^T (row c), rows 128-191 P (row t)
