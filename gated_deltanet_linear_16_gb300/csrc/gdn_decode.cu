@@ -30,7 +30,13 @@
 //    coalesced read per warp (a float per row) that lanes broadcast by shuffle;
 //  * the three dot products are butterfly shuffles inside the group of lanes
 //    that holds a row (32 lanes fp32, 16 lanes fp16); k.q is reduced once per
-//    warp, not per row.
+//    warp, not per row;
+//  * on grids of one wave (batch 1-3 at 48 heads), where a step's time is the
+//    CTA's own dependency chain rather than HBM, a lane's rows are reduced
+//    together by one transposed butterfly (a reduce-scatter with the
+//    butterfly's partners, so the sums keep their bits) instead of one
+//    butterfly per row, and four warps finish the norm while the rest return
+//    (single-layer step 3.20 -> 2.81 us).
 #include "gdn_internal.cuh"
 
 #ifndef STAGED_MIN_CTAS_PER_SM
@@ -85,6 +91,9 @@ decode_d128(const DecodeParams p)
     constexpr int NBAT = STAGED ? kGroups : NB;      // groups / batches of loads
     constexpr int PER = NLD / NBAT;                  // vectors per group / batch
     static_assert(NLD % NBAT == 0 && RPW <= 32, "shape");
+    // the one-wave path reduces all of a lane's rows in one transposed butterfly (below): 2 NLD values
+    // over LPR lanes, one per pair of lanes at the end
+    constexpr bool XPOSE = !STAGED && NB == 1 && 4 * NLD == LPR;
 
     const int unit = blockIdx.x;               // (sequence, value head)
     const int seq = unit / p.nv;
@@ -131,10 +140,13 @@ decode_d128(const DecodeParams p)
     }
     const bool row_lane = lane < RPW;          // lane r carries row row0 + r
     const float v_l = row_lane ? __ldg(p.v + seq * p.v_stride + (int64_t)h * kD + row0 + lane) : 0.f;
+    // z, gn: lane r of every warp for row row0 + r; on the one-wave path the norm's tail runs on the
+    // first kD / 32 warps, a row per lane (row 32 warp + lane), so those load the tail's rows instead
     float z_l = 0.f, gn_l = 0.f;
-    if (NORM && row_lane) {
-        z_l = __ldg(p.z + seq * p.z_stride + (int64_t)h * kD + row0 + lane);
-        gn_l = __ldg(p.gn + row0 + lane);
+    if (NORM && (XPOSE ? warp < kD / 32 : row_lane)) {
+        const int zr = XPOSE ? 32 * warp + lane : row0 + lane;
+        z_l = __ldg(p.z + seq * p.z_stride + (int64_t)h * kD + zr);
+        gn_l = __ldg(p.gn + zr);
     }
     const float alpha = __ldg(p.alpha + seq * p.gb_stride + h);
     const float beta = __ldg(p.beta + seq * p.gb_stride + h);
@@ -172,6 +184,69 @@ decode_d128(const DecodeParams p)
             }
         }
     };
+    if constexpr (XPOSE) {
+        // All of the lane's rows at once (the one-wave path, where a CTA's time is its own dependency
+        // chain): the partial dot products of every row, then a single reduce-scatter over the group's
+        // lanes with the butterfly's partners and order (offsets LPR/2 .. 1), so each sum is group_sum's
+        // bit for bit.  A level halves the values a lane carries: the lane keeps the half its partner
+        // does not, adding the partner's copy.  After it, lanes 4i, 4i+1 of a group hold u of the
+        // group's vector i and lanes 4i+2, 4i+3 its w; 2 x NLD shuffles in all instead of 2 x NLD x
+        // log2(LPR), and one chain of log2(LPR) levels instead of one per row.  Measured at batch 1:
+        // the row work took ~310 cycles a row, one row after another.
+        float part[2 * NLD];
+#pragma unroll
+        for (int i = 0; i < NLD; ++i) {
+            float s[EPV];
+            V::unpack(raw[0][i], s);
+            float u = 0.f, w = 0.f;
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
+            part[2 * i] = u;
+            part[2 * i + 1] = w;
+        }
+#pragma unroll
+        for (int lvl = 0; (LPR >> (lvl + 1)) > 0; ++lvl) {
+            const int off = LPR >> (lvl + 1), half = (2 * NLD) >> (lvl + 1);
+            const bool upper = (lane & off) != 0;
+            if (half > 0) {
+#pragma unroll
+                for (int j = 0; j < half; ++j) {
+                    const float keep = upper ? part[j + half] : part[j];
+                    const float send = upper ? part[j] : part[j + half];
+                    part[j] = keep + __shfl_xor_sync(kFull, send, off);
+                }
+            } else {
+                part[0] += __shfl_xor_sync(kFull, part[0], off);
+            }
+        }
+        const float other = __shfl_xor_sync(kFull, part[0], 2);
+        const bool is_w = ((lane % LPR) >> 1) & 1;
+        const float u = is_w ? other : part[0], w = is_w ? part[0] : other;
+        const int vi = (lane % LPR) >> 2;                    // the vector (row) this lane's quad reduced
+        const float va = __shfl_sync(kFull, v_l, vi * RPL + sub);
+        const float coef = beta * (va - alpha * u);
+        const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
+        // every lane takes its rows' coefficients (and outputs, for the sum of squares in row order)
+        const int gbase = lane & ~(LPR - 1);
+        float cf[NLD];
+#pragma unroll
+        for (int i = 0; i < NLD; ++i) {
+            cf[i] = __shfl_sync(kFull, coef, gbase + 4 * i);
+            if constexpr (NORM) {
+                const float oi = __shfl_sync(kFull, oa, gbase + 4 * i);
+                o_sq = fmaf(oi, oi, o_sq);
+            }
+        }
+        o_keep = __shfl_sync(kFull, oa, (lane % RPL) * LPR + 4 * ((lane / RPL) % NLD));   // lane r: row r
+#pragma unroll
+        for (int i = 0; i < NLD; ++i) {
+            float s[EPV];
+            V::unpack(raw[0][i], s);
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) s[j] = fmaf(cf[i], kx[j], alpha * s[j]);
+            st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
+        }
+    } else {
 #pragma unroll
     for (int bt = 0; bt < NBAT; ++bt) {
         if constexpr (STAGED) {
@@ -191,12 +266,25 @@ decode_d128(const DecodeParams p)
             for (int ii = 0; ii < PER; ++ii) row_step(raw[bt & 1][ii], bt * PER + ii);
         }
     }
+    }
 
     if constexpr (!NORM) {
         if (row_lane) p.o[seq * p.o_stride + (int64_t)h * kD + row0 + lane] = o_keep;
     } else {
         // 4. gated RMS norm over the head's 128 outputs, in this CTA
         __shared__ float red[W];
+        // One-wave path (a CTA's own chain is the time there): the head's o goes to shared memory and
+        // the first kD / 32 warps finish the head after the barrier, a row per lane, while the others
+        // return; they take the gate's silu(z) before the barrier, as the other warps finish their
+        // rows.  Measured per single-layer step: fp32 batch 1 2.835 -> 2.811 us, batch 2 3.50 -> 3.18,
+        // fp16 batch 1 2.24 -> 2.05.  The HBM-bound paths take silu after the barrier (0.9 % slower
+        // before it).  Either way silu is the product's last factor: the same bits.
+        __shared__ float o_s[XPOSE ? kD : 1];
+        float sz = 0.f;
+        if constexpr (XPOSE) {
+            if (row_lane) o_s[row0 + lane] = o_keep;
+            if (warp < kD / 32) sz = silu(z_l);
+        }
         // the warp's sum of squares: each row group's lanes accumulated its rows' o^2 in the loop, so
         // no reduction is left for the tail of the CTA (measured: 48-layer step 1.564 -> 1.517 ms)
         float ss = o_sq;
@@ -204,6 +292,9 @@ decode_d128(const DecodeParams p)
         for (int r = 1; r < RPL; ++r) ss += __shfl_sync(kFull, o_sq, r * LPR);
         if (lane == 0) red[warp] = ss;
         __syncthreads();
+        if constexpr (XPOSE) {
+            if (warp >= kD / 32) return;       // no barrier follows on this path
+        }
         float part[W];                         // pairwise sum of the warps' partials
 #pragma unroll
         for (int i = 0; i < W; ++i) part[i] = red[i];
@@ -212,7 +303,21 @@ decode_d128(const DecodeParams p)
 #pragma unroll
             for (int i = 0; i < n; ++i) part[i] += part[i + n];
         const float rstd = rsqrtf(part[0] * (1.0f / kD) + p.eps);
-        if constexpr (EPI == kEpiBf16) {
+        if constexpr (XPOSE) {
+            const int row = 32 * warp + lane;
+            const float y = gn_l * o_s[row] * rstd * sz;
+            if constexpr (EPI == kEpiBf16) {
+                p.out[seq * p.out_stride + (int64_t)h * kD + row] = bf16_bits_rn(y);
+            } else {                           // this warp's 32 rows are one int8 group
+                if (p.y != nullptr) p.y[seq * p.y_stride + (int64_t)h * kD + row] = y;
+                float am = fabsf(y);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, off));
+                const float sc = am > 0.f ? am / 127.0f : 1.0f;
+                p.xq[seq * p.xq_stride + (int64_t)h * kD + row] = (int8_t)__float2int_rn(y / sc);
+                if (lane == 0) p.xs[seq * p.xs_stride + (int64_t)h * (kD / 32) + warp] = sc;
+            }
+        } else if constexpr (EPI == kEpiBf16) {
             if (row_lane) {
                 const float y = gn_l * o_keep * rstd * silu(z_l);
                 p.out[seq * p.out_stride + (int64_t)h * kD + row0 + lane] = bf16_bits_rn(y);
