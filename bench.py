@@ -54,12 +54,12 @@ REF_LAYERS_PER_STEP = 4      # oracle sample per step of the reference arm
 # dram__bytes_write.sum), valid only while the kernel source is the one it was taken on.
 NCU_TRAFFIC = {
     # mean of three mid-sequence launches of the full 48-layer workload, ncu --cache-control none
-    # (reads 102.9-103.1 MB, writes 96.6-99.6 MB), from the ncu capture of the batch-32 48-layer decode
-    "decode_norm_f32": {"bytes_per_launch": 201592235,
-                        "src_sha256": "5d923227afa196262dda7d767f1a94d4e16f2f77a3a65b93d0713389cd90e1d3"},
-    # mean of two launches of the 256-slot fp16 pool decode (reads 413.4-413.6 MB, writes 388.4-388.7 MB)
-    "decode_norm_f16_pool": {"bytes_per_launch": 802042368,
-                             "src_sha256": "5d923227afa196262dda7d767f1a94d4e16f2f77a3a65b93d0713389cd90e1d3"},
+    # (reads 102.8 MB, writes 96.6-99.8 MB), from the ncu capture of the batch-32 48-layer decode
+    "decode_norm_f32": {"bytes_per_launch": 201434965,
+                        "src_sha256": "11c70d442179d75d266dd086e41d94898ee942088de56d54a8f346715905f3df"},
+    # mean of two launches of the 256-slot fp16 pool decode (reads 407.2 MB, writes 401.1-403.0 MB)
+    "decode_norm_f16_pool": {"bytes_per_launch": 809197696,
+                             "src_sha256": "11c70d442179d75d266dd086e41d94898ee942088de56d54a8f346715905f3df"},
     # mean of two launches of the batch-32 fp32 decode from projections (reads 105.8 MB, writes
     # 102.6-104.3 MB), ncu --cache-control none
     "conv_norm_f32": {"bytes_per_launch": 209281408, "src": ("gdn_conv_norm.cu", "gdn_internal.cuh"),

@@ -28,15 +28,17 @@
 //    Each lane reads back only the vectors it copied itself;
 //  * k and q are read as this lane's own 16-byte columns, v/z/gn as one
 //    coalesced read per warp (a float per row) that lanes broadcast by shuffle;
-//  * the three dot products are butterfly shuffles inside the group of lanes
-//    that holds a row (32 lanes fp32, 16 lanes fp16); k.q is reduced once per
-//    warp, not per row;
+//  * k.q is a butterfly sum inside the group of lanes that holds a row (32
+//    lanes fp32, 16 lanes fp16), once per warp; the rows' u = S[a].k and
+//    w = S[a].q are reduced a group of rows at a time (a commit group, a
+//    register batch, or all of a lane's rows on one-wave grids) by one
+//    transposed butterfly: a reduce-scatter with the butterfly's partners, so
+//    every sum keeps the butterfly's bits, in about 2 shuffles a row instead
+//    of 8-10 and one chain of levels a group instead of one a row (48-layer
+//    step 1.520 -> 1.508 ms, single-layer step 3.20 -> 2.80 us);
 //  * on grids of one wave (batch 1-3 at 48 heads), where a step's time is the
-//    CTA's own dependency chain rather than HBM, a lane's rows are reduced
-//    together by one transposed butterfly (a reduce-scatter with the
-//    butterfly's partners, so the sums keep their bits) instead of one
-//    butterfly per row, and four warps finish the norm while the rest return
-//    (single-layer step 3.20 -> 2.81 us).
+//    CTA's own dependency chain rather than HBM, four warps finish the norm,
+//    a row per lane, while the rest return.
 #include "gdn_internal.cuh"
 
 #ifndef STAGED_MIN_CTAS_PER_SM
@@ -91,9 +93,9 @@ decode_d128(const DecodeParams p)
     constexpr int NBAT = STAGED ? kGroups : NB;      // groups / batches of loads
     constexpr int PER = NLD / NBAT;                  // vectors per group / batch
     static_assert(NLD % NBAT == 0 && RPW <= 32, "shape");
-    // the one-wave path reduces all of a lane's rows in one transposed butterfly (below): 2 NLD values
-    // over LPR lanes, one per pair of lanes at the end
-    constexpr bool XPOSE = !STAGED && NB == 1 && 4 * NLD == LPR;
+    // the one-wave path (every load in registers, at most one CTA per SM): the norm is finished by
+    // the first kD / 32 warps, a row per lane, after the barrier
+    constexpr bool ONE_WAVE = !STAGED && NB == 1;
 
     const int unit = blockIdx.x;               // (sequence, value head)
     const int seq = unit / p.nv;
@@ -143,8 +145,8 @@ decode_d128(const DecodeParams p)
     // z, gn: lane r of every warp for row row0 + r; on the one-wave path the norm's tail runs on the
     // first kD / 32 warps, a row per lane (row 32 warp + lane), so those load the tail's rows instead
     float z_l = 0.f, gn_l = 0.f;
-    if (NORM && (XPOSE ? warp < kD / 32 : row_lane)) {
-        const int zr = XPOSE ? 32 * warp + lane : row0 + lane;
+    if (NORM && (ONE_WAVE ? warp < kD / 32 : row_lane)) {
+        const int zr = ONE_WAVE ? 32 * warp + lane : row0 + lane;
         z_l = __ldg(p.z + seq * p.z_stride + (int64_t)h * kD + zr);
         gn_l = __ldg(p.gn + zr);
     }
@@ -156,48 +158,25 @@ decode_d128(const DecodeParams p)
     for (int j = 0; j < EPV; ++j) kq = fmaf(kx[j], qx[j], kq);
     kq = group_sum<LPR>(kq);
 
-    // 3. per row: two dot products, the delta coefficient, output, write-back
+    // 3. per row: two dot products, the delta coefficient, output, write-back (in groups of rows)
     float o_keep = 0.f;                        // lane r keeps o of row row0 + r
     float o_sq = 0.f;                          // sum of o^2 over the rows of this lane's row group
-    auto row_step = [&](const uint4 packed, const int i) {   // i: vector index within the lane's slice
-        float s[EPV];
-        V::unpack(packed, s);
-        float u = 0.f, w = 0.f;
+    // A group of PER vectors (a commit group, a register batch, or on the one-wave path all of the
+    // lane's rows) at once: the partial dot products of its rows, then one reduce-scatter over the row
+    // group's lanes with the butterfly's partners and order (offsets LPR/2 .. 1), so each sum is
+    // group_sum's bit for bit.  A level halves the values a lane carries (while more than one is
+    // left): the lane keeps the half its partner gives away and adds the partner's copy.  After it,
+    // the R = LPR / (2 PER) lanes of block m of the group hold value m: u (m even) or w (m odd) of
+    // vector m / 2.  2 PER shuffles instead of 2 PER log2(LPR), and one chain of log2(LPR) levels
+    // instead of one per row (measured at batch 1: ~310 cycles a row, one row after another).
+    auto group_step = [&](const uint4 (&vec)[PER], const int i0) {
+        constexpr int R = LPR / (2 * PER);
+        static_assert(R >= 1 && (PER & (PER - 1)) == 0, "a group's 2 PER values over the LPR lanes of a row");
+        float part[2 * PER];
 #pragma unroll
-        for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
-        u = group_sum<LPR>(u);
-        w = group_sum<LPR>(w);
-        const float va = __shfl_sync(kFull, v_l, i * RPL + sub);
-        const float coef = beta * (va - alpha * u);
-        const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
-        if constexpr (NORM) o_sq = fmaf(oa, oa, o_sq);   // every lane of the group holds oa
-#pragma unroll
-        for (int j = 0; j < EPV; ++j) s[j] = fmaf(coef, kx[j], alpha * s[j]);
-        st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
-        if constexpr (RPL == 1) {
-            if (lane == i) o_keep = oa;
-        } else {
-#pragma unroll
-            for (int r = 0; r < RPL; ++r) {
-                const float orr = __shfl_sync(kFull, oa, r * LPR);
-                if (lane == i * RPL + r) o_keep = orr;
-            }
-        }
-    };
-    if constexpr (XPOSE) {
-        // All of the lane's rows at once (the one-wave path, where a CTA's time is its own dependency
-        // chain): the partial dot products of every row, then a single reduce-scatter over the group's
-        // lanes with the butterfly's partners and order (offsets LPR/2 .. 1), so each sum is group_sum's
-        // bit for bit.  A level halves the values a lane carries: the lane keeps the half its partner
-        // does not, adding the partner's copy.  After it, lanes 4i, 4i+1 of a group hold u of the
-        // group's vector i and lanes 4i+2, 4i+3 its w; 2 x NLD shuffles in all instead of 2 x NLD x
-        // log2(LPR), and one chain of log2(LPR) levels instead of one per row.  Measured at batch 1:
-        // the row work took ~310 cycles a row, one row after another.
-        float part[2 * NLD];
-#pragma unroll
-        for (int i = 0; i < NLD; ++i) {
+        for (int i = 0; i < PER; ++i) {
             float s[EPV];
-            V::unpack(raw[0][i], s);
+            V::unpack(vec[i], s);
             float u = 0.f, w = 0.f;
 #pragma unroll
             for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
@@ -206,9 +185,9 @@ decode_d128(const DecodeParams p)
         }
 #pragma unroll
         for (int lvl = 0; (LPR >> (lvl + 1)) > 0; ++lvl) {
-            const int off = LPR >> (lvl + 1), half = (2 * NLD) >> (lvl + 1);
-            const bool upper = (lane & off) != 0;
+            const int off = LPR >> (lvl + 1), half = (2 * PER) >> (lvl + 1);
             if (half > 0) {
+                const bool upper = (lane & off) != 0;
 #pragma unroll
                 for (int j = 0; j < half; ++j) {
                     const float keep = upper ? part[j + half] : part[j];
@@ -219,34 +198,38 @@ decode_d128(const DecodeParams p)
                 part[0] += __shfl_xor_sync(kFull, part[0], off);
             }
         }
-        const float other = __shfl_xor_sync(kFull, part[0], 2);
-        const bool is_w = ((lane % LPR) >> 1) & 1;
+        const float other = __shfl_xor_sync(kFull, part[0], R);
+        const bool is_w = ((lane % LPR) / R) & 1;
         const float u = is_w ? other : part[0], w = is_w ? part[0] : other;
-        const int vi = (lane % LPR) >> 2;                    // the vector (row) this lane's quad reduced
-        const float va = __shfl_sync(kFull, v_l, vi * RPL + sub);
+        const int vi = (lane % LPR) / (2 * R);               // the vector (row) these lanes reduced
+        const float va = __shfl_sync(kFull, v_l, (i0 + vi) * RPL + sub);
         const float coef = beta * (va - alpha * u);
         const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
         // every lane takes its rows' coefficients (and outputs, for the sum of squares in row order)
         const int gbase = lane & ~(LPR - 1);
-        float cf[NLD];
+        float cf[PER];
 #pragma unroll
-        for (int i = 0; i < NLD; ++i) {
-            cf[i] = __shfl_sync(kFull, coef, gbase + 4 * i);
+        for (int i = 0; i < PER; ++i) {
+            cf[i] = __shfl_sync(kFull, coef, gbase + 2 * R * i);
             if constexpr (NORM) {
-                const float oi = __shfl_sync(kFull, oa, gbase + 4 * i);
+                const float oi = __shfl_sync(kFull, oa, gbase + 2 * R * i);
                 o_sq = fmaf(oi, oi, o_sq);
             }
         }
-        o_keep = __shfl_sync(kFull, oa, (lane % RPL) * LPR + 4 * ((lane / RPL) % NLD));   // lane r: row r
+        {   // lane r < RPW keeps the o of row r: vector r / RPL of row group r % RPL
+            const int vr = lane / RPL - i0;
+            const float ok = __shfl_sync(kFull, oa, (lane % RPL) * LPR + (vr & (PER - 1)) * 2 * R);
+            if (lane < RPW && vr >= 0 && vr < PER) o_keep = ok;
+        }
 #pragma unroll
-        for (int i = 0; i < NLD; ++i) {
+        for (int i = 0; i < PER; ++i) {
             float s[EPV];
-            V::unpack(raw[0][i], s);
+            V::unpack(vec[i], s);
 #pragma unroll
             for (int j = 0; j < EPV; ++j) s[j] = fmaf(cf[i], kx[j], alpha * s[j]);
-            st_stream16(rowp + (int64_t)i * RPL * kD, V::pack(s));
+            st_stream16(rowp + (int64_t)(i0 + i) * RPL * kD, V::pack(s));
         }
-    } else {
+    };
 #pragma unroll
     for (int bt = 0; bt < NBAT; ++bt) {
         if constexpr (STAGED) {
@@ -254,18 +237,18 @@ decode_d128(const DecodeParams p)
             else if (bt == 1) cp_async_wait<kGroups - 2>();
             else if (bt == 2) cp_async_wait<kGroups - 3>();
             else cp_async_wait<0>();
+            uint4 vec[PER];
 #pragma unroll
-            for (int ii = 0; ii < PER; ++ii) row_step(mine[(bt * PER + ii) * RPL * VPR], bt * PER + ii);
+            for (int ii = 0; ii < PER; ++ii) vec[ii] = mine[(bt * PER + ii) * RPL * VPR];
+            group_step(vec, bt * PER);
         } else {
             if (bt + 1 < NBAT) {
 #pragma unroll
                 for (int i = 0; i < PER; ++i)
                     raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * PER + i) * RPL * kD);
             }
-#pragma unroll
-            for (int ii = 0; ii < PER; ++ii) row_step(raw[bt & 1][ii], bt * PER + ii);
+            group_step(raw[bt & 1], bt * PER);
         }
-    }
     }
 
     if constexpr (!NORM) {
@@ -279,9 +262,9 @@ decode_d128(const DecodeParams p)
         // rows.  Measured per single-layer step: fp32 batch 1 2.835 -> 2.811 us, batch 2 3.50 -> 3.18,
         // fp16 batch 1 2.24 -> 2.05.  The HBM-bound paths take silu after the barrier (0.9 % slower
         // before it).  Either way silu is the product's last factor: the same bits.
-        __shared__ float o_s[XPOSE ? kD : 1];
+        __shared__ float o_s[ONE_WAVE ? kD : 1];
         float sz = 0.f;
-        if constexpr (XPOSE) {
+        if constexpr (ONE_WAVE) {
             if (row_lane) o_s[row0 + lane] = o_keep;
             if (warp < kD / 32) sz = silu(z_l);
         }
@@ -292,7 +275,7 @@ decode_d128(const DecodeParams p)
         for (int r = 1; r < RPL; ++r) ss += __shfl_sync(kFull, o_sq, r * LPR);
         if (lane == 0) red[warp] = ss;
         __syncthreads();
-        if constexpr (XPOSE) {
+        if constexpr (ONE_WAVE) {
             if (warp >= kD / 32) return;       // no barrier follows on this path
         }
         float part[W];                         // pairwise sum of the warps' partials
@@ -303,7 +286,7 @@ decode_d128(const DecodeParams p)
 #pragma unroll
             for (int i = 0; i < n; ++i) part[i] += part[i + n];
         const float rstd = rsqrtf(part[0] * (1.0f / kD) + p.eps);
-        if constexpr (XPOSE) {
+        if constexpr (ONE_WAVE) {
             const int row = 32 * warp + lane;
             const float y = gn_l * o_s[row] * rstd * sz;
             if constexpr (EPI == kEpiBf16) {
@@ -487,11 +470,13 @@ cudaError_t launch_typed(const DecodeParams &p, bool fast, cudaStream_t s)
         decode_generic<TS, EPI, false><<<grid, kGenWarps * 32, 0, s>>>(p);
         return cudaGetLastError();
     }
-    // Early launch (grids of a few waves, see early_grid) with the first quarter of the head
-    // asked of the L2.  Measured on one layer at batch 32: a quarter -4.5 %; a half -6 %, but
-    // slower when host copies run beside the kernels; the whole head -3 %, slower still there.
+    // Early launch (grids of a few waves, see early_grid) with the first sixteenth of the head asked
+    // of the L2.  More is faster on its own but slower when host copies run beside the kernels:
+    // 48-layer step at batch 32, device-only / with per-layer host copies on a second stream, ms:
+    // a quarter 1.491 / 1.561, an eighth 1.501 / 1.544, a sixteenth 1.508 / 1.537, none 1.515 /
+    // 1.535 (with rows reduced one at a time a quarter had been best: 1.520 / 1.551).
     DecodeParams q = p;
-    q.pf_bytes = (unsigned)(kD * kD * sizeof(TS) / 4);
+    q.pf_bytes = (unsigned)(kD * kD * sizeof(TS) / 16);
     static_assert(kStagedMinCtasPerSm <= kEarlyMaxWaves * RegShape<float>::kMinBlocks,
                   "register-batched grids must stay within the early-launch waves");
     switch (pick_path<TS>(grid)) {
