@@ -54,16 +54,16 @@ REF_LAYERS_PER_STEP = 4      # oracle sample per step of the reference arm
 # dram__bytes_write.sum), valid only while the kernel source is the one it was taken on.
 NCU_TRAFFIC = {
     # mean of three mid-sequence launches of the full 48-layer workload, ncu --cache-control none
-    # (reads 102.8 MB, writes 96.6-99.8 MB), from the ncu capture of the batch-32 48-layer decode
-    "decode_norm_f32": {"bytes_per_launch": 201434965,
-                        "src_sha256": "11c70d442179d75d266dd086e41d94898ee942088de56d54a8f346715905f3df"},
-    # mean of two launches of the 256-slot fp16 pool decode (reads 407.2 MB, writes 401.1-403.0 MB)
-    "decode_norm_f16_pool": {"bytes_per_launch": 809197696,
-                             "src_sha256": "11c70d442179d75d266dd086e41d94898ee942088de56d54a8f346715905f3df"},
-    # mean of two launches of the batch-32 fp32 decode from projections (reads 105.8 MB, writes
-    # 102.6-104.3 MB), ncu --cache-control none
-    "conv_norm_f32": {"bytes_per_launch": 209281408, "src": ("gdn_conv_norm.cu", "gdn_internal.cuh"),
-                      "src_sha256": "61a0554729a214eb73b0eda023a7d81d6aa371f58cd23cd3dfb6f5779a63de8c"},
+    # (reads 102.8 MB, writes 96.7-99.8 MB), from the ncu capture of the batch-32 48-layer decode
+    "decode_norm_f32": {"bytes_per_launch": 201338539,
+                        "src_sha256": "d7ef0560d8c7516145aea11e87782e28b1a70a1a80d9dd698ca3c8112066c8e8"},
+    # mean of two launches of the 256-slot fp16 pool decode (reads 407.2-407.4 MB, writes 401.5-403.3 MB)
+    "decode_norm_f16_pool": {"bytes_per_launch": 809747200,
+                             "src_sha256": "d7ef0560d8c7516145aea11e87782e28b1a70a1a80d9dd698ca3c8112066c8e8"},
+    # mean of two launches of the batch-32 fp32 decode from projections (reads 105.8-105.9 MB, writes
+    # 102.8-104.3 MB), ncu --cache-control none
+    "conv_norm_f32": {"bytes_per_launch": 209422848, "src": ("gdn_conv_norm.cu", "gdn_internal.cuh"),
+                      "src_sha256": "991c5e322697d68f73e5a6a2a814c7162e42213e32d33b2904ca68f9be87a61e"},
 }
 
 

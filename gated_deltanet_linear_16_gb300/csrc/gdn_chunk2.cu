@@ -112,6 +112,13 @@ chunk2_d128(const DecodeParams p)
     }
 
     float o_keep[2] = {0.f, 0.f};
+    // fp32: LPB rows at once (a commit group or a register batch), token after token: u and w of the
+    // rows by one reduce-scatter over the row's lanes (the butterfly's sums bit for bit, as in the
+    // single-token kernel), the rows' coefficients broadcast back; token 1 continues from the state
+    // as stored after token 0.  fp16 (64 registers a thread, with both tokens' k and q, hold no group
+    // of rows): a row at a time, a butterfly per sum -- a one-row group measured 1.4 % slower (its
+    // shuffles form one longer chain instead of two interleaved ones).
+    constexpr int G = sizeof(TS) == 4 ? LPB : 1;
     auto row_steps = [&](const uint4 packed_in, const int i) {   // both tokens on state row slice i
             float s[EPV];
             V::unpack(packed_in, s);
@@ -145,6 +152,52 @@ chunk2_d128(const DecodeParams p)
                 }
             }
     };
+    auto group_steps = [&](const uint4 (&vec)[G], const int i0) {
+        constexpr int R = LPR / (2 * G);
+        static_assert(R >= 1 && (G == 1 || G == LPB), "a group's 2 G values over the LPR lanes of a row");
+        float s[G][EPV];                                     // the rows, unpacked once
+#pragma unroll
+        for (int ii = 0; ii < G; ++ii) V::unpack(vec[ii], s[ii]);
+        const int vi = (lane % LPR) / (2 * R);               // the vector (row) these lanes reduce
+        const bool is_w = ((lane % LPR) / R) & 1;
+        const int gbase = lane & ~(LPR - 1);
+        const int vr = lane / RPL - i0;                      // lane r < RPW keeps row r's o
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            float part[2 * G];
+#pragma unroll
+            for (int ii = 0; ii < G; ++ii) {
+                float u = 0.f, w = 0.f;
+#pragma unroll
+                for (int j = 0; j < EPV; ++j) { u = fmaf(s[ii][j], kx[t][j], u); w = fmaf(s[ii][j], qx[t][j], w); }
+                part[2 * ii] = u;
+                part[2 * ii + 1] = w;
+            }
+            const float mine_sum = reduce_scatter<LPR, 2 * G>(part, lane);
+            const float other = __shfl_xor_sync(kFull, mine_sum, R);
+            const float u = is_w ? other : mine_sum, w = is_w ? mine_sum : other;
+            const float va = __shfl_sync(kFull, v_l[t], (i0 + vi) * RPL + sub);
+            const float coef = beta[t] * (va - alpha[t] * u);
+            const float oa = (alpha[t] * w + coef * kq[t]) * p.inv_sqrt_d;
+            float cf[G];
+#pragma unroll
+            for (int ii = 0; ii < G; ++ii) cf[ii] = __shfl_sync(kFull, coef, gbase + 2 * R * ii);
+            const float ok = __shfl_sync(kFull, oa, (lane % RPL) * LPR + (vr & (G - 1)) * 2 * R);
+            if (lane < RPW && vr >= 0 && vr < G) o_keep[t] = ok;
+#pragma unroll
+            for (int ii = 0; ii < G; ++ii) {
+#pragma unroll
+                for (int j = 0; j < EPV; ++j) s[ii][j] = fmaf(cf[ii], kx[t][j], alpha[t] * s[ii][j]);
+                const uint4 packed = V::pack(s[ii]);
+                if (t == 0) {
+                    st_stream16(midp + (int64_t)(i0 + ii) * RPL * kD, packed);
+                    V::unpack(packed, s[ii]);        // continue from the stored (rounded) state
+                } else {
+                    st_stream16(rowp + (int64_t)(i0 + ii) * RPL * kD, packed);
+                }
+            }
+        }
+    };
 #pragma unroll
     for (int bt = 0; bt < NBAT; ++bt) {
         if constexpr (STAGED) {
@@ -152,16 +205,27 @@ chunk2_d128(const DecodeParams p)
             else if (bt == 1) cp_async_wait<kGroups - 2>();
             else if (bt == 2) cp_async_wait<kGroups - 3>();
             else cp_async_wait<0>();
+            if constexpr (G > 1) {
+                uint4 vec[G];
 #pragma unroll
-            for (int ii = 0; ii < LPB; ++ii) row_steps(mine[(bt * LPB + ii) * RPL * VPR], bt * LPB + ii);
+                for (int ii = 0; ii < G; ++ii) vec[ii] = mine[(bt * LPB + ii) * RPL * VPR];
+                group_steps(vec, bt * LPB);
+            } else {
+#pragma unroll
+                for (int ii = 0; ii < LPB; ++ii) row_steps(mine[(bt * LPB + ii) * RPL * VPR], bt * LPB + ii);
+            }
         } else {
             if (bt + 1 < NBAT) {
 #pragma unroll
                 for (int i = 0; i < LPB; ++i)
                     raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * LPB + i) * RPL * kD);
             }
+            if constexpr (G > 1) {
+                group_steps(raw[bt & 1], bt * LPB);
+            } else {
 #pragma unroll
-            for (int ii = 0; ii < LPB; ++ii) row_steps(raw[bt & 1][ii], bt * LPB + ii);
+                for (int ii = 0; ii < LPB; ++ii) row_steps(raw[bt & 1][ii], bt * LPB + ii);
+            }
         }
     }
     if (row_lane) {

@@ -268,7 +268,11 @@ conv_norm_d128(const ConvNormParams p)
     for (int j = 0; j < EPV; ++j) kq = fmaf(kx[j], qx[j], kq);
     kq = group_sum<LPR>(kq);
 
-    // 4. the step, as in the decode kernel
+    // 4. the step, as in the decode kernel.  fp32: PER rows at once (a commit group or register batch),
+    // u and w by one reduce-scatter over the row's lanes (the butterfly's sums bit for bit), then the
+    // rows' coefficients broadcast back; fp16 (48 registers a thread hold no group of rows): a row at a
+    // time, a butterfly per sum
+    constexpr int G = sizeof(TS) == 4 ? PER : 1;
     float o_keep = 0.f;
     auto row_step = [&](const uint4 packed, const int i) {
         float s[EPV];
@@ -292,6 +296,46 @@ conv_norm_d128(const ConvNormParams p)
                 const float orr = __shfl_sync(kFull, oa, r * LPR);
                 if (lane == i * RPL + r) o_keep = orr;
             }
+        }
+    };
+    auto group_step = [&](const uint4 (&vec)[G], const int i0) {
+        constexpr int R = LPR / (2 * G);
+        static_assert(R >= 1 && (G == 1 || G == PER), "a group's 2 G values over the LPR lanes of a row");
+        float part[2 * G];
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            float s[EPV];
+            V::unpack(vec[i], s);
+            float u = 0.f, w = 0.f;
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) { u = fmaf(s[j], kx[j], u); w = fmaf(s[j], qx[j], w); }
+            part[2 * i] = u;
+            part[2 * i + 1] = w;
+        }
+        const float mine_sum = reduce_scatter<LPR, 2 * G>(part, lane);
+        const float other = __shfl_xor_sync(kFull, mine_sum, R);
+        const bool is_w = ((lane % LPR) / R) & 1;
+        const float u = is_w ? other : mine_sum, w = is_w ? mine_sum : other;
+        const int vi = (lane % LPR) / (2 * R);               // the vector (row) these lanes reduced
+        const float va = __shfl_sync(kFull, v_l, (i0 + vi) * RPL + sub);
+        const float coef = beta * (va - alpha * u);
+        const float oa = (alpha * w + coef * kq) * p.inv_sqrt_d;
+        const int gbase = lane & ~(LPR - 1);
+        float cf[G];
+#pragma unroll
+        for (int i = 0; i < G; ++i) cf[i] = __shfl_sync(kFull, coef, gbase + 2 * R * i);
+        {   // lane r < kRowsPerWarp keeps the o of row r: vector r / RPL of row group r % RPL
+            const int vr = lane / RPL - i0;
+            const float ok = __shfl_sync(kFull, oa, (lane % RPL) * LPR + (vr & (G - 1)) * 2 * R);
+            if (lane < kRowsPerWarp && vr >= 0 && vr < G) o_keep = ok;
+        }
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            float s[EPV];
+            V::unpack(vec[i], s);
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) s[j] = fmaf(cf[i], kx[j], alpha * s[j]);
+            st_stream16(rowp + (int64_t)(i0 + i) * RPL * kD, V::pack(s));
         }
     };
     // This CTA's reads of the key head's q/k ring rows ended at the __syncthreads after step 3.  It
@@ -318,8 +362,15 @@ conv_norm_d128(const ConvNormParams p)
             else if (bt == 2) cp_async_wait<kGroups - 3>();
             else cp_async_wait<0>();
             count_reader(bt);
+            if constexpr (G > 1) {
+                uint4 vec[G];
 #pragma unroll
-            for (int ii = 0; ii < PER; ++ii) row_step(mine[(bt * PER + ii) * RPL * VPR], bt * PER + ii);
+                for (int ii = 0; ii < G; ++ii) vec[ii] = mine[(bt * PER + ii) * RPL * VPR];
+                group_step(vec, bt * PER);
+            } else {
+#pragma unroll
+                for (int ii = 0; ii < PER; ++ii) row_step(mine[(bt * PER + ii) * RPL * VPR], bt * PER + ii);
+            }
         } else {
             if (bt + 1 < NBAT) {
 #pragma unroll
@@ -327,8 +378,12 @@ conv_norm_d128(const ConvNormParams p)
                     raw[(bt + 1) & 1][i] = ld_stream16(rowp + (int64_t)((bt + 1) * PER + i) * RPL * kD);
             }
             count_reader(bt);
+            if constexpr (G > 1) {
+                group_step(raw[bt & 1], bt * PER);
+            } else {
 #pragma unroll
-            for (int ii = 0; ii < PER; ++ii) row_step(raw[bt & 1][ii], bt * PER + ii);
+                for (int ii = 0; ii < PER; ++ii) row_step(raw[bt & 1][ii], bt * PER + ii);
+            }
         }
     }
 

@@ -163,15 +163,13 @@ decode_d128(const DecodeParams p)
     float o_sq = 0.f;                          // sum of o^2 over the rows of this lane's row group
     // A group of PER vectors (a commit group, a register batch, or on the one-wave path all of the
     // lane's rows) at once: the partial dot products of its rows, then one reduce-scatter over the row
-    // group's lanes with the butterfly's partners and order (offsets LPR/2 .. 1), so each sum is
-    // group_sum's bit for bit.  A level halves the values a lane carries (while more than one is
-    // left): the lane keeps the half its partner gives away and adds the partner's copy.  After it,
-    // the R = LPR / (2 PER) lanes of block m of the group hold value m: u (m even) or w (m odd) of
-    // vector m / 2.  2 PER shuffles instead of 2 PER log2(LPR), and one chain of log2(LPR) levels
-    // instead of one per row (measured at batch 1: ~310 cycles a row, one row after another).
+    // group's lanes (reduce_scatter: the butterfly's sums bit for bit), after which the R = LPR /
+    // (2 PER) lanes of block m of the group hold value m: u (m even) or w (m odd) of vector m / 2.
+    // About 2 shuffles a row instead of 2 log2(LPR), and one chain of log2(LPR) levels a group
+    // instead of one a row (measured at batch 1: ~310 cycles a row, one row after another).
     auto group_step = [&](const uint4 (&vec)[PER], const int i0) {
         constexpr int R = LPR / (2 * PER);
-        static_assert(R >= 1 && (PER & (PER - 1)) == 0, "a group's 2 PER values over the LPR lanes of a row");
+        static_assert(R >= 1, "a group's 2 PER values over the LPR lanes of a row");
         float part[2 * PER];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
@@ -183,24 +181,10 @@ decode_d128(const DecodeParams p)
             part[2 * i] = u;
             part[2 * i + 1] = w;
         }
-#pragma unroll
-        for (int lvl = 0; (LPR >> (lvl + 1)) > 0; ++lvl) {
-            const int off = LPR >> (lvl + 1), half = (2 * PER) >> (lvl + 1);
-            if (half > 0) {
-                const bool upper = (lane & off) != 0;
-#pragma unroll
-                for (int j = 0; j < half; ++j) {
-                    const float keep = upper ? part[j + half] : part[j];
-                    const float send = upper ? part[j] : part[j + half];
-                    part[j] = keep + __shfl_xor_sync(kFull, send, off);
-                }
-            } else {
-                part[0] += __shfl_xor_sync(kFull, part[0], off);
-            }
-        }
-        const float other = __shfl_xor_sync(kFull, part[0], R);
+        const float mine_sum = reduce_scatter<LPR, 2 * PER>(part, lane);
+        const float other = __shfl_xor_sync(kFull, mine_sum, R);
         const bool is_w = ((lane % LPR) / R) & 1;
-        const float u = is_w ? other : part[0], w = is_w ? part[0] : other;
+        const float u = is_w ? other : mine_sum, w = is_w ? mine_sum : other;
         const int vi = (lane % LPR) / (2 * R);               // the vector (row) these lanes reduced
         const float va = __shfl_sync(kFull, v_l, (i0 + vi) * RPL + sub);
         const float coef = beta * (va - alpha * u);

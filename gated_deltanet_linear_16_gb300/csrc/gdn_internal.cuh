@@ -222,6 +222,34 @@ __device__ __forceinline__ float group_sum(float x) {
     return x;
 }
 
+// The sums of NVAL values at once, each spread over the same W lanes (part[j] on every lane of the
+// group: e.g. u and w of several rows, partial over the lanes' columns): a reduce-scatter with the
+// butterfly's partners and order (offsets W/2 .. 1), so every sum is group_sum<W>'s bit for bit.
+// While a lane carries more than one value, a level halves them: the lane keeps the half its partner
+// gives away and adds the partner's copy; the remaining levels are plain butterfly steps.  NVAL - 1
+// + log2(W / NVAL) shuffles instead of NVAL log2(W), in one chain of log2(W) levels.  Returns the sum
+// this lane ends with: value (lane % W) / (W / NVAL), held by W / NVAL consecutive lanes.
+template <int W, int NVAL>
+__device__ __forceinline__ float reduce_scatter(float (&part)[NVAL], int lane) {
+    static_assert(NVAL <= W && (NVAL & (NVAL - 1)) == 0 && (W & (W - 1)) == 0, "NVAL values over W lanes");
+#pragma unroll
+    for (int lvl = 0; (W >> (lvl + 1)) > 0; ++lvl) {
+        const int off = W >> (lvl + 1), half = NVAL >> (lvl + 1);
+        if (half > 0) {
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int j = 0; j < half; ++j) {
+                const float keep = upper ? part[j + half] : part[j];
+                const float send = upper ? part[j] : part[j + half];
+                part[j] = keep + __shfl_xor_sync(kFull, send, off);
+            }
+        } else {
+            part[0] += __shfl_xor_sync(kFull, part[0], off);
+        }
+    }
+    return part[0];
+}
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
 __device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
