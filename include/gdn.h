@@ -23,7 +23,11 @@
  * - Memory: every pointer is a DEVICE pointer to memory the caller owns.  The
  *   library allocates nothing, keeps no per-call state, and updates the state
  *   in place.  Calls are asynchronous on `stream` (a cudaStream_t passed as
- *   void*; NULL is the legacy default stream); the caller synchronises.
+ *   void*; NULL is the legacy default stream); the caller synchronises.  The
+ *   outputs of the gdn_decode* calls (o, out, and the int8 codes, scales and
+ *   y) may also be pinned host memory, which the kernels then write directly
+ *   over the host link (the same results; complete, like any output, when the
+ *   call's work in the stream is); everything else should be device memory.
  * - State layout: sequence b's slot starts `b * state_pitch` ELEMENTS after
  *   `state`; inside a slot, head h is a contiguous D x D row-major block at
  *   `h * D * D`, row a = value index, column c = key index.  state_pitch >=

@@ -105,3 +105,70 @@ def test_rejected_call_raises_and_touches_nothing():
     assert e.value.status == 4           # output inside the state
     torch.cuda.synchronize()
     assert torch.equal(before, st.raw)
+
+
+@pytest.mark.parametrize("norm", [True, False])
+@pytest.mark.parametrize("B", [1, 32])
+def test_outputs_in_pinned_host_memory(B, norm):
+    """Outputs may live in pinned host memory, which the kernels write directly over the host link (as
+    the end-to-end benchmark does): the same bits as outputs in device memory, from the same state and
+    inputs.  B = 1 runs the one-wave decode_d128 (16 warps, norm finished by four warps), B = 32 the
+    staged one."""
+    NK, NV, D = 16, 48, 128
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(900 + B)
+    st = torch.randn((B, NV, D, D), device=dev, generator=g) * 0.02
+    q = torch.nn.functional.normalize(torch.randn((B, NK, D), device=dev, generator=g), dim=-1).reshape(B, NK * D)
+    k = torch.nn.functional.normalize(torch.randn((B, NK, D), device=dev, generator=g), dim=-1).reshape(B, NK * D)
+    v = torch.randn((B, NV * D), device=dev, generator=g)
+    z = torch.randn((B, NV * D), device=dev, generator=g)
+    a = torch.sigmoid(torch.randn((B, NV), device=dev, generator=g) + 2.0)
+    b = torch.sigmoid(torch.randn((B, NV), device=dev, generator=g))
+    gn = 1.0 + 0.1 * torch.randn(D, device=dev, generator=g)
+    dt = torch.int16 if norm else torch.float32
+    outs, states = [], []
+    for host in (False, True):
+        s = st.clone()
+        out = torch.full((B, NV * D), -1, dtype=dt).pin_memory() if host else torch.full((B, NV * D), -1, dtype=dt, device=dev)
+        if norm:
+            gdn.gdn_decode_norm(s, q, k, v, a, b, z, gn, out, batch=B, nk=NK, nv=NV, d=D, eps=1e-6)
+        else:
+            gdn.gdn_decode(s, q, k, v, a, b, out, batch=B, nk=NK, nv=NV, d=D)
+        torch.cuda.synchronize()
+        outs.append(out.cpu())
+        states.append(s)
+    assert torch.equal(outs[0].view(torch.int16 if norm else torch.int32), outs[1].view(torch.int16 if norm else torch.int32))
+    assert torch.equal(states[0].view(torch.int32), states[1].view(torch.int32))
+    assert not torch.equal(outs[1], torch.full_like(outs[1], -1)), "nothing written"
+
+
+@pytest.mark.parametrize("B", [1, 32])
+def test_int8_outputs_in_pinned_host_memory(B):
+    """The int8 epilogue's codes, scales and fp32 y written into pinned host memory: the same bits as
+    into device memory (B = 1: one warp per group of 32 on the one-wave path; B = 32: staged)."""
+    NK, NV, D = 16, 48, 128
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(950 + B)
+    st = torch.randn((B, NV, D, D), device=dev, generator=g) * 0.02
+    q = torch.nn.functional.normalize(torch.randn((B, NK, D), device=dev, generator=g), dim=-1).reshape(B, NK * D)
+    k = torch.nn.functional.normalize(torch.randn((B, NK, D), device=dev, generator=g), dim=-1).reshape(B, NK * D)
+    v = torch.randn((B, NV * D), device=dev, generator=g)
+    z = torch.randn((B, NV * D), device=dev, generator=g)
+    a = torch.sigmoid(torch.randn((B, NV), device=dev, generator=g) + 2.0)
+    b = torch.sigmoid(torch.randn((B, NV), device=dev, generator=g))
+    gn = 1.0 + 0.1 * torch.randn(D, device=dev, generator=g)
+    res = []
+    for host in (False, True):
+        s = st.clone()
+        mk = (lambda *shape, dtype: torch.full(shape, -1, dtype=dtype).pin_memory()) if host else \
+             (lambda *shape, dtype: torch.full(shape, -1, dtype=dtype, device=dev))
+        xq, xs, y = mk(B, NV * D, dtype=torch.int8), mk(B, NV * D // 32, dtype=torch.float32), mk(B, NV * D, dtype=torch.float32)
+        gdn.gdn_decode_norm_q8(s, q, k, v, a, b, z, gn, xq, xs, y, batch=B, nk=NK, nv=NV, d=D, eps=1e-6)
+        torch.cuda.synchronize()
+        res.append((xq.cpu(), xs.cpu().view(torch.int32), y.cpu().view(torch.int32), s))
+    for i in range(3):
+        assert torch.equal(res[0][i], res[1][i])
+    assert torch.equal(res[0][3].view(torch.int32), res[1][3].view(torch.int32))
+    assert not torch.equal(res[1][0], torch.full_like(res[1][0], -1)), "nothing written"
