@@ -172,3 +172,33 @@ def test_int8_outputs_in_pinned_host_memory(B):
         assert torch.equal(res[0][i], res[1][i])
     assert torch.equal(res[0][3].view(torch.int32), res[1][3].view(torch.int32))
     assert not torch.equal(res[1][0], torch.full_like(res[1][0], -1)), "nothing written"
+
+
+@pytest.mark.parametrize("f16", [False, True])
+def test_load_paths_bitwise_identical(f16):
+    """The same heads (sequence 0's state and inputs) stepped inside grids of 48, 384 and 1920 CTAs: the
+    one-wave path (a lane's 8 rows in one reduce-scatter), register batches (fp32) or staging (fp16),
+    and staging at many waves (4 rows a group) give the same raw o and new state bit for bit, since
+    every reduction keeps the butterfly's association."""
+    NK, NV, D = 16, 48, 128
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    Bmax = 40
+    dt = torch.float16 if f16 else torch.float32
+    st = (torch.randn((Bmax, NV, D, D), device=dev, generator=g) * 0.02).to(dt)
+    q = torch.nn.functional.normalize(torch.randn((Bmax, NK, D), device=dev, generator=g), dim=-1).reshape(Bmax, NK * D)
+    k = torch.nn.functional.normalize(torch.randn((Bmax, NK, D), device=dev, generator=g), dim=-1).reshape(Bmax, NK * D)
+    v = torch.randn((Bmax, NV * D), device=dev, generator=g)
+    a = torch.sigmoid(torch.randn((Bmax, NV), device=dev, generator=g) + 2.0)
+    b = torch.sigmoid(torch.randn((Bmax, NV), device=dev, generator=g))
+    res = []
+    for B in (1, 8, Bmax):
+        s = st[:B].clone()
+        o = torch.empty((B, NV * D), device=dev)
+        gdn.gdn_decode(s, q[:B], k[:B], v[:B], a[:B], b[:B], o, batch=B, nk=NK, nv=NV, d=D)
+        torch.cuda.synchronize()
+        res.append((o[0].view(torch.int32).clone(), s[0].view(torch.int16 if f16 else torch.int32).clone()))
+    for o_, s_ in res[1:]:
+        assert torch.equal(o_, res[0][0]), "raw o differs between load paths"
+        assert torch.equal(s_, res[0][1]), "state differs between load paths"
